@@ -1,0 +1,209 @@
+/*
+ * moe.h -- C ABI of libmoe, a single-GPU (sm_103a) Mixture-of-Experts
+ * feed-forward layer.
+ *
+ * The layer is the one described on "NPU HunyuanImage-3.0模型推理优化实践"
+ * (HunyuanImage-3.0 inference on Ascend, cf-1.com/news/2296994):
+ *   RMSNorm ("RmsNorm算子优化") -> fp32 gate ("消除gate计算冗余cast算子")
+ *   -> GatingTopK ("MoE EP优化") -> init_routing / compute_expert_tokens
+ *   ("GMM使能&&Routing优化") -> grouped matmul over the merged gate/up weight
+ *   w13 with SwiGLU ("MoE TP优化 / 计算分解") -> grouped down matmul
+ *   -> finalize_routing ("GMM使能&&Routing优化"), plus an optional shared
+ *   expert ("MoE多流并行优化").
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer into memory the caller owns.
+ *     The library never allocates, frees or synchronises: each call only
+ *     enqueues kernels on `stream` (NULL = the legacy default stream) and
+ *     returns.  Outputs are valid once the caller has synchronised.
+ *   - All tensors are dense, row-major, contiguous.  bf16 values are passed
+ *     as their 16-bit patterns (moe_bf16_t).  Unless stated otherwise every
+ *     pointer must be 16-byte aligned.
+ *   - The return value reports host-side argument checks and launch errors;
+ *     nothing is enqueued when it is not MOE_OK.  Errors that only the
+ *     device can see are OR-ed as MOE_DEV_* bits into *dev_status (a device
+ *     int32 the caller zeroes beforehand; NULL = not reported).  A kernel
+ *     that detects one writes nothing out of bounds and returns early; the
+ *     outputs of that call are then undefined.
+ *   - Sizes: 1 <= k <= min(E, 32), E <= 1024, T*k < 2^31, H % 64 == 0,
+ *     I % 128 == 0 (I_shared likewise).  Inputs must be finite.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16_t;            /* bfloat16 bit pattern */
+typedef struct CUstream_st *moe_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,        /* null pointer, bad size or misalignment */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* sizes outside the limits above */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 3,
+    MOE_ERR_CUDA = 4,               /* a CUDA runtime/launch error */
+    MOE_ERR_NO_DEVICE = 5           /* no sm_100-family GPU is current */
+} moe_status_t;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+enum {
+    MOE_DEV_BAD_EXPERT_ID = 1,      /* an expert id outside [0, E) */
+    MOE_DEV_TIMEOUT = 2,            /* a pipeline wait ran past its limit */
+    MOE_DEV_BAD_OFFSETS = 4,        /* group offsets not monotone / out of range */
+    MOE_DEV_UNSORTED = 8            /* moe_expert_tokens input not sorted */
+};
+
+/* flags */
+enum {
+    MOE_RENORM = 1u << 0,      /* renormalise the top-k weights to sum 1 */
+    MOE_RMSNORM = 1u << 1,     /* RMSNorm before the gate */
+    MOE_SHARED = 1u << 2,      /* add the shared expert */
+    MOE_OUT_F32 = 1u << 3,     /* layer / finalize output in fp32 (else bf16) */
+    MOE_SHARED_F32 = 1u << 4   /* finalize: `shared` is fp32 (else bf16) */
+};
+
+typedef struct {
+    int32_t T;          /* tokens */
+    int32_t H;          /* hidden size */
+    int32_t E;          /* routed experts */
+    int32_t k;          /* experts per token */
+    int32_t I;          /* routed expert intermediate size */
+    int32_t I_shared;   /* shared expert intermediate size (MOE_SHARED) */
+    float rms_eps;      /* RMSNorm epsilon (MOE_RMSNORM) */
+    uint32_t flags;     /* MOE_RENORM | MOE_RMSNORM | MOE_SHARED | MOE_OUT_F32 */
+} moe_desc_t;
+
+/* Human-readable name of a moe_status_t value. */
+const char *moe_status_string(int status);
+
+/*
+ * RMSNorm and fp32 gate ("RmsNorm算子优化"; "消除gate计算冗余cast算子":
+ * the gate is an fp32 linear layer on the hidden states cast to float).
+ *   x      [T, H] bf16
+ *   gamma  [H] bf16, or NULL for all ones (used with MOE_RMSNORM only)
+ *   wg     [E, H] fp32 gate weight
+ *   gate_bias [E] fp32 per-expert logit offset, or NULL
+ *   xn     [T, H] bf16 out: bf16((x * r) * gamma), r = 1/sqrt(mean(x^2)+eps)
+ *          with the sum of squares taken in fp32 in ascending h.  Required
+ *          with MOE_RMSNORM, ignored (may be NULL) without it.
+ *   logits [T, E] fp32 out: fp32 dot product of the (normalised) row with
+ *          wg[e], one fused multiply-add per term in ascending h, plus
+ *          gate_bias[e].  These are bit-identical to the same steps done
+ *          sequentially on any IEEE fp32 machine.
+ * flags: MOE_RMSNORM.  T may be 0.
+ */
+moe_status_t moe_rmsnorm_gate(const moe_bf16_t *x, const moe_bf16_t *gamma,
+                              const float *wg, const float *gate_bias, int32_t T,
+                              int32_t H, int32_t E, float eps, uint32_t flags,
+                              moe_bf16_t *xn, float *logits, moe_stream_t stream);
+
+/*
+ * GatingTopK ("MoE EP优化"): per token, the k largest logits (descending;
+ * equal logits, -0 == +0, go to the lower expert index) and their softmax
+ * probabilities, renormalised over the k chosen with MOE_RENORM.
+ *   logits   [T, E] fp32 in
+ *   topk_idx [T, k] int32 out (slot 0 = largest)
+ *   topk_w   [T, k] fp32 out
+ */
+moe_status_t moe_gate_topk(const float *logits, int32_t T, int32_t E, int32_t k,
+                           uint32_t flags, int32_t *topk_idx, float *topk_w,
+                           moe_stream_t stream);
+
+/*
+ * init_routing ("GMM使能&&Routing优化": sort the tokens by expert).
+ * Assignment a = t*k + j goes to expert topk_idx[a]; rows are ordered by
+ * expert and, within an expert, by a (a stable counting sort):
+ *   counts[e] = #assignments to e;  offsets[0..E] = exclusive scan, offsets[E] = T*k
+ *   expanded_row_idx[a] = offsets[e] + #{a' < a : topk_idx[a'] == e}
+ *   src_token[r]        = token of the assignment placed in row r
+ *   sorted_expert_ids[r]= expert of row r (may be NULL)
+ *   expanded_x[r]       = x[src_token[r]]  ([T*k, H] bf16; may be NULL
+ *                         to build the indices only, then x may be NULL too)
+ * Workspace: moe_init_routing_workspace_size() bytes, 256-byte aligned.
+ * Bad expert ids set MOE_DEV_BAD_EXPERT_ID; those assignments get no row.
+ */
+moe_status_t moe_init_routing_workspace_size(int32_t T, int32_t k, int32_t E,
+                                             size_t *bytes);
+moe_status_t moe_init_routing(const int32_t *topk_idx, const moe_bf16_t *x, int32_t T,
+                              int32_t H, int32_t E, int32_t k, moe_bf16_t *expanded_x,
+                              int32_t *expanded_row_idx, int32_t *src_token,
+                              int32_t *sorted_expert_ids, int32_t *counts,
+                              int32_t *offsets, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * compute_expert_tokens ("GMM使能&&Routing优化": how many tokens each expert
+ * computes), from the expert ids of the sorted rows:
+ *   sorted_expert_ids [n] int32, ascending
+ *   counts [E], offsets [E+1] (offsets[e] = first row of expert e)
+ * An unsorted input sets MOE_DEV_UNSORTED, an id outside [0,E)
+ * MOE_DEV_BAD_EXPERT_ID.  n may be 0.
+ */
+moe_status_t moe_expert_tokens(const int32_t *sorted_expert_ids, int32_t n, int32_t E,
+                               int32_t *counts, int32_t *offsets, int32_t *dev_status,
+                               moe_stream_t stream);
+
+/*
+ * Grouped expert FFN ("GMM使能&&Routing优化": one grouped matmul for all
+ * experts; "MoE TP优化 / 计算分解": x = down(SiLU(gate(x)) * up(x)), gate and
+ * up merged into w13, SwiGLU = SiLU(first half) * second half).
+ *   expanded_x [n, H] bf16, rows sorted by group
+ *   offsets    [G+1] int32 device: group g owns rows [offsets[g], offsets[g+1])
+ *   w13        [G, 2I, H] bf16: rows 0..I-1 gate, I..2I-1 up
+ *   w2         [G, H, I] bf16
+ *   act        [n, I] bf16 out: bf16(SiLU(g) * u), g/u accumulated in fp32
+ *   y          [n, H] bf16 out: bf16(act . w2[g]^T), fp32 accumulation
+ * Rows past offsets[G] are left untouched.  Both matmuls run on the 5th
+ * generation tensor cores (tcgen05, TMEM accumulators, TMA operand loads).
+ */
+moe_status_t moe_grouped_mlp(const moe_bf16_t *expanded_x, const int32_t *offsets,
+                             int32_t G, const moe_bf16_t *w13, const moe_bf16_t *w2,
+                             int32_t n, int32_t H, int32_t I, moe_bf16_t *act,
+                             moe_bf16_t *y, int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * finalize_routing ("GMM使能&&Routing优化": put the expert outputs back in
+ * token order and form the weighted sum) plus the shared expert
+ * ("MoE多流并行优化"):
+ *   out[t, :] = sum_{j=0..k-1} topk_w[t, j] * y_exp[expanded_row_idx[t*k+j], :]
+ *               + shared[t, :]
+ * summed in fp32 in slot order j = 0..k-1, the shared term last; no atomics,
+ * so the result is deterministic.
+ *   y_exp [T*k, H] bf16; expanded_row_idx [T*k]; topk_w [T, k] fp32
+ *   shared [T, H] bf16 (fp32 with MOE_SHARED_F32) or NULL
+ *   out [T, H] bf16 (fp32 with MOE_OUT_F32)
+ */
+moe_status_t moe_finalize_routing(const moe_bf16_t *y_exp, const int32_t *expanded_row_idx,
+                                  const float *topk_w, const void *shared, int32_t T,
+                                  int32_t H, int32_t k, uint32_t flags, void *out,
+                                  moe_stream_t stream);
+
+/*
+ * The whole layer, every step above on `stream` with no host synchronisation:
+ *   x [T,H] bf16; gamma [H] bf16 or NULL (MOE_RMSNORM); wg [E,H] fp32;
+ *   gate_bias [E] fp32 or NULL; w13 [E,2I,H], w2 [E,H,I] bf16;
+ *   w13_s [2I_s,H], w2_s [H,I_s] bf16 (MOE_SHARED, else NULL);
+ *   out [T,H] bf16 (fp32 with MOE_OUT_F32).
+ * The shared expert runs on the normalised rows with weight 1 and its output
+ * enters the final sum in fp32.  Workspace: moe_layer_workspace_size() bytes,
+ * 256-byte aligned; its contents are scratch.
+ */
+moe_status_t moe_layer_workspace_size(const moe_desc_t *desc, size_t *bytes);
+moe_status_t moe_layer_forward(const moe_desc_t *desc, const moe_bf16_t *x,
+                               const moe_bf16_t *gamma, const float *wg,
+                               const float *gate_bias, const moe_bf16_t *w13,
+                               const moe_bf16_t *w2, const moe_bf16_t *w13_s,
+                               const moe_bf16_t *w2_s, void *out, void *workspace,
+                               size_t workspace_bytes, int32_t *dev_status,
+                               moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

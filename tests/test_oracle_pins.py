@@ -1,0 +1,342 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each pin checks the oracle against a value worked by hand from the page
+("NPU HunyuanImage-3.0模型推理优化实践", sections 'MoE TP优化 / 计算分解',
+'MoE EP优化', 'GMM使能&&Routing优化', 'RmsNorm算子优化',
+'消除gate计算冗余cast算子'), a closed form, an invariant, a library routine
+on a special case, or brute force on tiny inputs.  ``test_mutants_are_caught``
+plants plausible mistakes in temporary copies of the oracle source and checks
+that every one of them fails at least one pin.
+"""
+import json
+import math
+import os
+import shutil
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit, softmax
+
+import oracle
+from moe_inputs import WORKLOADS, make_inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f32_to_bf16_bits(a):
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_f64(bits):
+    return oracle.bits_to_float(bits).astype(np.float64)
+
+
+# --------------------------------------------------------------------- pins
+def pin_bf16_rounding():
+    # hand values: 1 + 2^-8 is a tie between 1 and 1 + 2^-7 -> even (1.0);
+    # 1 + 3*2^-8 ties between 1+2^-7 (odd) and 1+2^-6 (even) -> 1+2^-6;
+    # 1 + 2^-8 + 2^-40 is above the tie -> 1 + 2^-7 (a float detour would
+    # round twice and give 1.0).
+    got = oracle.bf16_bits([1.0, 1 + 2**-8, 1 + 3 * 2**-8, 1 + 2**-8 + 2**-40,
+                            -2.5, 0.0, 3.0e38, 3.4e38])
+    assert list(got[:6]) == [0x3F80, 0x3F80, 0x3F82, 0x3F81, 0xC020, 0x0000], got
+    # 3.0e38 = 1.7632 * 2^127 -> mantissa 97.69/128 -> 98 -> 0x7F62;
+    # 3.4e38 lies above the midpoint between the largest bf16 and 2^128 -> inf
+    assert got[6] == 0x7F62 and got[7] == 0x7F80, got
+    # library routine: torch's fp32 -> bf16 conversion rounds to nearest even
+    rng = np.random.default_rng(0)
+    v = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    assert np.array_equal(oracle.bf16_bits(v.astype(np.float64)), f32_to_bf16_bits(v))
+
+
+def pin_rmsnorm():
+    rng = np.random.default_rng(1)
+    T, H = 8, 256
+    gamma = f32_to_bf16_bits(1 + 0.1 * rng.standard_normal(H))
+    # constant row 2: mean(x^2) = 4, r = 1/sqrt(4 + eps) ~ 0.5, so x*r rounds
+    # to 1 in bf16 and xn = gamma exactly
+    x = np.full((1, H), 0x4000, dtype=np.uint16)   # bf16 2.0
+    assert np.array_equal(oracle.rmsnorm(x, gamma, 1e-6)[0], gamma)
+    # with eps = 0, scaling x by a power of two leaves xn bit-identical
+    x = f32_to_bf16_bits(rng.standard_normal((T, H)))
+    x4 = f32_to_bf16_bits(bits_f64(x) * 4.0)
+    assert np.array_equal(oracle.rmsnorm(x, gamma, 0.0), oracle.rmsnorm(x4, gamma, 0.0))
+    # library routine: torch rms_norm in fp32, within one bf16 ulp
+    xt = torch.from_numpy(bits_f64(x).astype(np.float32))
+    gt = torch.from_numpy(bits_f64(gamma).astype(np.float32))
+    ref = torch.nn.functional.rms_norm(xt, (H,), gt, eps=1e-6).to(torch.float64).numpy()
+    got = bits_f64(oracle.rmsnorm(x, gamma, 1e-6))
+    ulp = np.abs(ref) * 2.0**-7
+    assert np.all(np.abs(got - ref) <= ulp + 1e-30)
+
+
+def pin_gate():
+    rng = np.random.default_rng(2)
+    T, H, E = 5, 96, 7
+    # small integers: every product and partial sum is exact -> exact logits
+    xi = rng.integers(-3, 4, (T, H)).astype(np.float64)
+    wi = rng.integers(-3, 4, (E, H)).astype(np.float32)
+    b = rng.integers(-2, 3, E).astype(np.float32)
+    got = oracle.gate_logits(f32_to_bf16_bits(xi), wi, b)
+    assert np.array_equal(got, (xi @ wi.T.astype(np.float64) + b).astype(np.float32))
+    # random values: within the fp32 error bound of an H-term sum
+    x = f32_to_bf16_bits(rng.standard_normal((T, H)))
+    wg = (0.02 * rng.standard_normal((E, H))).astype(np.float32)
+    ref = bits_f64(x) @ wg.T.astype(np.float64)
+    bound = H * 2.0**-24 * (np.abs(bits_f64(x)) @ np.abs(wg.T.astype(np.float64)))
+    assert np.all(np.abs(oracle.gate_logits(x, wg) - ref) <= bound)
+
+
+def pin_topk():
+    rng = np.random.default_rng(3)
+    T, E, k = 64, 16, 4
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    lg[0] = 0.5                      # all equal -> experts 0..k-1
+    lg[1, :] = -1.0
+    lg[1, [3, 9, 12]] = 2.0          # three-way tie at the top
+    lg[2, :2] = [-0.0, 0.0]          # -0 and +0 compare equal
+    lg[2, 2:] = -5.0
+    idx, w = oracle.topk_softmax(lg, k, renorm=True)
+    # numpy's stable argsort on the negated logits: lowest index first on ties
+    ref_idx = np.argsort(-lg, axis=1, kind="stable")[:, :k]
+    assert np.array_equal(idx, ref_idx)
+    assert list(idx[0]) == [0, 1, 2, 3] and np.allclose(w[0], 0.25)
+    assert list(idx[1][:3]) == [3, 9, 12] and idx[2][0] == 0
+    # renormalised weights = softmax over the chosen logits (scipy)
+    ref_w = softmax(np.take_along_axis(lg, idx, 1).astype(np.float64), axis=1)
+    assert np.allclose(w, ref_w, rtol=1e-6, atol=1e-7)
+    assert np.allclose(w.astype(np.float64).sum(1), 1.0, atol=1e-6)
+    # without renormalisation: the full softmax probabilities of the chosen
+    idx2, w2 = oracle.topk_softmax(lg, k, renorm=False)
+    ref_p = np.take_along_axis(softmax(lg.astype(np.float64), axis=1), idx2, 1)
+    assert np.allclose(w2, ref_p, rtol=1e-6, atol=1e-7)
+
+
+def pin_routing():
+    rng = np.random.default_rng(4)
+    T, k, E = 300, 3, 11
+    ti = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    ti[:40] = ti[0]                         # many equal keys
+    r = oracle.init_routing(ti, E)
+    flat = ti.reshape(-1)
+    order = np.argsort(flat, kind="stable")     # row -> assignment
+    N = T * k
+    assert np.array_equal(np.sort(r["row_idx"]), np.arange(N))
+    assert np.array_equal(r["row_idx"][order], np.arange(N))
+    assert np.array_equal(r["src_token"], order // k)
+    assert np.array_equal(r["sorted_ids"], flat[order])
+    assert np.array_equal(r["counts"], np.bincount(flat, minlength=E))
+    assert r["offsets"][0] == 0 and r["offsets"][-1] == N
+    assert np.array_equal(np.diff(r["offsets"]), r["counts"])
+    c, o = oracle.expert_tokens(r["sorted_ids"], E)
+    assert np.array_equal(c, r["counts"]) and np.array_equal(o, r["offsets"])
+    bad = ti.copy()
+    bad[5, 1] = E
+    with pytest.raises(oracle.OracleError):
+        oracle.init_routing(bad, E)
+
+
+def pin_expert_mlp():
+    rng = np.random.default_rng(5)
+    n, H, I = 6, 40, 24              # H != I catches a transposed w2
+    xe = f32_to_bf16_bits(rng.standard_normal((n, H)))
+    w13 = f32_to_bf16_bits(0.2 * rng.standard_normal((2 * I, H)))
+    w2 = f32_to_bf16_bits(0.2 * rng.standard_normal((H, I)))
+    act, yb, yf = oracle.expert_mlp(xe, w13, w2, want_f64=True)
+    X, W13, W2 = bits_f64(xe), bits_f64(w13), bits_f64(w2)
+    g = X @ W13[:I].T                 # products of bf16 are exact in fp64
+    u = X @ W13[I:].T
+    ref_act = oracle.bf16_bits(g * expit(g) * u)   # SiLU(g) = g * sigmoid(g)
+    assert np.array_equal(act, ref_act)
+    ref_y = bits_f64(act) @ W2.T
+    assert np.allclose(yf, ref_y, rtol=1e-12, atol=1e-15)
+    assert np.array_equal(yb, oracle.bf16_bits(yf))
+    # SwiGLU special cases: SiLU(0) = 0 and SiLU(g) -> g for large g
+    xe1 = np.zeros((1, H), dtype=np.uint16)
+    xe1[0, 0] = 0x3F80                 # one-hot 1.0
+    w = np.zeros((2 * I, H), dtype=np.uint16)
+    w[0, 0] = 0x4180                   # gate 16
+    w[I, 0] = 0x3F80                   # up 1
+    w[I + 1, 0] = 0x4000               # gate 0, up 2 -> 0
+    a1, _ = oracle.expert_mlp(xe1, w, w2)
+    assert a1[0, 0] == 0x4180 and a1[0, 1] == 0
+    # grouped with one group == dense
+    off = np.array([0, n], dtype=np.int32)
+    ga, gy = oracle.grouped_mlp(xe, off, w13[None], w2[None])
+    assert np.array_equal(ga, act) and np.array_equal(gy, yb)
+
+
+def pin_finalize():
+    rng = np.random.default_rng(6)
+    T, H, E, k = 50, 32, 6, 3
+    x = f32_to_bf16_bits(rng.standard_normal((T, H)))
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    idx, w = oracle.topk_softmax(lg, k)
+    r = oracle.init_routing(idx, E)
+    ex = oracle.permute(x, r["src_token"])
+    # identity experts (y = expanded x): the renormalised weights sum to 1
+    out = oracle.finalize(ex, r["row_idx"], w)
+    assert np.allclose(out, bits_f64(x), rtol=4e-7, atol=1e-30)
+    sh = rng.standard_normal((T, H))
+    out2 = oracle.finalize(ex, r["row_idx"], w, sh)
+    assert np.allclose(out2, bits_f64(x) + sh, rtol=1e-6, atol=1e-6)
+
+
+def pin_worked_example():
+    with open(os.path.join(GOLDEN, "worked_example.json")) as f:
+        ex = json.load(f)
+    s = ex["shapes"]
+    T, H, E, k, I = s["T"], s["H"], s["E"], s["k"], s["I"]
+    x = f32_to_bf16_bits(np.array(ex["x"], dtype=np.float32))
+    wg = np.array(ex["wg"], dtype=np.float32)
+    w13 = np.zeros((E, 2 * I, H), dtype=np.float32)
+    w2 = np.zeros((E, H, I), dtype=np.float32)
+    for e in range(E):
+        w13[e, :, 0] = [e, 0, 1, 1]
+        w13[e, :, 1] = [1, -1, 2, 0.5]
+        w2[e, :, 0] = [1, -1, 0.5, 0]
+        w2[e, :, 1] = [0, 0, 0, 1]
+    from moe_inputs import Workload
+    wl = Workload("worked", T=T, H=H, E=E, k=k, I=I)
+    inputs = dict(x=torch.from_numpy(bits_f64(x).astype(np.float32)).to(torch.bfloat16),
+                  gamma=None, wg=wg, gate_bias=None,
+                  w13=torch.from_numpy(w13).to(torch.bfloat16),
+                  w2=torch.from_numpy(w2).to(torch.bfloat16), w13_s=None, w2_s=None)
+    out, idx, w = oracle.layer_tokens(inputs, wl)
+    exp = ex["expected"]
+    assert idx.tolist() == exp["topk_idx"]
+    assert np.allclose(w, exp["topk_w"], rtol=1e-7, atol=0)
+    assert np.allclose(out, exp["out"], rtol=0, atol=exp["out_tolerance"])
+    a, _ = oracle.expert_mlp(x[:1], f32_to_bf16_bits(w13[1]), f32_to_bf16_bits(w2[1]))
+    assert np.array_equal(bits_f64(a)[0], exp["act_token0_expert1"])
+    a, _ = oracle.expert_mlp(x[:1], f32_to_bf16_bits(w13[3]), f32_to_bf16_bits(w2[3]))
+    assert np.array_equal(bits_f64(a)[0], exp["act_token0_expert3"])
+    a, _ = oracle.expert_mlp(x[1:], f32_to_bf16_bits(w13[0]), f32_to_bf16_bits(w2[0]))
+    assert np.array_equal(bits_f64(a)[0], exp["act_token1"])
+
+
+def pin_layer_brute_force():
+    """Whole layer vs a per-token loop with no routing, no sort and no
+    permutation, written with numpy matmuls (tiny workload, seed 0)."""
+    wl = WORKLOADS["tiny"]
+    d = make_inputs(wl, 0)
+    out, idx, w = oracle.layer_tokens(d, wl)
+    X = d["x"].to(torch.float64).numpy()
+    WG = d["wg"].to(torch.float64).numpy()
+    W13 = d["w13"].to(torch.float64).numpy()
+    W2 = d["w2"].to(torch.float64).numpy()
+    logits = X @ WG.T
+    srt = np.sort(logits, axis=1)[:, ::-1]
+    margin = srt[:, wl.k - 1] - srt[:, wl.k]
+    assert margin.min() > 1e-5          # no near-ties for this seed
+    for t in range(wl.T):
+        sel = np.argsort(-logits[t], kind="stable")[: wl.k]
+        assert sorted(sel) == sorted(idx[t])
+        p = softmax(logits[t, sel])
+        acc = np.zeros(wl.H)
+        for j, e in enumerate(sel):
+            g = X[t] @ W13[e, : wl.I].T
+            u = X[t] @ W13[e, wl.I:].T
+            a = bits_f64(oracle.bf16_bits(g * expit(g) * u))
+            y = bits_f64(oracle.bf16_bits(a @ W2[e].T))
+            acc += p[j] * y
+        assert np.allclose(out[t], acc, rtol=1e-5, atol=1e-7), t
+
+
+def pin_layer_shared_rmsnorm():
+    """A small workload with RMSNorm, a gate offset and a shared expert:
+    the layer equals the composition of its steps, and the shared term is
+    exactly the shared expert's unrounded output."""
+    from moe_inputs import Workload
+    wl = Workload("small", T=24, H=64, E=6, k=2, I=32, I_s=48, rmsnorm=True,
+                  gamma_std=0.1, skew_s=1.2, skew_beta=0.5)
+    d = make_inputs(wl, 3)
+    out, idx, w = oracle.layer_tokens(d, wl)
+    xn = oracle.rmsnorm(d["x"], d["gamma"], wl.eps)
+    lg = oracle.gate_logits(xn, d["wg"], d["gate_bias"])
+    i2, w2_ = oracle.topk_softmax(lg, wl.k)
+    assert np.array_equal(idx, i2) and np.array_equal(w, w2_)
+    r = oracle.init_routing(i2, wl.E)
+    ex = oracle.permute(xn, r["src_token"])
+    _, y = oracle.grouped_mlp(ex, r["offsets"], d["w13"], d["w2"])
+    _, _, ys = oracle.expert_mlp(xn, d["w13_s"], d["w2_s"], want_f64=True)
+    ref = oracle.finalize(y, r["row_idx"], w, ys)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-15)
+    # with the shared expert's weights zeroed the shared term vanishes
+    d0 = dict(d, w2_s=torch.zeros_like(d["w2_s"]))
+    out0, _, _ = oracle.layer_tokens(d0, wl)
+    assert np.allclose(out - out0, ys, rtol=1e-12, atol=1e-15)
+
+
+PINS = [pin_bf16_rounding, pin_rmsnorm, pin_gate, pin_topk, pin_routing,
+        pin_expert_mlp, pin_finalize, pin_worked_example, pin_layer_brute_force,
+        pin_layer_shared_rmsnorm]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin()
+
+
+# ------------------------------------------------------------------ mutants
+# (original text, planted mistake) in moe_oracle.c
+MUTANTS = {
+    "rms_no_sqrt": ("1.0f / sqrtf(mean + eps)", "1.0f / (mean + eps)"),
+    "rms_no_mean": ("ss / (float)H", "ss"),
+    "rms_no_gamma": ("v = v * bf16_to_float(gamma[h]);", "v = v;"),
+    "gate_transposed": ("wg[e * H + h], acc)", "wg[h * E + e], acc)"),
+    "gate_no_bias": ("acc = acc + bias[e];", "acc = acc;"),
+    "topk_ties_high": ("l[e] > l[best]", "l[e] >= l[best]"),
+    "softmax_sign": ("exp((double)l[topk_idx[t * k + j]] - m) / den",
+                     "exp(m - (double)l[topk_idx[t * k + j]]) / den"),
+    "no_renorm": ("if (renorm) {", "if (0) {"),
+    "route_src_mod": ("src_token[row] = (int32_t)(a / k);",
+                      "src_token[row] = (int32_t)(a % k);"),
+    "route_unstable": ("const int32_t row = offsets[e] + fill[e]++;",
+                       "const int32_t row = offsets[e + 1] - ++fill[e];"),
+    "swiglu_swapped": ("const bf16_t *wgate = w13 + i * H;\n            const bf16_t *wup = w13 + (I + i) * H;",
+                       "const bf16_t *wup = w13 + i * H;\n            const bf16_t *wgate = w13 + (I + i) * H;"),
+    "silu_sign": ("g / (1.0 + exp(-g))", "g / (1.0 + exp(g))"),
+    "down_transposed": ("const bf16_t *wr = w2 + c * I;", "const bf16_t *wr = w2 + c;"),
+    "finalize_no_shared": ("s += shared[t * H + c];", "s += 0.0;"),
+    "finalize_weight_index": ("(double)topk_w[t * k + j] *", "(double)topk_w[j] *"),
+    "bf16_truncate": ("nearbyint(ldexp(m, 8))", "floor(ldexp(m, 8))"),
+    "layer_shared_dropped": ("o[c] += ys[c];", "o[c] += 0.0;"),
+}
+
+
+def _build_mutant(src_text, tmpdir, name, old, new):
+    assert src_text.count(old) >= 1, f"mutant {name}: pattern not found"
+    path_c = os.path.join(tmpdir, f"{name}.c")
+    with open(path_c, "w") as f:
+        f.write(src_text.replace(old, new))
+    path_so = os.path.join(tmpdir, f"lib{name}.so")
+    subprocess.run(["gcc", "-O1", "-std=gnu11", "-fPIC", "-shared", "-fopenmp",
+                    "-ffp-contract=off", "-o", path_so, path_c, "-lm"], check=True)
+    return path_so
+
+
+def test_mutants_are_caught():
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")).read()
+    survivors = []
+    tmpdir = tempfile.mkdtemp(prefix="oracle_mutants_")
+    try:
+        for name, (old, new) in MUTANTS.items():
+            so = _build_mutant(src, tmpdir, name, old, new)
+            caught = False
+            with oracle.using_library(so):
+                for pin in PINS:
+                    try:
+                        pin()
+                    except (AssertionError, oracle.OracleError, ValueError, IndexError):
+                        caught = True
+                        break
+            if not caught:
+                survivors.append(name)
+    finally:
+        shutil.rmtree(tmpdir, ignore_errors=True)
+    assert not survivors, f"mutants not caught by any pin: {survivors}"
