@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 MoE feed-forward layer (libmoe, sm_103a).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+One step = one pass of the whole layer (RMSNorm, fp32 gate, top-k, routing,
+permute, grouped w13 GEMM + SwiGLU, grouped down GEMM, shared expert,
+finalize) over one batch of seeded synthetic tokens, through the C ABI.
+Inputs (weights 4.9 GB for the image-gen block) are resident in HBM and far
+larger than L2, so no L2 flush is needed between steps.  The K timed steps
+are bracketed by a barrier and a device synchronisation; the time is taken
+with CUDA events on the launching stream, max over ranks.  Per-stage times
+come from events the library records between its launches in the same
+timed steps (moe_layer_forward_timed).
+
+N > 1 (torchrun, one rank per GPU): every rank runs an independent replica
+of the layer on its own batch (weak scaling, no collective on the data
+path); ``value`` is all ranks' tokens over the slowest rank's time.
+
+--impl reference times the CPU oracle (oracle/, the plain C definition of
+the layer) on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s; grouped-GEMM TFLOP/s (% bf16 peak); routing GB/s"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="imagegen-16k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU work of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", "GPU-" + uuid if not uuid.startswith("GPU-") else uuid]
+        except Exception:
+            sel = []
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *sel, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = set()
+        for r in rows:
+            for name, v in zip(self.REASONS, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# --------------------------------------------------------------- traffic
+def kernel_fingerprint() -> str:
+    h = hashlib.sha256()
+    for rel in ("moe_expert_routing_fp32_gb300/csrc/gemm.cu",
+                "moe_expert_routing_fp32_gb300/csrc/common.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the w13 GEMM from the committed ncu summary,
+    if it was taken on the current kernel source for this workload."""
+    path = os.path.join(ROOT, "profiles", "gemm_w13_swiglu_" + workload + ".md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fp = kernel_fingerprint()
+    for line in text.splitlines():
+        if line.startswith("traffic_bytes_per_launch:"):
+            parts = dict(p.split("=", 1) for p in line.split(":", 1)[1].split() if "=" in p)
+            if parts.get("kernel") == fp:
+                return float(parts["bytes"])
+    return None
+
+
+# --------------------------------------------------------------- oracle
+def cpu_oracle_rate(inputs_cpu, wl, seconds, first_token=0):
+    """Oracle tokens/s on a bounded sample (first tokens of the batch)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.layer_tokens(inputs_cpu, wl, np.array([first_token], dtype=np.int32))
+    one = max(time.perf_counter() - t0, 1e-3)
+    n = int(max(1, min(wl.T - first_token, seconds / one)))
+    tok = np.arange(first_token, first_token + n, dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.layer_tokens(inputs_cpu, wl, tok)
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt
+
+
+# --------------------------------------------------------------- our arm
+def stage_bytes_flops(wl):
+    T, H, E, k, I, Is = wl.T, wl.H, wl.E, wl.k, wl.I, wl.I_s
+    N = T * k
+    return {
+        "router": {"bytes": T * H * 2 * (2 if wl.rmsnorm else 1) + E * H * 4 + N * 8 +
+                   (T * H * 2 if wl.rmsnorm else 0), "flops": 2.0 * T * H * E},
+        "permute": {"bytes": T * H * 2 + N * H * 2 + N * 4},
+        "gemm_w13_swiglu": {"flops": 4.0 * N * H * I + 4.0 * T * H * Is,
+                            "bytes": E * 2 * I * H * 2 + 2 * I_s_or0(Is) * H * 2},
+        "gemm_down": {"flops": 2.0 * N * H * I + 2.0 * T * H * Is},
+        "finalize": {"bytes": N * H * 2 + (T * H * 4 if Is else 0) + T * H * 2 + N * 8},
+    }
+
+
+def I_s_or0(v):
+    return v or 0
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import moe_expert_routing_fp32_gb300 as moe
+    from moe_inputs import WORKLOADS, make_inputs
+
+    moe.build()
+    wl = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    g = make_inputs(wl, args.seed, device=str(dev))
+    weights = moe.LayerWeights(wg=g["wg"], w13=g["w13"], w2=g["w2"], gamma=g["gamma"],
+                               gate_bias=g["gate_bias"], w13_s=g["w13_s"], w2_s=g["w2_s"])
+    desc = moe.make_desc(wl.T, wl.H, wl.E, wl.k, wl.I, wl.I_s, rmsnorm=wl.rmsnorm, eps=wl.eps,
+                         renorm=wl.renorm, out_f32=False)
+    ws = torch.empty(moe.layer_workspace_size(desc), dtype=torch.uint8, device=dev)
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
+    status = moe.new_status(dev)
+    x = g["x"]
+    K, W = args.steps, args.warmup
+    nst = moe.NUM_STAGES + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(K)]
+    for row in evs:
+        for e in row:
+            e.record()           # creates the event handles
+    for _ in range(W):
+        moe.layer_forward(desc, x, weights, out=out, workspace=ws, status=status)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+
+    dist = world > 1
+    if dist:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(K):
+        moe.layer_forward(desc, x, weights, out=out, workspace=ws, status=status,
+                          stage_events=evs[i])
+    end.record()
+    torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the timed steps")
+
+    stage_ms = {}
+    for j, name in enumerate(moe.STAGE_NAMES):
+        stage_ms[name] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+    step_ms = elapsed_ms / K
+    value = world * wl.T * K / (elapsed_ms / 1e3)
+
+    # end to end on host buffers (pinned), through the same public call
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, pin_memory=True)
+    x_dev = torch.empty_like(x)
+    for _ in range(2):
+        moe.layer_forward_host(desc, x_host, weights, out_host, x_dev=x_dev, out_dev=out,
+                               workspace=ws, status=status)
+    Ke = max(3, min(K, 20))
+    if dist:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(Ke):
+        moe.layer_forward_host(desc, x_host, weights, out_host, x_dev=x_dev, out_dev=out,
+                               workspace=ws, status=status)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * wl.T * Ke / (e2e_ms / 1e3)
+
+    peaks, peak_src = load_peaks()
+    work = stage_bytes_flops(wl)
+    dom = "gemm_w13_swiglu"
+    dom_s = stage_ms[dom] / 1e3
+    tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = work[dom]["flops"] / dom_s / 1e12
+    gemm_s = (stage_ms["gemm_w13_swiglu"] + stage_ms["gemm_down"]) / 1e3
+    gemm_tflops = (work["gemm_w13_swiglu"]["flops"] + work["gemm_down"]["flops"]) / gemm_s / 1e12
+    per_stage = {}
+    for name, ms in stage_ms.items():
+        e = {"ms": round(ms, 4), "share": round(ms / step_ms, 4)}
+        wk = work.get(name, {})
+        if "flops" in wk and name.startswith("gemm"):
+            e["tflops"] = round(wk["flops"] / (ms / 1e3) / 1e12, 1)
+            e["frac_bf16_peak"] = round(e["tflops"] / tc_peak, 4)
+        if "bytes" in wk and not name.startswith("gemm"):
+            e["gbs"] = round(wk["bytes"] / (ms / 1e3) / 1e9, 1)
+            e["frac_hbm"] = round(e["gbs"] / hbm_peak, 4)
+        per_stage[name] = e
+
+    launches_per_step = 7 + (2 if wl.E > 64 else 0)
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) random-init weights)",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
+                   "I_shared": wl.I_s, "rmsnorm": wl.rmsnorm, "out": "bf16",
+                   "gate": "fp32", "l2": "inputs larger than L2 (no flush needed)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": tc_peak, "unit": "TFLOP/s", "frac": round(achieved / tc_peak, 4),
+                     "peak_source": f"bf16_tflops_sustained ({peak_src})",
+                     "traffic": recorded_traffic(wl.name)},
+        "gemm_tflops": round(gemm_tflops, 1),
+        "gemm_frac_bf16_peak": round(gemm_tflops / tc_peak, 4),
+        "stages": per_stage,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
+                "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in g.items()}
+        rate, n, dt = cpu_oracle_rate(cpu, wl, args.cpu_seconds)
+        res["cpu_baseline"] = {"value": round(rate, 3), "unit": UNIT, "cores": host_cores(),
+                               "kind": "oracle",
+                               "sample": f"first {n} tokens of the batch, {dt:.1f} s"}
+    return res
+
+
+# --------------------------------------------------------------- reference arm
+def run_reference(args):
+    import numpy as np
+    import torch
+    from moe_inputs import WORKLOADS, make_inputs
+    import oracle
+
+    oracle.build()
+    wl = WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    g = make_inputs(wl, args.seed, device=dev)     # drawn where it is fast
+    cpu = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in g.items()}
+    del g
+    # size a step so that warm-up + steps take about a minute and a half
+    t0 = time.perf_counter()
+    oracle.layer_tokens(cpu, wl, np.array([0], dtype=np.int32))
+    one = max(time.perf_counter() - t0, 1e-3)
+    total_steps = args.steps + args.warmup
+    per_step = int(max(1, min(wl.T // max(total_steps, 1), 90.0 / total_steps / one)))
+    tok = 0
+    for _ in range(args.warmup):
+        oracle.layer_tokens(cpu, wl, np.arange(tok, tok + per_step, dtype=np.int32) % wl.T)
+        tok += per_step
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.layer_tokens(cpu, wl, np.arange(tok, tok + per_step, dtype=np.int32) % wl.T)
+        tok += per_step
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    sample = f"{per_step} tokens per step of the {wl.name} batch"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
+                   "I_shared": wl.I_s},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": host_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        res = run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -202,6 +202,28 @@ moe_status_t moe_layer_forward(const moe_desc_t *desc, const moe_bf16_t *x,
                                size_t workspace_bytes, int32_t *dev_status,
                                moe_stream_t stream);
 
+/*
+ * moe_layer_forward with per-stage timing: identical work, plus
+ * cudaEventRecord(stage_events[i], stream) before launch stage i and
+ * stage_events[MOE_NUM_STAGES] after the last one.  Stages:
+ *   0 RMSNorm + gate + top-k (+ routing histogram)
+ *   1 routing scan + stable scatter
+ *   2 permute (expanded_x rows)
+ *   3 grouped w13 matmul + SwiGLU (routed and shared expert)
+ *   4 grouped down matmul
+ *   5 finalize
+ * stage_events: MOE_NUM_STAGES + 1 cudaEvent_t handles owned by the caller
+ * (created with timing enabled); NULL behaves as moe_layer_forward.
+ */
+#define MOE_NUM_STAGES 6
+moe_status_t moe_layer_forward_timed(const moe_desc_t *desc, const moe_bf16_t *x,
+                                     const moe_bf16_t *gamma, const float *wg,
+                                     const float *gate_bias, const moe_bf16_t *w13,
+                                     const moe_bf16_t *w2, const moe_bf16_t *w13_s,
+                                     const moe_bf16_t *w2_s, void *out, void *workspace,
+                                     size_t workspace_bytes, int32_t *dev_status,
+                                     moe_stream_t stream, void *const *stage_events);
+
 #ifdef __cplusplus
 }
 #endif

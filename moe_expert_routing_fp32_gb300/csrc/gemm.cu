@@ -1,0 +1,544 @@
+// gemm.cu -- grouped expert matmuls on the 5th-generation tensor cores.
+//
+// "NPU HunyuanImage-3.0模型推理优化实践": "GMM使能&&Routing优化" (one grouped
+// matmul computes all experts instead of a per-expert loop) and
+// "MoE TP优化 / 计算分解" (gate and up merged into w13; SwiGLU returns
+// SiLU(first half) * second half).
+//
+// One persistent kernel serves both matmuls of the expert FFN:
+//   SWIGLU: act[r, n] = bf16(SiLU(g) * u), g = A[r] . W[grp, n], u = A[r] . W[grp, half + n]
+//   STORE:  out[r, n] = A[r] . W[grp, n]          (bf16, or fp32 for segment 1)
+// over ragged groups: group g owns rows [offsets[g], offsets[g+1]) of A and
+// weight slice W[g].  An optional dense "segment 1" (the shared expert, its
+// own A, W and output) is appended to the same tile list.
+//
+// Tiles are 128 rows x BN columns (SWIGLU: 128 gate + 128 up columns giving
+// 128 act columns).  The tile list is built on the device from `offsets`
+// (no host sync): per group ceil(rows/128) m-blocks x n-blocks, m fastest so
+// CTAs running at the same time share weight tiles through L2.  A tile may
+// read rows of the next group; the epilogue stores only the group's rows.
+//
+// CTA roles (192 threads, one CTA per SM):
+//   warp 0     TMA producer: A and B k-slices (64 wide, 128-byte swizzle)
+//              into a 4-stage shared-memory ring;
+//   warp 1     allocates 2*BN TMEM columns; one thread issues
+//              tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM
+//              accumulators and commits stage releases / tile completion;
+//   warps 2-5  epilogue: tcgen05.ld of the finished accumulator (each warp
+//              its 32-lane quarter), SwiGLU or conversion, 16-byte stores.
+// The two accumulators let the epilogue of tile i overlap the MMAs of i+1.
+// Every wait is bounded (MOE_DEV_TIMEOUT) and on abort each role lets its
+// in-flight copies / MMAs finish before the TMEM is freed.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int THREADS = 192;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int MAX_GROUPS = 1024;
+
+enum { MODE_SWIGLU = 0, MODE_STORE = 1 };
+
+struct Params {
+    CUtensorMap tmA0;   // routed A [rows0, K0]
+    CUtensorMap tmB0;   // routed W [G, NW0, K0]
+    CUtensorMap tmA1;   // segment-1 A [rows1, K1]
+    CUtensorMap tmB1;   // segment-1 W [NW1, K1]
+    const int32_t *offsets;
+    int32_t G;
+    int32_t rows0;      // rows of A0 / out0 (bounds the offsets)
+    int32_t K0, K1;
+    int32_t nt0, nt1;   // n-blocks per m-block
+    int32_t half0, half1;
+    int32_t rows1;      // 0 = no segment 1
+    void *out0;
+    int64_t ldo0;
+    void *out1;
+    int64_t ldo1;
+    int32_t out1_f32;
+    int32_t *dev_status;
+};
+
+struct Tile {
+    int seg, g, row0, row_end, n_blk, kblocks;
+};
+
+template <int BN>
+struct Cfg {
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+    // barriers: full[S], empty[S], tfull[2], tempty[2], drain
+    static constexpr int NBARS = 2 * STAGES + 5;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int OFFS_OFF = MISC_OFF + 16;
+    static constexpr int PREFIX_OFF = OFFS_OFF + (MAX_GROUPS + 1) * 4;
+    static constexpr int SMEM = 1024 + PREFIX_OFF + (MAX_GROUPS + 2) * 4;
+};
+
+__device__ __forceinline__ Tile decode_tile(const Params &p, int tile, const int *s_off,
+                                            const int *s_prefix, int total0) {
+    Tile t;
+    if (tile < total0) {
+        // last group whose prefix is <= tile
+        int lo = 0, hi = p.G - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_prefix[mid] <= tile)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int g = lo;
+        const int cnt = s_off[g + 1] - s_off[g];
+        const int mt = (cnt + BM - 1) / BM;
+        const int local = tile - s_prefix[g];
+        t.seg = 0;
+        t.g = g;
+        t.row0 = s_off[g] + (local % mt) * BM;
+        t.row_end = s_off[g + 1];
+        t.n_blk = local / mt;
+        t.kblocks = p.K0 / BK;
+    } else {
+        const int local = tile - total0;
+        const int mt = (p.rows1 + BM - 1) / BM;
+        t.seg = 1;
+        t.g = 0;
+        t.row0 = (local % mt) * BM;
+        t.row_end = p.rows1;
+        t.n_blk = local / mt;
+        t.kblocks = p.K1 / BK;
+    }
+    return t;
+}
+
+template <int MODE, int BN>
+__global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_constant__ Params p) {
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *tfull = bars + 2 * STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+    volatile int *s_bad = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 8);
+    int *s_off = reinterpret_cast<int *>(smem + C::OFFS_OFF);
+    int *s_prefix = reinterpret_cast<int *>(smem + C::PREFIX_OFF);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    // ---- prologue: group offsets, tile prefix, barriers
+    if (tid == 0) {
+        *s_abort = 0;
+        *s_bad = 0;
+    }
+    for (int g = tid; g <= p.G; g += THREADS) s_off[g] = p.offsets[g];
+    __syncthreads();
+    if (warp == 0) {
+        int run = 0;
+        bool bad = false;
+        for (int g0 = 0; g0 < p.G; g0 += 32) {
+            const int g = g0 + lane;
+            int tiles = 0;
+            if (g < p.G) {
+                const int a = s_off[g], b = s_off[g + 1];
+                if (a < 0 || b < a || b > p.rows0) bad = true;
+                tiles = b > a ? ((b - a + BM - 1) / BM) * p.nt0 : 0;
+            }
+            int inc = tiles;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, inc, off);
+                if (lane >= off) inc += o;
+            }
+            if (g < p.G) s_prefix[g] = run + inc - tiles;
+            run += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) s_prefix[p.G] = run;
+        if (__any_sync(0xffffffffu, bad) && lane == 0) *s_bad = 1;
+    }
+    if (tid == 32) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (*s_bad) {
+        if (tid == 0 && blockIdx.x == 0) report(p.dev_status, MOE_DEV_BAD_OFFSETS);
+        return;
+    }
+    const int total0 = s_prefix[p.G];
+    const int total = total0 + (p.rows1 > 0 ? ((p.rows1 + BM - 1) / BM) * p.nt1 : 0);
+
+    if (warp == 1) {
+        tmem_alloc(s_tmem, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+
+    if (warp == 0) {
+        // ================= TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmA0);
+            tma_prefetch_desc(&p.tmB0);
+            if (p.rows1 > 0) {
+                tma_prefetch_desc(&p.tmA1);
+                tma_prefetch_desc(&p.tmB1);
+            }
+            int stage = 0;
+            uint32_t phase = 0;
+            int armed[STAGES];
+            for (int s = 0; s < STAGES; ++s) armed[s] = -1;
+            for (int tile = blockIdx.x; tile < total && !*s_abort; tile += gridDim.x) {
+                const Tile t = decode_tile(p, tile, s_off, s_prefix, total0);
+                bool ok = true;
+                for (int kb = 0; kb < t.kblocks; ++kb) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1, s_abort, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    armed[stage] = static_cast<int>(phase);
+                    uint8_t *a_dst = smem + stage * C::STAGE_BYTES;
+                    uint8_t *b_dst = a_dst + A_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                    const int k0 = kb * BK;
+                    if (t.seg == 0) {
+                        tma_load_2d(a_dst, &p.tmA0, &full[stage], k0, t.row0);
+                        if (MODE == MODE_SWIGLU) {
+                            tma_load_3d(b_dst, &p.tmB0, &full[stage], k0, t.n_blk * 128, t.g);
+                            tma_load_3d(b_dst + 128 * BK * 2, &p.tmB0, &full[stage], k0,
+                                        p.half0 + t.n_blk * 128, t.g);
+                        } else {
+                            tma_load_3d(b_dst, &p.tmB0, &full[stage], k0, t.n_blk * BN, t.g);
+                        }
+                    } else {
+                        tma_load_2d(a_dst, &p.tmA1, &full[stage], k0, t.row0);
+                        if (MODE == MODE_SWIGLU) {
+                            tma_load_2d(b_dst, &p.tmB1, &full[stage], k0, t.n_blk * 128);
+                            tma_load_2d(b_dst + 128 * BK * 2, &p.tmB1, &full[stage], k0,
+                                        p.half1 + t.n_blk * 128);
+                        } else {
+                            tma_load_2d(b_dst, &p.tmB1, &full[stage], k0, t.n_blk * BN);
+                        }
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+            }
+            if (*s_abort) {
+                for (int s = 0; s < STAGES; ++s)
+                    if (armed[s] >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>(armed[s]));
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================= MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool issued = false;
+            for (int tile = blockIdx.x; tile < total && !*s_abort; tile += gridDim.x) {
+                const Tile t = decode_tile(p, tile, s_off, s_prefix, total0);
+                if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, s_abort, p.dev_status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                bool ok = true;
+                for (int kb = 0; kb < t.kblocks; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase, s_abort, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        tc_mma_bf16(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32),
+                                    sdesc_kmajor_sw128(b_addr + kk * 32), IDESC,
+                                    (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    tc_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            if (*s_abort && issued) {
+                // unwinding: wait for every MMA issued so far before TMEM is freed
+                tc_commit(drain);
+                mbar_wait_drain(drain, 0);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================= epilogue (warps 2..5)
+        const int q = warp & 3;               // TMEM lane quarter of this warp
+        const int row_in_tile = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const Tile t = decode_tile(p, tile, s_off, s_prefix, total0);
+            if (!mbar_wait_bounded(&tfull[acc], acc_phase, s_abort, p.dev_status)) break;
+            tc_fence_after();
+            const int row = t.row0 + row_in_tile;
+            const bool ok = row < t.row_end;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            if (MODE == MODE_SWIGLU) {
+                uint16_t *out = static_cast<uint16_t *>(t.seg == 0 ? p.out0 : p.out1);
+                const int64_t ldo = t.seg == 0 ? p.ldo0 : p.ldo1;
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 32) {
+                    float g[32], u[32];
+                    __syncwarp();
+                    tmem_ld32(taddr + c, g);
+                    tmem_ld32(taddr + 128 + c, u);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float a0 = __fdiv_rn(g[2 * i], 1.0f + expf(-g[2 * i])) * u[2 * i];
+                        const float a1 =
+                            __fdiv_rn(g[2 * i + 1], 1.0f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+                        pk[i] = pack_bf16x2(a0, a1);
+                    }
+                    if (ok) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            out + static_cast<int64_t>(row) * ldo + t.n_blk * 128 + c);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                                                pk[4 * v + 3]);
+                    }
+                }
+            } else {
+                const bool f32 = t.seg == 1 && p.out1_f32;
+                void *outp = t.seg == 0 ? p.out0 : p.out1;
+                const int64_t ldo = t.seg == 0 ? p.ldo0 : p.ldo1;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    float v[32];
+                    __syncwarp();
+                    tmem_ld32(taddr + c, v);
+                    tmem_ld_wait();
+                    if (!ok) continue;
+                    const int64_t off = static_cast<int64_t>(row) * ldo + t.n_blk * BN + c;
+                    if (f32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(outp) + off);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    } else {
+                        uint4 *dst =
+                            reinterpret_cast<uint4 *>(static_cast<uint16_t *>(outp) + off);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]),
+                                                pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                                pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                                                pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+                    }
+                }
+            }
+            __syncwarp();
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// bf16 tensor [outer...][inner] viewed as K-major tiles of box_rows x 64.
+bool make_map(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[3], gstride[2];
+    cuuint32_t box[3], estr[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) gdim[i] = dims[i];
+    gstride[0] = dims[0] * 2;
+    if (rank == 3) gstride[1] = dims[0] * dims[1] * 2;
+    box[0] = BK;
+    box[1] = static_cast<cuuint32_t>(box_rows);
+    box[2] = 1;
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(ptr),
+                          gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int MODE, int BN>
+cudaError_t launch(Params &p, int max_rows0, cudaStream_t stream) {
+    using C = Cfg<BN>;
+    static std::mutex mu;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !attr_done[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, BN>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 C::SMEM);
+            if (e != cudaSuccess) return e;
+            attr_done[dev] = true;
+        }
+    }
+    // an upper bound on the tile count: sum over groups of ceil(rows/128)
+    const int64_t mblocks0 = ceil_div(max_rows0, BM) + p.G;
+    const int64_t tiles = mblocks0 * p.nt0 + (p.rows1 > 0 ? ceil_div(p.rows1, BM) * p.nt1 : 0);
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), tiles)));
+    grouped_gemm_kernel<MODE, BN><<<grid, THREADS, C::SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tensor_maps_available() { return encode_fn() != nullptr; }
+
+cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G, int n, int K,
+                               const uint16_t *W13, int N, uint16_t *act,
+                               const GemmSegment1 &seg1, int32_t *dev_status,
+                               cudaStream_t stream) {
+    if (G > MAX_GROUPS) return cudaErrorInvalidValue;
+    Params p{};
+    const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
+    const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(2 * N),
+                            static_cast<uint64_t>(G)};
+    if (!make_map(&p.tmA0, A, 2, a0, BM) || !make_map(&p.tmB0, W13, 3, b0, 128))
+        return cudaErrorInvalidValue;
+    p.tmA1 = p.tmA0;
+    p.tmB1 = p.tmB0;
+    if (seg1.rows > 0) {
+        const uint64_t a1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.rows)};
+        const uint64_t b1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(2 * seg1.N1)};
+        if (!make_map(&p.tmA1, seg1.A, 2, a1, BM) || !make_map(&p.tmB1, seg1.B, 2, b1, 128))
+            return cudaErrorInvalidValue;
+    }
+    p.offsets = offsets;
+    p.G = G;
+    p.rows0 = n;
+    p.K0 = K;
+    p.K1 = seg1.K1;
+    p.nt0 = N / 128;
+    p.nt1 = seg1.N1 / 128;
+    p.half0 = N;
+    p.half1 = seg1.N1;
+    p.rows1 = seg1.rows;
+    p.out0 = act;
+    p.ldo0 = N;
+    p.out1 = seg1.out;
+    p.ldo1 = seg1.N1;
+    p.out1_f32 = 0;
+    p.dev_status = dev_status;
+    return launch<MODE_SWIGLU, 256>(p, n, stream);
+}
+
+cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, int n, int K,
+                              const uint16_t *W, int N, uint16_t *y, const GemmSegment1 &seg1,
+                              int32_t *dev_status, cudaStream_t stream) {
+    if (G > MAX_GROUPS) return cudaErrorInvalidValue;
+    const int BN = (N % 256 == 0 && (seg1.rows == 0 || seg1.N1 % 256 == 0)) ? 256 : 128;
+    Params p{};
+    const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
+    const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                            static_cast<uint64_t>(G)};
+    if (!make_map(&p.tmA0, A, 2, a0, BM) || !make_map(&p.tmB0, W, 3, b0, BN))
+        return cudaErrorInvalidValue;
+    p.tmA1 = p.tmA0;
+    p.tmB1 = p.tmB0;
+    if (seg1.rows > 0) {
+        const uint64_t a1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.rows)};
+        const uint64_t b1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.N1)};
+        if (!make_map(&p.tmA1, seg1.A, 2, a1, BM) || !make_map(&p.tmB1, seg1.B, 2, b1, BN))
+            return cudaErrorInvalidValue;
+    }
+    p.offsets = offsets;
+    p.G = G;
+    p.rows0 = n;
+    p.K0 = K;
+    p.K1 = seg1.K1;
+    p.nt0 = N / BN;
+    p.nt1 = seg1.N1 / BN;
+    p.half0 = 0;
+    p.half1 = 0;
+    p.rows1 = seg1.rows;
+    p.out0 = y;
+    p.ldo0 = N;
+    p.out1 = seg1.out;
+    p.ldo1 = seg1.N1;
+    p.out1_f32 = seg1.out_f32 ? 1 : 0;
+    p.dev_status = dev_status;
+    if (BN == 256) return launch<MODE_STORE, 256>(p, n, stream);
+    return launch<MODE_STORE, 128>(p, n, stream);
+}
+
+}  // namespace moe

@@ -1,0 +1,74 @@
+// internal.h -- launchers shared between the libmoe translation units.
+// Every launcher only enqueues work on `stream`; it returns the
+// cudaGetLastError() of its launches.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// tokens per routing chunk: the router's CTA and the routing kernels agree on it
+constexpr int kChunkTokens = 32;
+// largest E for which the router fuses top-k and the routing histogram
+constexpr int kRouterExperts = 64;
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int num_sms();  // of the current device (cached)
+
+// ---- router.cu
+// RMSNorm (optional) + fp32 gate.  If fuse_topk (requires E <= 64), also
+// top-k/softmax into topk_idx/topk_w and the per-chunk expert histogram
+// into hist[ceil(T/32)][E] (hist may be NULL).
+cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float *wg,
+                          const float *gate_bias, int T, int H, int E, float eps, bool rmsnorm,
+                          uint16_t *xn, float *logits, bool fuse_topk, int k, bool renorm,
+                          int32_t *topk_idx, float *topk_w, int32_t *hist,
+                          int32_t *dev_status, cudaStream_t stream);
+
+cudaError_t launch_topk(const float *logits, int T, int E, int k, bool renorm,
+                        int32_t *topk_idx, float *topk_w, cudaStream_t stream);
+
+// ---- routing.cu
+cudaError_t launch_route_hist(const int32_t *topk_idx, int T, int k, int E, int32_t *hist,
+                              int32_t *dev_status, cudaStream_t stream);
+// hist [B][E] -> in place per-chunk row bases; counts [E]; offsets [E+1]
+cudaError_t launch_route_scan(int32_t *hist, int B, int E, int32_t *counts, int32_t *offsets,
+                              cudaStream_t stream);
+cudaError_t launch_route_scatter(const int32_t *topk_idx, const int32_t *base, int T, int k,
+                                 int E, int32_t *row_idx, int32_t *src_token,
+                                 int32_t *sorted_ids, int32_t *dev_status, cudaStream_t stream);
+cudaError_t launch_permute(const uint16_t *xs, const int32_t *row_idx, int T, int H, int k,
+                           uint16_t *expanded_x, cudaStream_t stream);
+cudaError_t launch_expert_tokens(const int32_t *ids, int n, int E, int32_t *counts,
+                                 int32_t *offsets, int32_t *dev_status, cudaStream_t stream);
+cudaError_t launch_finalize(const uint16_t *y_exp, const int32_t *row_idx, const float *topk_w,
+                            const void *shared, bool shared_f32, int T, int H, int k,
+                            void *out, bool out_f32, cudaStream_t stream);
+
+// ---- gemm.cu
+struct GemmSegment1 {       // an optional dense problem appended to the grouped one
+    const uint16_t *A;      // [rows, K1]
+    const uint16_t *B;      // SwiGLU: [2*N1, K1]; store: [N1, K1]
+    int rows = 0;           // 0 = absent
+    int K1 = 0;
+    int N1 = 0;             // SwiGLU: I_s (act columns); store: output columns
+    void *out = nullptr;    // [rows, N1] bf16 (or fp32 with out_f32)
+    bool out_f32 = false;
+};
+
+// act[r, :] = bf16(SiLU(A W13g^T) * (A W13u^T)) per group; A [n, K], W13 [G, 2N, K]
+cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G, int n, int K,
+                               const uint16_t *W13, int N, uint16_t *act,
+                               const GemmSegment1 &seg1, int32_t *dev_status,
+                               cudaStream_t stream);
+// y[r, :] = bf16(A W^T) per group; A [n, K], W [G, N, K]
+cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, int n, int K,
+                              const uint16_t *W, int N, uint16_t *y, const GemmSegment1 &seg1,
+                              int32_t *dev_status, cudaStream_t stream);
+bool tensor_maps_available();
+
+}  // namespace moe

@@ -1,0 +1,369 @@
+// moe_abi.cu -- the extern "C" entry points declared in include/moe.h.
+//
+// Host side only: argument checks, workspace carving and the launch sequence
+// of each operation.  Nothing here allocates, frees or synchronises.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int sms = 0;
+    bool ok = false;
+};
+
+DeviceInfo &device_info(int dev) {
+    static DeviceInfo info[kMaxDevices];
+    static std::once_flag once[kMaxDevices];
+    std::call_once(once[dev], [dev] {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) == cudaSuccess) {
+            info[dev].sms = prop.multiProcessorCount;
+            info[dev].ok = prop.major == 10;   // the sm_100 family (sm_103a build)
+        }
+    });
+    return info[dev];
+}
+
+bool current_device_ok() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return false;
+    }
+    return device_info(dev).ok;
+}
+
+inline bool a16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+#define MOE_TRY(expr)                                   \
+    do {                                                \
+        cudaError_t err_ = (expr);                      \
+        if (err_ != cudaSuccess) return MOE_ERR_CUDA;   \
+    } while (0)
+
+// Layout of the layer workspace (offsets in bytes, each 256-aligned).
+struct LayerWs {
+    size_t xn = 0, logits = 0, idx = 0, w = 0, hist = 0, counts = 0, offsets = 0, row_idx = 0,
+           expanded_x = 0, act = 0, y = 0, act_s = 0, y_s = 0, total = 0;
+};
+
+LayerWs layer_layout(const moe_desc_t &d) {
+    LayerWs L;
+    const size_t T = d.T, H = d.H, E = d.E, k = d.k, I = d.I, Is = d.I_shared;
+    const size_t N = T * k;
+    const size_t B = static_cast<size_t>(ceil_div(d.T, kChunkTokens));
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += align256(bytes);
+        return o;
+    };
+    if (d.flags & MOE_RMSNORM) L.xn = take(T * H * 2);
+    if (d.E > kRouterExperts) L.logits = take(T * E * 4);
+    L.idx = take(N * 4);
+    L.w = take(N * 4);
+    L.hist = take(B * E * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.row_idx = take(N * 4);
+    L.expanded_x = take(N * H * 2);
+    L.act = take(N * I * 2);
+    L.y = take(N * H * 2);
+    if (d.flags & MOE_SHARED) {
+        L.act_s = take(T * Is * 2);
+        L.y_s = take(T * H * 4);
+    }
+    L.total = off;
+    return L;
+}
+
+moe_status_t check_desc(const moe_desc_t *d) {
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (d->T < 0 || d->H <= 0 || d->E <= 0 || d->k <= 0 || d->I <= 0) return MOE_ERR_INVALID_ARG;
+    if (d->E > 1024 || d->k > 32 || d->k > d->E) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (d->H % 128 != 0 || d->I % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<int64_t>(d->T) * d->k >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (d->flags & MOE_SHARED) {
+        if (d->I_shared <= 0) return MOE_ERR_INVALID_ARG;
+        if (d->I_shared % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    }
+    if ((d->flags & MOE_RMSNORM) && !(d->rms_eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+}  // namespace
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    const int s = device_info(dev).sms;
+    return s > 0 ? s : 148;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_NO_DEVICE: return "MOE_ERR_NO_DEVICE";
+        default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+moe_status_t moe_rmsnorm_gate(const moe_bf16_t *x, const moe_bf16_t *gamma, const float *wg,
+                              const float *gate_bias, int32_t T, int32_t H, int32_t E, float eps,
+                              uint32_t flags, moe_bf16_t *xn, float *logits,
+                              moe_stream_t stream) {
+    const bool rms = (flags & MOE_RMSNORM) != 0;
+    if (T < 0 || H <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+    if (H % 64 != 0 || E > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!x || !wg || !logits || (rms && !xn)) return MOE_ERR_INVALID_ARG;
+    if (!a16(x) || !a16(wg) || (rms && !a16(xn)) || (gamma && !a16(gamma)) || (rms && !(eps >= 0)))
+        return MOE_ERR_INVALID_ARG;
+    if (!current_device_ok()) return MOE_ERR_NO_DEVICE;
+    MOE_TRY(launch_router(x, rms ? gamma : nullptr, wg, gate_bias, T, H, E, eps, rms,
+                          rms ? xn : nullptr, logits, false, 1, false, nullptr, nullptr, nullptr,
+                          nullptr, reinterpret_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+moe_status_t moe_gate_topk(const float *logits, int32_t T, int32_t E, int32_t k, uint32_t flags,
+                           int32_t *topk_idx, float *topk_w, moe_stream_t stream) {
+    if (T < 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    if (E > 1024 || k > 32 || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!current_device_ok()) return MOE_ERR_NO_DEVICE;
+    MOE_TRY(launch_topk(logits, T, E, k, (flags & MOE_RENORM) != 0, topk_idx, topk_w,
+                        reinterpret_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+moe_status_t moe_init_routing_workspace_size(int32_t T, int32_t k, int32_t E, size_t *bytes) {
+    if (!bytes || T < 0 || k <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+    *bytes = align256(static_cast<size_t>(ceil_div(T, kChunkTokens)) * E * 4);
+    return MOE_OK;
+}
+
+moe_status_t moe_init_routing(const int32_t *topk_idx, const moe_bf16_t *x, int32_t T, int32_t H,
+                              int32_t E, int32_t k, moe_bf16_t *expanded_x,
+                              int32_t *expanded_row_idx, int32_t *src_token,
+                              int32_t *sorted_expert_ids, int32_t *counts, int32_t *offsets,
+                              void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                              moe_stream_t stream) {
+    if (T < 0 || E <= 0 || k <= 0 || H < 0) return MOE_ERR_INVALID_ARG;
+    if (E > 1024 || k > 32 || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<int64_t>(T) * k >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !expanded_row_idx || !src_token)) return MOE_ERR_INVALID_ARG;
+    if (expanded_x) {
+        if (!x || H <= 0) return MOE_ERR_INVALID_ARG;
+        if (H % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+        if (!a16(x) || !a16(expanded_x)) return MOE_ERR_INVALID_ARG;
+    }
+    size_t need = 0;
+    moe_init_routing_workspace_size(T, k, E, &need);
+    if (T > 0 && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (!current_device_ok()) return MOE_ERR_NO_DEVICE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t *hist = static_cast<int32_t *>(workspace);
+    const int B = static_cast<int>(ceil_div(T, kChunkTokens));
+    if (T == 0) {
+        MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s));
+        MOE_TRY(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s));
+        return MOE_OK;
+    }
+    MOE_TRY(launch_route_hist(topk_idx, T, k, E, hist, dev_status, s));
+    MOE_TRY(launch_route_scan(hist, B, E, counts, offsets, s));
+    MOE_TRY(launch_route_scatter(topk_idx, hist, T, k, E, expanded_row_idx, src_token,
+                                 sorted_expert_ids, dev_status, s));
+    if (expanded_x) MOE_TRY(launch_permute(x, expanded_row_idx, T, H, k, expanded_x, s));
+    return MOE_OK;
+}
+
+moe_status_t moe_expert_tokens(const int32_t *sorted_expert_ids, int32_t n, int32_t E,
+                               int32_t *counts, int32_t *offsets, int32_t *dev_status,
+                               moe_stream_t stream) {
+    if (n < 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+    if (E > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!counts || !offsets || (n > 0 && !sorted_expert_ids)) return MOE_ERR_INVALID_ARG;
+    if (!current_device_ok()) return MOE_ERR_NO_DEVICE;
+    MOE_TRY(launch_expert_tokens(sorted_expert_ids, n, E, counts, offsets, dev_status,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+moe_status_t moe_grouped_mlp(const moe_bf16_t *expanded_x, const int32_t *offsets, int32_t G,
+                             const moe_bf16_t *w13, const moe_bf16_t *w2, int32_t n, int32_t H,
+                             int32_t I, moe_bf16_t *act, moe_bf16_t *y, int32_t *dev_status,
+                             moe_stream_t stream) {
+    if (G <= 0 || n < 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+    if (G > 1024 || H % 128 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!offsets || !w13 || !w2) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    if (!expanded_x || !act || !y) return MOE_ERR_INVALID_ARG;
+    if (!a16(expanded_x) || !a16(w13) || !a16(w2) || !a16(act) || !a16(y))
+        return MOE_ERR_INVALID_ARG;
+    if (!current_device_ok()) return MOE_ERR_NO_DEVICE;
+    if (!tensor_maps_available()) return MOE_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    GemmSegment1 none;
+    MOE_TRY(launch_gemm_swiglu(expanded_x, offsets, G, n, H, w13, I, act, none, dev_status, s));
+    MOE_TRY(launch_gemm_store(act, offsets, G, n, I, w2, H, y, none, dev_status, s));
+    return MOE_OK;
+}
+
+moe_status_t moe_finalize_routing(const moe_bf16_t *y_exp, const int32_t *expanded_row_idx,
+                                  const float *topk_w, const void *shared, int32_t T, int32_t H,
+                                  int32_t k, uint32_t flags, void *out, moe_stream_t stream) {
+    if (T < 0 || H <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0 || k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!y_exp || !expanded_row_idx || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    if (!a16(y_exp) || !a16(out) || (shared && !a16(shared))) return MOE_ERR_INVALID_ARG;
+    if (!current_device_ok()) return MOE_ERR_NO_DEVICE;
+    MOE_TRY(launch_finalize(y_exp, expanded_row_idx, topk_w, shared,
+                            (flags & MOE_SHARED_F32) != 0, T, H, k, out,
+                            (flags & MOE_OUT_F32) != 0, reinterpret_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+moe_status_t moe_layer_workspace_size(const moe_desc_t *desc, size_t *bytes) {
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    const moe_status_t st = check_desc(desc);
+    if (st != MOE_OK) return st;
+    *bytes = layer_layout(*desc).total;
+    return MOE_OK;
+}
+
+moe_status_t moe_layer_forward(const moe_desc_t *desc, const moe_bf16_t *x,
+                               const moe_bf16_t *gamma, const float *wg, const float *gate_bias,
+                               const moe_bf16_t *w13, const moe_bf16_t *w2,
+                               const moe_bf16_t *w13_s, const moe_bf16_t *w2_s, void *out,
+                               void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                               moe_stream_t stream) {
+    return moe_layer_forward_timed(desc, x, gamma, wg, gate_bias, w13, w2, w13_s, w2_s, out,
+                                   workspace, workspace_bytes, dev_status, stream, nullptr);
+}
+
+moe_status_t moe_layer_forward_timed(const moe_desc_t *desc, const moe_bf16_t *x,
+                                     const moe_bf16_t *gamma, const float *wg,
+                                     const float *gate_bias, const moe_bf16_t *w13,
+                                     const moe_bf16_t *w2, const moe_bf16_t *w13_s,
+                                     const moe_bf16_t *w2_s, void *out, void *workspace,
+                                     size_t workspace_bytes, int32_t *dev_status,
+                                     moe_stream_t stream, void *const *stage_events) {
+    moe_status_t st = check_desc(desc);
+    if (st != MOE_OK) return st;
+    const moe_desc_t d = *desc;
+    const bool rms = (d.flags & MOE_RMSNORM) != 0;
+    const bool shared = (d.flags & MOE_SHARED) != 0;
+    if (!wg || !w13 || !w2 || (shared && (!w13_s || !w2_s))) return MOE_ERR_INVALID_ARG;
+    if (d.T == 0) return MOE_OK;
+    if (!x || !out) return MOE_ERR_INVALID_ARG;
+    if (!a16(x) || !a16(wg) || !a16(w13) || !a16(w2) || !a16(out) || (gamma && !a16(gamma)) ||
+        (shared && (!a16(w13_s) || !a16(w2_s))))
+        return MOE_ERR_INVALID_ARG;
+    const LayerWs L = layer_layout(d);
+    if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (!current_device_ok()) return MOE_ERR_NO_DEVICE;
+    if (!tensor_maps_available()) return MOE_ERR_CUDA;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    auto at = [&](size_t off) { return static_cast<void *>(ws + off); };
+    uint16_t *xn = rms ? static_cast<uint16_t *>(at(L.xn)) : nullptr;
+    float *logits = d.E > kRouterExperts ? static_cast<float *>(at(L.logits)) : nullptr;
+    int32_t *idx = static_cast<int32_t *>(at(L.idx));
+    float *w = static_cast<float *>(at(L.w));
+    int32_t *hist = static_cast<int32_t *>(at(L.hist));
+    int32_t *counts = static_cast<int32_t *>(at(L.counts));
+    int32_t *offsets = static_cast<int32_t *>(at(L.offsets));
+    int32_t *row_idx = static_cast<int32_t *>(at(L.row_idx));
+    uint16_t *ex = static_cast<uint16_t *>(at(L.expanded_x));
+    uint16_t *act = static_cast<uint16_t *>(at(L.act));
+    uint16_t *y = static_cast<uint16_t *>(at(L.y));
+    uint16_t *act_s = shared ? static_cast<uint16_t *>(at(L.act_s)) : nullptr;
+    float *y_s = shared ? static_cast<float *>(at(L.y_s)) : nullptr;
+    const uint16_t *xs = rms ? xn : x;
+    const bool renorm = (d.flags & MOE_RENORM) != 0;
+    const int T = d.T, H = d.H, E = d.E, k = d.k, I = d.I;
+    const int N = T * k;
+    const int B = static_cast<int>(ceil_div(T, kChunkTokens));
+
+    auto mark = [&](int i) -> cudaError_t {
+        if (!stage_events) return cudaSuccess;
+        return cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s);
+    };
+
+    // 1. RMSNorm + gate (+ top-k + routing histogram when E <= 64)
+    MOE_TRY(mark(0));
+    const bool fuse = E <= kRouterExperts;
+    MOE_TRY(launch_router(x, rms ? gamma : nullptr, wg, gate_bias, T, H, E, d.rms_eps, rms, xn,
+                          logits, fuse, k, renorm, idx, w, fuse ? hist : nullptr, dev_status, s));
+    if (!fuse) {
+        MOE_TRY(launch_topk(logits, T, E, k, renorm, idx, w, s));
+        MOE_TRY(launch_route_hist(idx, T, k, E, hist, dev_status, s));
+    }
+    // 2. init_routing: scan + stable scatter, then the row copies
+    MOE_TRY(mark(1));
+    MOE_TRY(launch_route_scan(hist, B, E, counts, offsets, s));
+    MOE_TRY(launch_route_scatter(idx, hist, T, k, E, row_idx, nullptr, nullptr, dev_status, s));
+    MOE_TRY(mark(2));
+    MOE_TRY(launch_permute(xs, row_idx, T, H, k, ex, s));
+    // 3. grouped w13 + SwiGLU (the shared expert rides along as a dense segment)
+    GemmSegment1 s1;
+    if (shared) {
+        s1.A = xs;
+        s1.B = w13_s;
+        s1.rows = T;
+        s1.K1 = H;
+        s1.N1 = d.I_shared;
+        s1.out = act_s;
+    }
+    MOE_TRY(mark(3));
+    MOE_TRY(launch_gemm_swiglu(ex, offsets, E, N, H, w13, I, act, s1, dev_status, s));
+    // 4. grouped down projection (shared expert output kept in fp32)
+    GemmSegment1 s2;
+    if (shared) {
+        s2.A = act_s;
+        s2.B = w2_s;
+        s2.rows = T;
+        s2.K1 = d.I_shared;
+        s2.N1 = H;
+        s2.out = y_s;
+        s2.out_f32 = true;
+    }
+    MOE_TRY(mark(4));
+    MOE_TRY(launch_gemm_store(act, offsets, E, N, I, w2, H, y, s2, dev_status, s));
+    // 5. finalize: weighted sum in slot order + shared row
+    MOE_TRY(mark(5));
+    MOE_TRY(launch_finalize(y, row_idx, w, y_s, true, T, H, k, out,
+                            (d.flags & MOE_OUT_F32) != 0, s));
+    MOE_TRY(mark(6));
+    return MOE_OK;
+}
+
+}  // extern "C"

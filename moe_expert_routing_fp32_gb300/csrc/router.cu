@@ -1,0 +1,452 @@
+// router.cu -- RMSNorm, fp32 gate and GatingTopK.
+//
+// "NPU HunyuanImage-3.0模型推理优化实践": "RmsNorm算子优化" (RMSNorm before
+// the MoE block), "消除gate计算冗余cast算子" (the gate runs in fp32 on the
+// hidden states cast to float, autocast off) and "MoE EP优化" (GatingTopK).
+//
+// One CTA owns 32 tokens and 64 experts:
+//   phase 1 (RMSNorm only): the 32 rows stream through shared memory in
+//     512-byte pieces (TMA bulk copies, 3-stage ring); warp 0 keeps one fp32
+//     sum of squares per token, accumulated in ascending h;
+//   phase 2: 32-wide slices of the normalised rows (bf16-rounded, then fp32)
+//     and of the gate weight are staged in shared memory; every thread owns
+//     4 tokens x 4 experts and accumulates each logit with one FMA per term
+//     in ascending h.  These are the same fp32 operations in the same order
+//     as a plain sequential loop, so the logits (and every routing decision
+//     taken on them) are bit-identical to it;
+//   phase 3 (E <= 64): warp-per-token top-k / softmax, the routing
+//     histogram of the 32-token chunk, and the logits row write-out.
+// The gate is plain fp32 FMA work (2*T*H*E flops); it does not use tensor
+// cores, whose fp32-input mode (tf32) would round the inputs.
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int RT_THREADS = 128;
+constexpr int RT_TOK = kChunkTokens;     // 32
+constexpr int RT_EXP = kRouterExperts;   // 64
+constexpr int SS_HC = 256;               // h per sum-of-squares piece
+constexpr int SS_ROW = SS_HC * 2 + 16;   // padded smem row (bytes)
+constexpr int SS_STAGES = 3;
+constexpr int G_HC = 32;                 // h per gate slice
+constexpr int G_LD = 36;                 // padded fp32 row stride
+
+constexpr int SMEM_SS = SS_STAGES * RT_TOK * SS_ROW;                       // 50688
+constexpr int SMEM_XS = 2 * RT_TOK * G_LD * 4;                             // 9216
+constexpr int SMEM_WS = 2 * RT_EXP * G_LD * 4;                             // 18432
+constexpr int SMEM_LG = RT_TOK * (RT_EXP + 1) * 4;                         // 8320
+constexpr int SMEM_MAIN = SMEM_SS > (SMEM_XS + SMEM_WS) ? SMEM_SS : (SMEM_XS + SMEM_WS);
+constexpr int SMEM_TOTAL = SMEM_MAIN + SMEM_LG + 64 * 8 /*bars*/ + RT_TOK * 4 + RT_EXP * 4 + 16;
+
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+    return va > vb || (va == vb && ia < ib);
+}
+
+// Warp-wide top-k over values spread as v[i] = value of expert lane + 32*i
+// (-inf where the expert does not exist).  Lane j < k receives slot j's
+// expert in *sel_e and its logit in *sel_v.
+template <int NV>
+__device__ __forceinline__ void warp_topk(const float (&v)[NV], int k, int *sel_e,
+                                          float *sel_v) {
+    const int lane = threadIdx.x & 31;
+    uint32_t taken = 0;
+    *sel_e = -1;
+    *sel_v = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int e = lane + 32 * i;
+            if (!((taken >> i) & 1u) && better(v[i], e, bv, bi)) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (better(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+            *sel_e = bi;
+            *sel_v = bv;
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float s) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    return s;
+}
+
+// Softmax weights of the chosen slots.  Lane j < k holds slot j (sel_v); m is
+// slot 0's logit (the row maximum).  renorm: divide by the sum over the k
+// chosen; otherwise by the sum over all experts (v[], -inf for absent ones).
+template <int NV>
+__device__ __forceinline__ float slot_weight(const float (&v)[NV], int k, bool renorm,
+                                             float sel_v) {
+    const int lane = threadIdx.x & 31;
+    const float m = __shfl_sync(0xffffffffu, sel_v, 0);
+    const float ej = lane < k ? expf(sel_v - m) : 0.0f;
+    float den;
+    if (renorm) {
+        den = warp_sum(ej);
+    } else {
+        float s = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) s += expf(v[i] - m);   // exp(-inf) = 0
+        den = warp_sum(s);
+    }
+    return ej / den;
+}
+
+__global__ void __launch_bounds__(RT_THREADS)
+router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
+              const float *__restrict__ wg, const float *__restrict__ gate_bias, int T, int H,
+              int E, float eps, int rmsnorm, uint16_t *__restrict__ xn,
+              float *__restrict__ logits, int fuse_topk, int k, int renorm,
+              int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+              int32_t *__restrict__ hist, int32_t *dev_status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *ss_buf = smem;                                        // phase 1
+    float *xs = reinterpret_cast<float *>(smem);                   // phase 2
+    float *ws = reinterpret_cast<float *>(smem + SMEM_XS);
+    float *lg = reinterpret_cast<float *>(smem + SMEM_MAIN);       // phase 3
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SMEM_MAIN + SMEM_LG);
+    uint64_t *full = bars;                 // [SS_STAGES]
+    uint64_t *empty = bars + SS_STAGES;    // [SS_STAGES]
+    float *s_r = reinterpret_cast<float *>(bars + 64);
+    int *s_cnt = reinterpret_cast<int *>(s_r + RT_TOK);
+    volatile int *s_abort = s_cnt + RT_EXP;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int tok0 = blockIdx.x * RT_TOK;
+    const int e0 = blockIdx.y * RT_EXP;
+    const int ntok = min(RT_TOK, T - tok0);
+
+    if (tid == 0) {
+        *s_abort = 0;
+        for (int s = 0; s < SS_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        fence_barrier_init();
+    }
+    if (tid < RT_EXP) s_cnt[tid] = 0;
+    if (tid < RT_TOK) s_r[tid] = 1.0f;
+    __syncthreads();
+
+    // ---------------- phase 1: r = 1/sqrt(mean(x^2) + eps) per token
+    if (rmsnorm) {
+        const int npieces = (H + SS_HC - 1) / SS_HC;
+        if (warp == 1) {
+            // producer: lane t copies token t's piece of every stage
+            uint32_t phase = 0;
+            int armed[SS_STAGES];
+            for (int s = 0; s < SS_STAGES; ++s) armed[s] = -1;
+            for (int c = 0, s = 0; c < npieces; ++c) {
+                if (!mbar_wait_bounded(&empty[s], phase ^ 1, s_abort, dev_status)) break;
+                armed[s] = static_cast<int>(phase);
+                const int h0 = c * SS_HC;
+                const int bytes = min(SS_HC, H - h0) * 2;
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes * ntok);
+                __syncwarp();
+                if (lane < ntok) {
+                    const uint16_t *src = x + static_cast<size_t>(tok0 + lane) * H + h0;
+                    uint8_t *dst = ss_buf + (s * RT_TOK + lane) * SS_ROW;
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                        " [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+                        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+                        "r"(smem_u32(&full[s]))
+                        : "memory");
+                }
+                if (++s == SS_STAGES) {
+                    s = 0;
+                    phase ^= 1;
+                }
+            }
+            if (*s_abort) {
+                // unwinding: let every copy this warp started land first
+                for (int s = 0; s < SS_STAGES; ++s)
+                    if (armed[s] >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>(armed[s]));
+            }
+        } else if (warp == 0) {
+            // consumer: lane t sums token t's squares in ascending h
+            float ss = 0.0f;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int c = 0, s = 0; c < npieces; ++c) {
+                if (!mbar_wait_bounded(&full[s], phase, s_abort, dev_status)) {
+                    ok = false;
+                    break;
+                }
+                const int nv = min(SS_HC, H - c * SS_HC) / 8;
+                const uint8_t *row = ss_buf + (s * RT_TOK + lane) * SS_ROW;
+                for (int v = 0; v < nv; ++v) {
+                    const uint4 q = *reinterpret_cast<const uint4 *>(row + v * 16);
+                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float a = __uint_as_float(w[i] << 16);
+                        const float b = __uint_as_float(w[i] & 0xFFFF0000u);
+                        ss = __fmaf_rn(a, a, ss);
+                        ss = __fmaf_rn(b, b, ss);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                if (++s == SS_STAGES) {
+                    s = 0;
+                    phase ^= 1;
+                }
+            }
+            if (ok) {
+                const float mean = __fdiv_rn(ss, static_cast<float>(H));
+                s_r[lane] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+            }
+        }
+        __syncthreads();
+        if (*s_abort) return;
+    }
+
+    // ---------------- phase 2: logits
+    const int ty = tid >> 4, tx = tid & 15;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+
+    const int lt = tid >> 2, lg4 = tid & 3;           // x slice loader: token, 8-h group
+    const bool write_xn = rmsnorm && xn != nullptr && blockIdx.y == 0;
+    const float r_t = s_r[lt];
+    const int nslices = H / G_HC;
+
+    uint4 xq;
+    uint4 wq[4];
+    auto load_slice = [&](int c) {
+        const int h0 = c * G_HC;
+        if (lt < ntok)
+            xq = *reinterpret_cast<const uint4 *>(x + static_cast<size_t>(tok0 + lt) * H + h0 +
+                                                  8 * lg4);
+        else
+            xq = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int e = e0 + p * 16 + (tid >> 3);
+            if (e < E)
+                wq[p] = *reinterpret_cast<const uint4 *>(wg + static_cast<size_t>(e) * H + h0 +
+                                                         4 * (tid & 7));
+            else
+                wq[p] = make_uint4(0, 0, 0, 0);
+        }
+    };
+    auto store_slice = [&](int c, int buf) {
+        const int h0 = c * G_HC;
+        const uint32_t w[4] = {xq.x, xq.y, xq.z, xq.w};
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+        if (rmsnorm) {
+            float gm[8];
+            if (gamma) {
+                const uint4 gq = *reinterpret_cast<const uint4 *>(gamma + h0 + 8 * lg4);
+                const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    gm[2 * i] = __uint_as_float(gw[i] << 16);
+                    gm[2 * i + 1] = __uint_as_float(gw[i] & 0xFFFF0000u);
+                }
+            }
+            uint32_t packed[4];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float v = __fmul_rn(f[i], r_t);
+                if (gamma) v = __fmul_rn(v, gm[i]);
+                const uint16_t b = float_to_bf16_bits(v);
+                f[i] = bf16_bits_to_float(b);
+                if (i & 1)
+                    packed[i >> 1] |= static_cast<uint32_t>(b) << 16;
+                else
+                    packed[i >> 1] = b;
+            }
+            if (write_xn && lt < ntok)
+                *reinterpret_cast<uint4 *>(xn + static_cast<size_t>(tok0 + lt) * H + h0 +
+                                           8 * lg4) =
+                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+        float *xd = xs + (buf * RT_TOK + lt) * G_LD + 8 * lg4;
+        *reinterpret_cast<float4 *>(xd) = make_float4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<float4 *>(xd + 4) = make_float4(f[4], f[5], f[6], f[7]);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            float *wd = ws + (buf * RT_EXP + p * 16 + (tid >> 3)) * G_LD + 4 * (tid & 7);
+            *reinterpret_cast<uint4 *>(wd) = wq[p];
+        }
+    };
+
+    load_slice(0);
+    store_slice(0, 0);
+    __syncthreads();
+    for (int c = 0; c < nslices; ++c) {
+        const int buf = c & 1;
+        if (c + 1 < nslices) load_slice(c + 1);
+        const float *xb = xs + buf * RT_TOK * G_LD;
+        const float *wb = ws + buf * RT_EXP * G_LD;
+#pragma unroll
+        for (int hh = 0; hh < G_HC; hh += 4) {
+            float4 xv[4], wv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                xv[i] = *reinterpret_cast<const float4 *>(xb + (ty + 8 * i) * G_LD + hh);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                wv[j] = *reinterpret_cast<const float4 *>(wb + (tx + 16 * j) * G_LD + hh);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[i][j] = __fmaf_rn(xv[i].x, wv[j].x, acc[i][j]);
+                    acc[i][j] = __fmaf_rn(xv[i].y, wv[j].y, acc[i][j]);
+                    acc[i][j] = __fmaf_rn(xv[i].z, wv[j].z, acc[i][j]);
+                    acc[i][j] = __fmaf_rn(xv[i].w, wv[j].w, acc[i][j]);
+                }
+        }
+        if (c + 1 < nslices) store_slice(c + 1, buf ^ 1);
+        __syncthreads();
+    }
+
+    // ---------------- phase 3: bias, logits out, top-k, histogram
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = e0 + tx + 16 * j;
+            float v = acc[i][j];
+            if (gate_bias && e < E) v = __fadd_rn(v, gate_bias[e]);
+            lg[(ty + 8 * i) * (RT_EXP + 1) + tx + 16 * j] = v;
+        }
+    __syncthreads();
+    if (logits) {
+        const int ne = min(RT_EXP, E - e0);
+        for (int idx = tid; idx < ntok * ne; idx += RT_THREADS) {
+            const int t = idx / ne, e = idx % ne;
+            logits[static_cast<size_t>(tok0 + t) * E + e0 + e] = lg[t * (RT_EXP + 1) + e];
+        }
+    }
+    if (!fuse_topk) return;
+
+    for (int t = warp; t < ntok; t += RT_THREADS / 32) {
+        float v[2];
+        v[0] = lane < E ? lg[t * (RT_EXP + 1) + lane] : -INFINITY;
+        v[1] = lane + 32 < E ? lg[t * (RT_EXP + 1) + lane + 32] : -INFINITY;
+        int sel_e;
+        float sel_v;
+        warp_topk<2>(v, k, &sel_e, &sel_v);
+        const float w = slot_weight<2>(v, k, renorm != 0, sel_v);
+        if (lane < k) {
+            const size_t a = static_cast<size_t>(tok0 + t) * k + lane;
+            topk_idx[a] = sel_e;
+            topk_w[a] = w;
+            atomicAdd(&s_cnt[sel_e], 1);
+        }
+    }
+    if (hist) {
+        __syncthreads();
+        for (int e = tid; e < E; e += RT_THREADS)
+            hist[static_cast<size_t>(blockIdx.x) * E + e] = s_cnt[e];
+    }
+}
+
+template <int NV>
+__global__ void __launch_bounds__(256)
+topk_kernel(const float *__restrict__ logits, int T, int E, int k, int renorm,
+            int32_t *__restrict__ topk_idx, float *__restrict__ topk_w) {
+    const int lane = threadIdx.x & 31;
+    const int warps = blockDim.x >> 5;
+    for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T; t += gridDim.x * warps) {
+        float v[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = e < E ? logits[static_cast<size_t>(t) * E + e] : -INFINITY;
+        }
+        int sel_e;
+        float sel_v;
+        warp_topk<NV>(v, k, &sel_e, &sel_v);
+        const float w = slot_weight<NV>(v, k, renorm != 0, sel_v);
+        if (lane < k) {
+            topk_idx[static_cast<size_t>(t) * k + lane] = sel_e;
+            topk_w[static_cast<size_t>(t) * k + lane] = w;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float *wg,
+                          const float *gate_bias, int T, int H, int E, float eps, bool rmsnorm,
+                          uint16_t *xn, float *logits, bool fuse_topk, int k, bool renorm,
+                          int32_t *topk_idx, float *topk_w, int32_t *hist,
+                          int32_t *dev_status, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(router_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_TOTAL);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    dim3 grid(static_cast<unsigned>(ceil_div(T, RT_TOK)),
+              static_cast<unsigned>(ceil_div(E, RT_EXP)));
+    router_kernel<<<grid, RT_THREADS, SMEM_TOTAL, stream>>>(
+        x, gamma, wg, gate_bias, T, H, E, eps, rmsnorm ? 1 : 0, xn, logits,
+        fuse_topk ? 1 : 0, k, renorm ? 1 : 0, topk_idx, topk_w, hist, dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float *logits, int T, int E, int k, bool renorm,
+                        int32_t *topk_idx, float *topk_w, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int threads = 256;
+    const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(T, threads / 32), 152 * 16));
+    const int nv = static_cast<int>(ceil_div(E, 32));
+    const int rn = renorm ? 1 : 0;
+    if (nv <= 1)
+        topk_kernel<1><<<blocks, threads, 0, stream>>>(logits, T, E, k, rn, topk_idx, topk_w);
+    else if (nv <= 2)
+        topk_kernel<2><<<blocks, threads, 0, stream>>>(logits, T, E, k, rn, topk_idx, topk_w);
+    else if (nv <= 4)
+        topk_kernel<4><<<blocks, threads, 0, stream>>>(logits, T, E, k, rn, topk_idx, topk_w);
+    else if (nv <= 8)
+        topk_kernel<8><<<blocks, threads, 0, stream>>>(logits, T, E, k, rn, topk_idx, topk_w);
+    else if (nv <= 16)
+        topk_kernel<16><<<blocks, threads, 0, stream>>>(logits, T, E, k, rn, topk_idx, topk_w);
+    else
+        topk_kernel<32><<<blocks, threads, 0, stream>>>(logits, T, E, k, rn, topk_idx, topk_w);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

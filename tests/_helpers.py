@@ -1,0 +1,63 @@
+"""Shared helpers of the test suite: conversions and the output tolerances.
+
+Tolerances (layer outputs): the fp32 output mode must be within max-abs 2e-2
+and relative-L2 5e-3 of the oracle's double result; the bf16 output mode may
+in addition be off by half a bf16 ulp of the oracle value (its own final
+rounding).  act / y_exp (bf16 intermediates) may differ from the oracle by
+one bf16 ulp where the fp32 tensor-core sum and the oracle's exact sum round
+to neighbouring bf16 values; such flips must stay rare.
+"""
+import numpy as np
+import torch
+
+MAX_ABS = 2e-2
+REL_L2 = 5e-3
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def t2f64(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return bf16_to_f64(u16(t))
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |v| (8 significant bits)."""
+    a = np.maximum(np.abs(v), 2.0**-126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+def check_out(gpu: np.ndarray, ref: np.ndarray, bf16_out: bool, what=""):
+    """Assert the layer-output tolerance; returns (max_abs, rel_l2)."""
+    d = np.abs(gpu - ref)
+    rel = float(np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-30))
+    mx = float(d.max()) if d.size else 0.0
+    if bf16_out:
+        bound = MAX_ABS + 0.5 * bf16_ulp(ref)
+        bad = d > bound
+        assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond 2e-2 + ulp/2, max {mx}"
+    else:
+        assert mx <= MAX_ABS, f"{what}: max-abs {mx} > {MAX_ABS}"
+    assert rel <= REL_L2, f"{what}: rel-L2 {rel} > {REL_L2}"
+    return mx, rel
+
+
+def check_bf16_close(gpu_bits: np.ndarray, ref_bits: np.ndarray, max_flip_frac: float,
+                     what=""):
+    """bf16 tensors equal up to one-ulp flips, which must be rare."""
+    g = bf16_to_f64(gpu_bits)
+    r = bf16_to_f64(ref_bits)
+    d = np.abs(g - r)
+    tol = bf16_ulp(r) * 1.0001 + 1e-38
+    assert np.all(d <= tol), f"{what}: differences beyond one bf16 ulp, max {d.max()}"
+    flips = float(np.mean(d > 0)) if d.size else 0.0
+    assert flips <= max_flip_frac, f"{what}: {flips:.2e} of values flipped one ulp"
+    return flips

@@ -1,0 +1,136 @@
+"""GPU parity of the whole layer (moe_layer_forward through the C ABI)
+against the CPU oracle.
+
+Small workloads are compared on every token.  The full-size workloads
+(T=4096 balanced, T=16384 image-gen block, T=32768 skewed, small batches)
+are run exactly as the benchmark runs them; the oracle recomputes the gate,
+top-k and routing for every token (bit-exact comparison of the step entry
+points on the same inputs) and the layer output for a sample of tokens.
+Inputs of the full-size workloads are drawn on the GPU by the seeded
+generator and copied to the host for the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_routing_fp32_gb300 as moe
+import oracle
+from moe_inputs import WORKLOADS, Workload, make_inputs
+from tests._helpers import check_out, t2f64, u16
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _weights(g):
+    return moe.LayerWeights(wg=g["wg"], w13=g["w13"], w2=g["w2"], gamma=g["gamma"],
+                            gate_bias=g["gate_bias"], w13_s=g["w13_s"], w2_s=g["w2_s"])
+
+
+def _desc(wl, T=None, out_f32=True):
+    return moe.make_desc(wl.T if T is None else T, wl.H, wl.E, wl.k, wl.I, wl.I_s,
+                         rmsnorm=wl.rmsnorm, eps=wl.eps, renorm=wl.renorm, out_f32=out_f32)
+
+
+def _run_layer(wl, g, out_f32, T=None):
+    st = moe.new_status(DEV)
+    out = moe.layer_forward(_desc(wl, T, out_f32), g["x"], _weights(g), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    return out
+
+
+SMALL = [
+    WORKLOADS["tiny"],
+    Workload("small-shared", T=300, H=256, E=16, k=4, I=256, I_s=384, rmsnorm=True,
+             gamma_std=0.1, x_std=1.0),
+    Workload("small-skew", T=257, H=384, E=64, k=8, I=128, x_std=1.0, skew_s=1.2,
+             skew_beta=1.5),
+    Workload("small-wideE", T=129, H=256, E=96, k=6, I=128, I_s=128, rmsnorm=True),
+    Workload("small-one", T=1, H=128, E=4, k=1, I=128),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("out_f32", [True, False], ids=["f32", "bf16"])
+def test_layer_small_all_tokens(wl, out_f32):
+    d = make_inputs(wl, 2)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    out = _run_layer(wl, g, out_f32)
+    ref, ridx, rw = oracle.layer_tokens(d, wl)
+    check_out(t2f64(out), ref, bf16_out=not out_f32, what=wl.name)
+
+
+def test_layer_deterministic_and_workspace_reuse():
+    wl = SMALL[1]
+    d = make_inputs(wl, 4)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    desc = _desc(wl)
+    ws = torch.full((moe.layer_workspace_size(desc),), 0x7F, dtype=torch.uint8, device=DEV)
+    a = moe.layer_forward(desc, g["x"], _weights(g), workspace=ws)
+    ws.fill_(0xFF)
+    b = moe.layer_forward(desc, g["x"], _weights(g), workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_layer_empty_tokens():
+    wl = WORKLOADS["tiny"]
+    d = make_inputs(wl, 0)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    x0 = g["x"][:0]
+    out = moe.layer_forward(_desc(wl, T=0), x0, _weights(g))
+    assert out.shape == (0, wl.H)
+
+
+# ------------------------------------------------------------ full sizes
+FULL = ["balanced-4k", "imagegen-16k", "skewed-32k", "smallbatch-8", "smallbatch-64",
+        "smallbatch-256"]
+
+
+def _sample_tokens(T, n, seed):
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(T, size=min(T, n), replace=False).tolist())
+    pick.update({0, T - 1})
+    return np.array(sorted(pick), dtype=np.int32)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_layer_full_size(name):
+    wl = WORKLOADS[name]
+    g = make_inputs(wl, 0, device=DEV)
+    cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in g.items()}
+
+    # routing over every token, bit-exact given the same inputs
+    xn, logits = moe.rmsnorm_gate(g["x"], g["wg"], g["gamma"], g["gate_bias"], wl.eps,
+                                  rmsnorm=wl.rmsnorm)
+    idx, w = moe.gate_topk(logits, wl.k, wl.renorm)
+    r = moe.init_routing(idx, None, wl.E, with_rows=False)
+    torch.cuda.synchronize()
+    xs_ref = oracle.rmsnorm(cpu["x"], cpu["gamma"], wl.eps) if wl.rmsnorm else u16(cpu["x"])
+    if wl.rmsnorm:
+        assert np.array_equal(u16(xn), xs_ref)
+    lg_ref = oracle.gate_logits(xs_ref, cpu["wg"], cpu["gate_bias"])
+    assert np.array_equal(logits.cpu().numpy().view(np.uint32), lg_ref.view(np.uint32))
+    ridx, rw = oracle.topk_softmax(lg_ref, wl.k, wl.renorm)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=2e-6, atol=2e-7)
+    rr = oracle.init_routing(ridx, wl.E)
+    for key in ("row_idx", "src_token", "counts", "offsets"):
+        assert np.array_equal(r[key].cpu().numpy(), rr[key]), key
+    counts = rr["counts"]
+    if name.startswith("skewed"):
+        print(f"{name}: {int((counts == 0).sum())} idle experts, top share "
+              f"{counts.max() / counts.sum():.4f}")
+
+    # layer output on sampled tokens (fp32 mode strict, bf16 mode + half ulp)
+    tok = _sample_tokens(wl.T, 48, 7)
+    # include tokens routed to the busiest expert
+    busiest = int(np.argmax(counts))
+    hot = np.nonzero((ridx == busiest).any(axis=1))[0][:4]
+    tok = np.unique(np.concatenate([tok, hot]).astype(np.int32))
+    ref, _, _ = oracle.layer_tokens(cpu, wl, tok)
+    for out_f32 in (True, False):
+        out = _run_layer(wl, g, out_f32)
+        got = t2f64(out[torch.from_numpy(tok).long().to(DEV)])
+        check_out(got, ref, bf16_out=not out_f32, what=f"{name} f32={out_f32}")
