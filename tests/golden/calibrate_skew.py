@@ -41,6 +41,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--device", default="cpu")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--out", default=None, help="result file (default: beside this script)")
     args = ap.parse_args()
     wl = WORKLOADS["skewed-32k"]
     d = make_inputs(wl, args.seed, device=args.device, only=("x", "wg"))
@@ -61,8 +62,8 @@ def main():
     res = dict(workload=wl.name, seed=args.seed, device=args.device, beta=beta,
                zero_experts=nz, top_share=float(counts.max() / counts.sum()),
                counts=counts.tolist())
-    out = os.path.join(os.path.dirname(os.path.abspath(__file__)),
-                       "skew_calibration.json")
+    out = args.out or os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                                   "skew_calibration.json")
     with open(out, "w") as f:
         json.dump(res, f, indent=1)
     print(json.dumps({k: v for k, v in res.items() if k != "counts"}))
