@@ -137,6 +137,34 @@ moe_status_t moe_init_routing(const int32_t *topk_idx, const moe_bf16_t *x, int3
                               int32_t *dev_status, moe_stream_t stream);
 
 /*
+ * moe_init_routing without a workspace argument, for callers that cannot
+ * allocate device memory (for example code that only receives input and
+ * output pointers from a host framework that owns all memory, or a context
+ * where a cudaMalloc is not allowed or would stall the device).  The page
+ * has no counterpart of this entry point; it is a convenience of this
+ * library.  Same arguments, results and errors as moe_init_routing.
+ *   - The routing histogram lives in a 1 MiB array inside the library
+ *     (262144 int32), held on every GPU that loads the library until the
+ *     process exits.  A call needs ceil(T/32) * E of its entries; larger
+ *     calls are rejected with MOE_ERR_WORKSPACE_TOO_SMALL (e.g. E = 64 allows
+ *     T up to 131072).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (every entry a call reads it writes first, so nothing needs clearing).
+ *     Calls whose execution overlaps on the GPU (different streams, or
+ *     different host threads) race on it and give wrong results: serialise
+ *     them.
+ * Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ */
+moe_status_t moe_init_routing_noalloc(const int32_t *topk_idx, const moe_bf16_t *x, int32_t T,
+                                      int32_t H, int32_t E, int32_t k, moe_bf16_t *expanded_x,
+                                      int32_t *expanded_row_idx, int32_t *src_token,
+                                      int32_t *sorted_expert_ids, int32_t *counts,
+                                      int32_t *offsets, int32_t *dev_status,
+                                      moe_stream_t stream);
+
+/*
  * compute_expert_tokens ("GMM使能&&Routing优化": how many tokens each expert
  * computes), from the expert ids of the sorted rows:
  *   sorted_expert_ids [n] int32, ascending

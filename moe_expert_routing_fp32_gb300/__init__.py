@@ -32,7 +32,8 @@ RENORM, RMSNORM, SHARED, OUT_F32, SHARED_F32 = 1, 2, 4, 8, 16
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_status_string", "moe_rmsnorm_gate", "moe_gate_topk",
-           "moe_init_routing_workspace_size", "moe_init_routing", "moe_expert_tokens",
+           "moe_init_routing_workspace_size", "moe_init_routing", "moe_init_routing_noalloc",
+           "moe_expert_tokens",
            "moe_grouped_mlp", "moe_finalize_routing", "moe_layer_workspace_size",
            "moe_layer_forward", "moe_layer_forward_timed")
 NUM_STAGES = 6
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
                 "moe_gate_topk": [P, I32, I32, I32, U32, P, P, P],
                 "moe_init_routing_workspace_size": [I32, I32, I32, PSZ],
                 "moe_init_routing": [P, P, I32, I32, I32, I32, P, P, P, P, P, P, P, SZ, P, P],
+                "moe_init_routing_noalloc": [P, P, I32, I32, I32, I32, P, P, P, P, P, P, P, P],
                 "moe_expert_tokens": [P, I32, I32, P, P, P, P],
                 "moe_grouped_mlp": [P, P, I32, P, P, I32, I32, I32, P, P, P, P],
                 "moe_finalize_routing": [P, P, P, P, I32, I32, I32, U32, P, P],
