@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--T", type=int, default=None, help="override the token count")
+    ap.add_argument("--E", type=int, default=None, help="override the expert count")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU work of the oracle baseline sample")
     return ap.parse_args()
@@ -189,28 +192,24 @@ def cpu_oracle_rate(inputs_cpu, wl, seconds, first_token=0):
 def stage_bytes_flops(wl):
     T, H, E, k, I, Is = wl.T, wl.H, wl.E, wl.k, wl.I, wl.I_s
     N = T * k
+    # algorithmic work of each stage (what the step must touch or compute once)
     return {
-        "router": {"bytes": T * H * 2 * (2 if wl.rmsnorm else 1) + E * H * 4 + N * 8 +
-                   (T * H * 2 if wl.rmsnorm else 0), "flops": 2.0 * T * H * E},
+        "router": {"bytes": T * H * 2 + (T * H * 2 if wl.rmsnorm else 0) + E * H * 4 + N * 8,
+                   "gate_flops": 2.0 * T * H * E},
         "permute": {"bytes": T * H * 2 + N * H * 2 + N * 4},
-        "gemm_w13_swiglu": {"flops": 4.0 * N * H * I + 4.0 * T * H * Is,
-                            "bytes": E * 2 * I * H * 2 + 2 * I_s_or0(Is) * H * 2},
+        "gemm_w13_swiglu": {"flops": 4.0 * N * H * I + 4.0 * T * H * Is},
         "gemm_down": {"flops": 2.0 * N * H * I + 2.0 * T * H * Is},
         "finalize": {"bytes": N * H * 2 + (T * H * 4 if Is else 0) + T * H * 2 + N * 8},
     }
 
 
-def I_s_or0(v):
-    return v or 0
-
-
 def run_ours(args, rank, world, local):
     import torch
     import moe_expert_routing_fp32_gb300 as moe
-    from moe_inputs import WORKLOADS, make_inputs
+    from moe_inputs import make_inputs
 
     moe.build()
-    wl = WORKLOADS[args.workload]
+    wl = workload_of(args)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     g = make_inputs(wl, args.seed, device=str(dev))
@@ -261,10 +260,10 @@ def run_ours(args, rank, world, local):
     stage_ms = {}
     for j, name in enumerate(moe.STAGE_NAMES):
         stage_ms[name] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
-    step_ms = elapsed_ms / K
-    value = world * wl.T * K / (elapsed_ms / 1e3)
 
     # end to end on host buffers (pinned), through the same public call
+    if args.no_e2e:
+        return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, None, g)
     x_host = x.cpu().pin_memory()
     out_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, pin_memory=True)
     x_dev = torch.empty_like(x)
@@ -288,7 +287,13 @@ def run_ours(args, rank, world, local):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(t.item())
     e2e_value = world * wl.T * Ke / (e2e_ms / 1e3)
+    return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g)
 
+
+def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g):
+    import moe_expert_routing_fp32_gb300 as moe  # noqa: F401
+    step_ms = elapsed_ms / K
+    value = world * wl.T * K / (elapsed_ms / 1e3)
     peaks, peak_src = load_peaks()
     work = stage_bytes_flops(wl)
     dom = "gemm_w13_swiglu"
@@ -308,6 +313,8 @@ def run_ours(args, rank, world, local):
         if "bytes" in wk and not name.startswith("gemm"):
             e["gbs"] = round(wk["bytes"] / (ms / 1e3) / 1e9, 1)
             e["frac_hbm"] = round(e["gbs"] / hbm_peak, 4)
+        if "gate_flops" in wk:
+            e["gate_fp32_tflops"] = round(wk["gate_flops"] / (ms / 1e3) / 1e12, 2)
         per_stage[name] = e
 
     launches_per_step = 7 + (2 if wl.E > 64 else 0)
@@ -327,8 +334,9 @@ def run_ours(args, rank, world, local):
         "gemm_tflops": round(gemm_tflops, 1),
         "gemm_frac_bf16_peak": round(gemm_tflops / tc_peak, 4),
         "stages": per_stage,
-        "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
-                "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2},
+        "e2e": None if e2e_value is None else {
+            "value": round(e2e_value, 1), "unit": UNIT,
+            "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2},
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }
@@ -342,14 +350,24 @@ def run_ours(args, rank, world, local):
 
 
 # --------------------------------------------------------------- reference arm
+def workload_of(args):
+    from moe_inputs import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    if args.T is not None:
+        wl = wl.replace(T=args.T)
+    if args.E is not None:
+        wl = wl.replace(E=args.E, skew_s=0.0 if args.E != wl.E else wl.skew_s)
+    return wl
+
+
 def run_reference(args):
     import numpy as np
     import torch
-    from moe_inputs import WORKLOADS, make_inputs
+    from moe_inputs import make_inputs
     import oracle
 
     oracle.build()
-    wl = WORKLOADS[args.workload]
+    wl = workload_of(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     g = make_inputs(wl, args.seed, device=dev)     # drawn where it is fast
     cpu = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in g.items()}
