@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--E", type=int, default=None, help="override the expert count")
+    ap.add_argument("--I", type=int, default=None, help="override the expert inter size")
+    ap.add_argument("--Is", type=int, default=None, help="override the shared inter size")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU work of the oracle baseline sample")
     return ap.parse_args()
@@ -134,6 +136,7 @@ class ClockSampler:
                 return None
         sm = [num(r[0]) for r in rows if num(r[0]) is not None]
         mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
         reasons = set()
         for r in rows:
             for name, v in zip(self.REASONS, r[4:8]):
@@ -141,6 +144,7 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
+                "power_w_median": statistics.median(pw) if pw else None,
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
@@ -357,6 +361,10 @@ def workload_of(args):
         wl = wl.replace(T=args.T)
     if args.E is not None:
         wl = wl.replace(E=args.E, skew_s=0.0 if args.E != wl.E else wl.skew_s)
+    if args.I is not None:
+        wl = wl.replace(I=args.I)
+    if args.Is is not None and wl.I_s > 0:
+        wl = wl.replace(I_s=args.Is)
     return wl
 
 

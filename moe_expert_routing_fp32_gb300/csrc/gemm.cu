@@ -14,8 +14,10 @@
 //
 // Tiles are 128 rows x BN columns (SWIGLU: 128 gate + 128 up columns giving
 // 128 act columns).  The tile list is built on the device from `offsets`
-// (no host sync): per group ceil(rows/128) m-blocks x n-blocks, m fastest so
-// CTAs running at the same time share weight tiles through L2.  A tile may
+// (no host sync): per group ceil(rows/128) m-blocks x n-blocks, ordered so
+// that CTAs running at the same time share the larger operand through L2
+// (m fastest when the group has fewer rows than its weight slice, n fastest
+// otherwise, e.g. the shared expert or a very busy expert).  A tile may
 // read rows of the next group; the epilogue stores only the group's rows.
 //
 // CTA roles (192 threads, one CTA per SM):
@@ -60,6 +62,7 @@ struct Params {
     int32_t K0, K1;
     int32_t nt0, nt1;   // n-blocks per m-block
     int32_t half0, half1;
+    int32_t brows0, brows1;  // rows of one group's weight slice (2N for SwiGLU, N for store)
     int32_t rows1;      // 0 = no segment 1
     void *out0;
     int64_t ldo0;
@@ -104,20 +107,26 @@ __device__ __forceinline__ Tile decode_tile(const Params &p, int tile, const int
         const int cnt = s_off[g + 1] - s_off[g];
         const int mt = (cnt + BM - 1) / BM;
         const int local = tile - s_prefix[g];
+        // Keep the larger operand stationary: m fastest when the group's rows
+        // are fewer than its weight slice (weights reused from L2 across
+        // m-blocks), n fastest otherwise (the A rows reused across n-blocks).
+        const bool nfast = cnt > p.brows0;
+        const int m_blk = nfast ? local / p.nt0 : local % mt;
         t.seg = 0;
         t.g = g;
-        t.row0 = s_off[g] + (local % mt) * BM;
+        t.row0 = s_off[g] + m_blk * BM;
         t.row_end = s_off[g + 1];
-        t.n_blk = local / mt;
+        t.n_blk = nfast ? local % p.nt0 : local / mt;
         t.kblocks = p.K0 / BK;
     } else {
         const int local = tile - total0;
         const int mt = (p.rows1 + BM - 1) / BM;
+        const bool nfast = p.rows1 > p.brows1;
         t.seg = 1;
         t.g = 0;
-        t.row0 = (local % mt) * BM;
+        t.row0 = (nfast ? local / p.nt1 : local % mt) * BM;
         t.row_end = p.rows1;
-        t.n_blk = local / mt;
+        t.n_blk = nfast ? local % p.nt1 : local / mt;
         t.kblocks = p.K1 / BK;
     }
     return t;
@@ -492,6 +501,8 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
     p.nt1 = seg1.N1 / 128;
     p.half0 = N;
     p.half1 = seg1.N1;
+    p.brows0 = 2 * N;
+    p.brows1 = 2 * seg1.N1;
     p.rows1 = seg1.rows;
     p.out0 = act;
     p.ldo0 = N;
@@ -530,6 +541,8 @@ cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, 
     p.nt1 = seg1.N1 / BN;
     p.half0 = 0;
     p.half1 = 0;
+    p.brows0 = N;
+    p.brows1 = seg1.N1;
     p.rows1 = seg1.rows;
     p.out0 = y;
     p.ldo0 = N;

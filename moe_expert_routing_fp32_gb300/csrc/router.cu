@@ -6,7 +6,7 @@
 //
 // One CTA owns 32 tokens and 64 experts:
 //   phase 1 (RMSNorm only): the 32 rows stream through shared memory in
-//     512-byte pieces (TMA bulk copies, 3-stage ring); warp 0 keeps one fp32
+//     512-byte pieces (TMA bulk copies, 2-stage ring); warp 0 keeps one fp32
 //     sum of squares per token, accumulated in ascending h;
 //   phase 2: 32-wide slices of the normalised rows (bf16-rounded, then fp32)
 //     and of the gate weight are staged in shared memory; every thread owns
@@ -16,6 +16,8 @@
 //     taken on them) are bit-identical to it;
 //   phase 3 (E <= 64): warp-per-token top-k / softmax, the routing
 //     histogram of the 32-token chunk, and the logits row write-out.
+// Batches of at most 512 tokens use router_small_kernel instead (one CTA per
+// token, one thread per expert), which keeps every SM busy.
 // The gate is plain fp32 FMA work (2*T*H*E flops); it does not use tensor
 // cores, whose fp32-input mode (tf32) would round the inputs.
 #include <math.h>
@@ -33,16 +35,32 @@ constexpr int RT_TOK = kChunkTokens;     // 32
 constexpr int RT_EXP = kRouterExperts;   // 64
 constexpr int SS_HC = 256;               // h per sum-of-squares piece
 constexpr int SS_ROW = SS_HC * 2 + 16;   // padded smem row (bytes)
-constexpr int SS_STAGES = 3;
+constexpr int SS_STAGES = 2;
 constexpr int G_HC = 32;                 // h per gate slice
 constexpr int G_LD = 36;                 // padded fp32 row stride
+constexpr int G_STAGES = 3;              // cp.async ring depth of the gate slices
 
-constexpr int SMEM_SS = SS_STAGES * RT_TOK * SS_ROW;                       // 50688
+constexpr int SMEM_SS = SS_STAGES * RT_TOK * SS_ROW;                       // 33792
+constexpr int WG_STAGE = RT_EXP * G_LD * 4;                                // 9216
+constexpr int XR_STAGE = RT_TOK * G_HC * 2;                                // 2048
 constexpr int SMEM_XS = 2 * RT_TOK * G_LD * 4;                             // 9216
-constexpr int SMEM_WS = 2 * RT_EXP * G_LD * 4;                             // 18432
+constexpr int SMEM_G = G_STAGES * (WG_STAGE + XR_STAGE) + SMEM_XS;         // 43008
 constexpr int SMEM_LG = RT_TOK * (RT_EXP + 1) * 4;                         // 8320
-constexpr int SMEM_MAIN = SMEM_SS > (SMEM_XS + SMEM_WS) ? SMEM_SS : (SMEM_XS + SMEM_WS);
+constexpr int SMEM_MAIN = SMEM_SS > SMEM_G ? SMEM_SS : SMEM_G;
 constexpr int SMEM_TOTAL = SMEM_MAIN + SMEM_LG + 64 * 8 /*bars*/ + RT_TOK * 4 + RT_EXP * 4 + 16;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)),
+                 "l"(reinterpret_cast<uint64_t>(gmem)), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
@@ -121,9 +139,7 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
               int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
               int32_t *__restrict__ hist, int32_t *dev_status) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *ss_buf = smem;                                        // phase 1
-    float *xs = reinterpret_cast<float *>(smem);                   // phase 2
-    float *ws = reinterpret_cast<float *>(smem + SMEM_XS);
+    uint8_t *ss_buf = smem;                                        // phase 1 (phase 2 reuses it)
     float *lg = reinterpret_cast<float *>(smem + SMEM_MAIN);       // phase 3
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SMEM_MAIN + SMEM_LG);
     uint64_t *full = bars;                 // [SS_STAGES]
@@ -197,9 +213,11 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
                     break;
                 }
                 const int nv = min(SS_HC, H - c * SS_HC) / 8;
-                const uint8_t *row = ss_buf + (s * RT_TOK + lane) * SS_ROW;
+                const uint4 *row =
+                    reinterpret_cast<const uint4 *>(ss_buf + (s * RT_TOK + lane) * SS_ROW);
+                uint4 q = row[0];
                 for (int v = 0; v < nv; ++v) {
-                    const uint4 q = *reinterpret_cast<const uint4 *>(row + v * 16);
+                    const uint4 qn = row[v + 1 < nv ? v + 1 : v];   // load ahead of the chain
                     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -208,6 +226,7 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
                         ss = __fmaf_rn(a, a, ss);
                         ss = __fmaf_rn(b, b, ss);
                     }
+                    q = qn;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -226,6 +245,15 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
     }
 
     // ---------------- phase 2: logits
+    // Slices of G_HC columns: the raw x slice (bf16) and the gate-weight slice
+    // (fp32, padded rows) arrive through a G_STAGES-deep cp.async ring; each x
+    // slice is then normalised once into an fp32 buffer (double-buffered).
+    fence_proxy_async();      // phase 1 wrote this memory through the async proxy
+    __syncthreads();
+    uint8_t *wg_ring = smem;
+    uint8_t *xr_ring = smem + G_STAGES * WG_STAGE;
+    float *xs = reinterpret_cast<float *>(smem + G_STAGES * (WG_STAGE + XR_STAGE));
+
     const int ty = tid >> 4, tx = tid & 15;
     float acc[4][4];
 #pragma unroll
@@ -233,32 +261,31 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
 
-    const int lt = tid >> 2, lg4 = tid & 3;           // x slice loader: token, 8-h group
+    const int lt = tid >> 2, lg4 = tid & 3;           // x slice: token, 8-column group
     const bool write_xn = rmsnorm && xn != nullptr && blockIdx.y == 0;
     const float r_t = s_r[lt];
     const int nslices = H / G_HC;
 
-    uint4 xq;
-    uint4 wq[4];
-    auto load_slice = [&](int c) {
+    auto issue = [&](int c) {
+        const int st = c % G_STAGES;
         const int h0 = c * G_HC;
-        if (lt < ntok)
-            xq = *reinterpret_cast<const uint4 *>(x + static_cast<size_t>(tok0 + lt) * H + h0 +
-                                                  8 * lg4);
-        else
-            xq = make_uint4(0, 0, 0, 0);
+        const bool okt = lt < ntok;
+        const uint16_t *xsrc = okt ? x + static_cast<size_t>(tok0 + lt) * H + h0 + 8 * lg4 : x;
+        cp_async16(xr_ring + st * XR_STAGE + lt * (G_HC * 2) + lg4 * 16, xsrc, okt ? 16 : 0);
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-            const int e = e0 + p * 16 + (tid >> 3);
-            if (e < E)
-                wq[p] = *reinterpret_cast<const uint4 *>(wg + static_cast<size_t>(e) * H + h0 +
-                                                         4 * (tid & 7));
-            else
-                wq[p] = make_uint4(0, 0, 0, 0);
+            const int e = p * 16 + (tid >> 3);
+            const bool oke = e0 + e < E;
+            const float *wsrc =
+                oke ? wg + static_cast<size_t>(e0 + e) * H + h0 + 4 * (tid & 7) : wg;
+            cp_async16(wg_ring + st * WG_STAGE + e * (G_LD * 4) + (tid & 7) * 16, wsrc,
+                       oke ? 16 : 0);
         }
     };
-    auto store_slice = [&](int c, int buf) {
+    auto convert = [&](int c, int buf) {
         const int h0 = c * G_HC;
+        const uint4 xq = *reinterpret_cast<const uint4 *>(
+            xr_ring + (c % G_STAGES) * XR_STAGE + lt * (G_HC * 2) + lg4 * 16);
         const uint32_t w[4] = {xq.x, xq.y, xq.z, xq.w};
         float f[8];
 #pragma unroll
@@ -297,21 +324,22 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
         float *xd = xs + (buf * RT_TOK + lt) * G_LD + 8 * lg4;
         *reinterpret_cast<float4 *>(xd) = make_float4(f[0], f[1], f[2], f[3]);
         *reinterpret_cast<float4 *>(xd + 4) = make_float4(f[4], f[5], f[6], f[7]);
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            float *wd = ws + (buf * RT_EXP + p * 16 + (tid >> 3)) * G_LD + 4 * (tid & 7);
-            *reinterpret_cast<uint4 *>(wd) = wq[p];
-        }
     };
 
-    load_slice(0);
-    store_slice(0, 0);
+#pragma unroll
+    for (int c = 0; c < G_STAGES - 1; ++c) {
+        if (c < nslices) issue(c);
+        cp_async_commit();
+    }
+    cp_async_wait<G_STAGES - 2>();
+    __syncthreads();
+    convert(0, 0);
     __syncthreads();
     for (int c = 0; c < nslices; ++c) {
-        const int buf = c & 1;
-        if (c + 1 < nslices) load_slice(c + 1);
-        const float *xb = xs + buf * RT_TOK * G_LD;
-        const float *wb = ws + buf * RT_EXP * G_LD;
+        if (c + G_STAGES - 1 < nslices) issue(c + G_STAGES - 1);
+        cp_async_commit();
+        const float *xb = xs + (c & 1) * RT_TOK * G_LD;
+        const float *wb = reinterpret_cast<const float *>(wg_ring + (c % G_STAGES) * WG_STAGE);
 #pragma unroll
         for (int hh = 0; hh < G_HC; hh += 4) {
             float4 xv[4], wv[4];
@@ -331,7 +359,9 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
                     acc[i][j] = __fmaf_rn(xv[i].w, wv[j].w, acc[i][j]);
                 }
         }
-        if (c + 1 < nslices) store_slice(c + 1, buf ^ 1);
+        cp_async_wait<G_STAGES - 2>();
+        __syncthreads();
+        if (c + 1 < nslices) convert(c + 1, (c + 1) & 1);
         __syncthreads();
     }
 
@@ -377,6 +407,170 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
     }
 }
 
+// Few tokens (T <= 512): one CTA per token and one thread per expert, so
+// that every logit's sequential FMA chain runs at the same time.  The row is
+// kept in shared memory as fp32; thread 0 takes the sum of squares in
+// ascending h; the gate weight streams through a SM_SLOTS-deep cp.async ring
+// in 64-column chunks (rows padded to 68 floats: conflict-free 16-byte
+// reads), filled while the sum of squares runs.
+// Same arithmetic, in the same order, as the tiled kernel above.
+constexpr int SM_HC = 64;
+constexpr int SM_LD = 68;
+constexpr int SM_SLOTS = 4;
+constexpr int SMALL_MAX_T = 512;
+constexpr int SMALL_MAX_E = 128;
+constexpr int SMALL_MAX_H = 8192;
+
+__global__ void __launch_bounds__(128)
+router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
+                    const float *__restrict__ wg, const float *__restrict__ gate_bias, int H,
+                    int E, float eps, int rmsnorm, uint16_t *__restrict__ xn,
+                    float *__restrict__ logits, int fuse_topk, int k, int renorm,
+                    int32_t *__restrict__ topk_idx, float *__restrict__ topk_w) {
+    extern __shared__ __align__(16) float sm[];
+    float *xf = sm;                    // [H]
+    float *ring = sm + H;              // [SM_SLOTS][E][SM_LD]
+    __shared__ float s_r;
+    __shared__ float s_lg[SMALL_MAX_E];
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const int nvec = H / 8;
+
+    const uint4 *xq = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
+    for (int v = tid; v < nvec; v += nthr) {
+        const uint4 q = xq[v];
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+        *reinterpret_cast<float4 *>(xf + 8 * v) = make_float4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<float4 *>(xf + 8 * v + 4) = make_float4(f[4], f[5], f[6], f[7]);
+    }
+    const int nch = H / SM_HC;
+    auto issue = [&](int c) {
+        const int st = c % SM_SLOTS;
+        const int h0 = c * SM_HC;
+        for (int i = tid; i < E * (SM_HC / 4); i += nthr) {
+            const int e = i / (SM_HC / 4), q = i % (SM_HC / 4);
+            cp_async16(ring + (st * E + e) * SM_LD + 4 * q,
+                       wg + static_cast<size_t>(e) * H + h0 + 4 * q, 16);
+        }
+    };
+#pragma unroll
+    for (int c = 0; c < SM_SLOTS - 1; ++c) {
+        if (c < nch) issue(c);
+        cp_async_commit();
+    }
+    __syncthreads();
+
+    if (rmsnorm) {
+        if (tid == 0) {
+            // one sequential chain; the 16-byte loads run ahead of it
+            float ss = 0.0f;
+            const float4 *xv = reinterpret_cast<const float4 *>(xf);
+            float4 cur[4], nxt[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) cur[u] = xv[u];
+            for (int b = 0; b < H / 16; ++b) {
+                if (b + 1 < H / 16) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) nxt[u] = xv[4 * (b + 1) + u];
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    ss = __fmaf_rn(cur[u].x, cur[u].x, ss);
+                    ss = __fmaf_rn(cur[u].y, cur[u].y, ss);
+                    ss = __fmaf_rn(cur[u].z, cur[u].z, ss);
+                    ss = __fmaf_rn(cur[u].w, cur[u].w, ss);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+            }
+            const float mean = __fdiv_rn(ss, static_cast<float>(H));
+            s_r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+        }
+        __syncthreads();
+        const float r = s_r;
+        for (int v = tid; v < nvec; v += nthr) {
+            float gm[8];
+            if (gamma) {
+                const uint4 gq = reinterpret_cast<const uint4 *>(gamma)[v];
+                const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    gm[2 * i] = __uint_as_float(gw[i] << 16);
+                    gm[2 * i + 1] = __uint_as_float(gw[i] & 0xFFFF0000u);
+                }
+            }
+            uint32_t packed[4];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float val = __fmul_rn(xf[8 * v + i], r);
+                if (gamma) val = __fmul_rn(val, gm[i]);
+                const uint16_t b = float_to_bf16_bits(val);
+                xf[8 * v + i] = bf16_bits_to_float(b);
+                if (i & 1)
+                    packed[i >> 1] |= static_cast<uint32_t>(b) << 16;
+                else
+                    packed[i >> 1] = b;
+            }
+            if (xn)
+                reinterpret_cast<uint4 *>(xn + static_cast<size_t>(t) * H)[v] =
+                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+        __syncthreads();
+    }
+
+    const int e = tid;
+    float acc = 0.0f;
+    for (int c = 0; c < nch; ++c) {
+        if (c + SM_SLOTS - 1 < nch) issue(c + SM_SLOTS - 1);
+        cp_async_commit();
+        cp_async_wait<SM_SLOTS - 1>();
+        __syncthreads();
+        if (e < E) {
+            const float *wr = ring + ((c % SM_SLOTS) * E + e) * SM_LD;
+            const float *xc = xf + c * SM_HC;
+#pragma unroll
+            for (int q = 0; q < SM_HC / 4; ++q) {
+                const float4 wv = *reinterpret_cast<const float4 *>(wr + 4 * q);
+                const float4 xv = *reinterpret_cast<const float4 *>(xc + 4 * q);
+                acc = __fmaf_rn(xv.x, wv.x, acc);
+                acc = __fmaf_rn(xv.y, wv.y, acc);
+                acc = __fmaf_rn(xv.z, wv.z, acc);
+                acc = __fmaf_rn(xv.w, wv.w, acc);
+            }
+        }
+        __syncthreads();
+    }
+    if (e < E) {
+        if (gate_bias) acc = __fadd_rn(acc, gate_bias[e]);
+        s_lg[e] = acc;
+        if (logits) logits[static_cast<size_t>(t) * E + e] = acc;
+    }
+    __syncthreads();
+    if (fuse_topk && tid < 32) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int ee = tid + 32 * i;
+            v[i] = ee < E ? s_lg[ee] : -INFINITY;
+        }
+        int sel_e;
+        float sel_v;
+        warp_topk<4>(v, k, &sel_e, &sel_v);
+        const float w = slot_weight<4>(v, k, renorm != 0, sel_v);
+        if (tid < k) {
+            topk_idx[static_cast<size_t>(t) * k + tid] = sel_e;
+            topk_w[static_cast<size_t>(t) * k + tid] = w;
+        }
+    }
+}
+
 template <int NV>
 __global__ void __launch_bounds__(256)
 topk_kernel(const float *__restrict__ logits, int T, int E, int k, int renorm,
@@ -409,6 +603,22 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
                           int32_t *topk_idx, float *topk_w, int32_t *hist,
                           int32_t *dev_status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
+    if (T <= SMALL_MAX_T && E <= SMALL_MAX_E && H <= SMALL_MAX_H) {
+        const int threads = std::max(64, static_cast<int>(ceil_div(E, 32)) * 32);
+        const size_t smem = (static_cast<size_t>(H) + SM_SLOTS * E * SM_LD) * sizeof(float);
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(router_small_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+        }
+        router_small_kernel<<<T, threads, smem, stream>>>(
+            x, gamma, wg, gate_bias, H, E, eps, rmsnorm ? 1 : 0, xn, logits, fuse_topk ? 1 : 0,
+            k, renorm ? 1 : 0, topk_idx, topk_w);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess || !fuse_topk || hist == nullptr) return e;
+        return launch_route_hist(topk_idx, T, k, E, hist, dev_status, stream);
+    }
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);

@@ -48,6 +48,11 @@ SMALL = [
              skew_beta=1.5),
     Workload("small-wideE", T=129, H=256, E=96, k=6, I=128, I_s=128, rmsnorm=True),
     Workload("small-one", T=1, H=128, E=4, k=1, I=128),
+    # > 512 tokens: tiled router with the routing histogram fused in
+    Workload("mid-tiled", T=700, H=256, E=32, k=4, I=128, I_s=128, rmsnorm=True,
+             gamma_std=0.1),
+    # E > 64: separate top-k and histogram launches
+    Workload("mid-wideE", T=640, H=128, E=80, k=5, I=128),
 ]
 
 

@@ -28,6 +28,11 @@ def _cuda(d):
     Workload("g-rms", T=77, H=320, E=13, k=3, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-bias", T=100, H=256, E=64, k=8, I=128, rmsnorm=True, skew_s=1.2, skew_beta=1.0),
     Workload("g-wideE", T=40, H=192, E=160, k=6, I=128, rmsnorm=True),
+    # more than 512 tokens: the tiled router (32 tokens x 64 experts per CTA)
+    Workload("g-tiled", T=700, H=256, E=64, k=8, I=128, rmsnorm=True, gamma_std=0.1),
+    Workload("g-tiled-plain", T=1025, H=128, E=8, k=2, I=128),
+    Workload("g-tiled-E100", T=600, H=320, E=100, k=4, I=128, rmsnorm=True, skew_s=1.2,
+             skew_beta=0.7),
 ], ids=lambda w: w.name)
 def test_rmsnorm_gate_bitexact(wl):
     d = make_inputs(wl, 1)
