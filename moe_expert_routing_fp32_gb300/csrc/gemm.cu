@@ -33,6 +33,8 @@
 // in-flight copies / MMAs finish before the TMEM is freed.
 #include <cuda.h>
 
+#include <stdlib.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -405,6 +407,344 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
     }
 }
 
+// ------------------------------------------------------------------ CTA-pair kernel
+// Same tile list and epilogues, but each tile is 256 rows computed by a
+// cluster of two CTAs on a TPC with tcgen05.mma.cta_group::2 (M=256, N=256):
+// every CTA stages only its own 128 A rows and half of the B slice (32 KB a
+// stage instead of 48 KB), so a 6-deep ring fits and the L2 -> shared memory
+// traffic per flop drops by a third.
+//   - both CTAs' TMA loads complete on the even CTA's full barrier;
+//   - one thread of the even CTA issues the MMAs; its commits are multicast
+//     to both CTAs (stage release, accumulator ready);
+//   - each CTA's epilogue reads its own TMEM rows and arrives on the even
+//     CTA's accumulator-empty barrier.
+constexpr int BM2 = 256;
+constexpr int STAGES2 = 6;
+constexpr int STAGE2_BYTES = 2 * A_BYTES;   // 128x64 A + 128x64 B per CTA
+constexpr int TMEM2_COLS = 512;
+struct Cfg2 {
+    static constexpr int BAR_OFF = STAGES2 * STAGE2_BYTES;
+    static constexpr int NBARS = 2 * STAGES2 + 5;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int OFFS_OFF = MISC_OFF + 16;
+    static constexpr int PREFIX_OFF = OFFS_OFF + (MAX_GROUPS + 1) * 4;
+    static constexpr int SMEM = 1024 + PREFIX_OFF + (MAX_GROUPS + 2) * 4;
+};
+
+__device__ __forceinline__ Tile decode_tile_pair(const Params &p, int tile, const int *s_off,
+                                                 const int *s_prefix, int total0) {
+    Tile t;
+    if (tile < total0) {
+        int lo = 0, hi = p.G - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_prefix[mid] <= tile)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int g = lo;
+        const int cnt = s_off[g + 1] - s_off[g];
+        const int mt = (cnt + BM2 - 1) / BM2;
+        const int local = tile - s_prefix[g];
+        const bool nfast = cnt > p.brows0;
+        const int m_blk = nfast ? local / p.nt0 : local % mt;
+        t.seg = 0;
+        t.g = g;
+        t.row0 = s_off[g] + m_blk * BM2;
+        t.row_end = s_off[g + 1];
+        t.n_blk = nfast ? local % p.nt0 : local / mt;
+        t.kblocks = p.K0 / BK;
+    } else {
+        const int local = tile - total0;
+        const int mt = (p.rows1 + BM2 - 1) / BM2;
+        const bool nfast = p.rows1 > p.brows1;
+        t.seg = 1;
+        t.g = 0;
+        t.row0 = (nfast ? local / p.nt1 : local % mt) * BM2;
+        t.row_end = p.rows1;
+        t.n_blk = nfast ? local % p.nt1 : local / mt;
+        t.kblocks = p.K1 / BK;
+    }
+    return t;
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ Params p) {
+    constexpr int BN = 256;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg2::BAR_OFF);
+    uint64_t *full = bars;                      // used in the even CTA only
+    uint64_t *empty = bars + STAGES2;
+    uint64_t *tfull = bars + 2 * STAGES2;
+    uint64_t *tempty = tfull + 2;               // used in the even CTA only
+    uint64_t *drain = tempty + 2;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + Cfg2::MISC_OFF);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + Cfg2::MISC_OFF + 4);
+    volatile int *s_bad = reinterpret_cast<volatile int *>(smem + Cfg2::MISC_OFF + 8);
+    int *s_off = reinterpret_cast<int *>(smem + Cfg2::OFFS_OFF);
+    int *s_prefix = reinterpret_cast<int *>(smem + Cfg2::PREFIX_OFF);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();     // 0 = even CTA (issues the MMAs)
+    const bool leader = rank == 0;
+    const int cid = static_cast<int>(cluster_id_x());
+    const int ncl = static_cast<int>(num_clusters_x());
+
+    if (tid == 0) {
+        *s_abort = 0;
+        *s_bad = 0;
+    }
+    for (int g = tid; g <= p.G; g += THREADS) s_off[g] = p.offsets[g];
+    __syncthreads();
+    if (warp == 0) {
+        int run = 0;
+        bool bad = false;
+        for (int g0 = 0; g0 < p.G; g0 += 32) {
+            const int g = g0 + lane;
+            int tiles = 0;
+            if (g < p.G) {
+                const int a = s_off[g], b = s_off[g + 1];
+                if (a < 0 || b < a || b > p.rows0) bad = true;
+                tiles = b > a ? ((b - a + BM2 - 1) / BM2) * p.nt0 : 0;
+            }
+            int inc = tiles;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, inc, off);
+                if (lane >= off) inc += o;
+            }
+            if (g < p.G) s_prefix[g] = run + inc - tiles;
+            run += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) s_prefix[p.G] = run;
+        if (__any_sync(0xffffffffu, bad) && lane == 0) *s_bad = 1;
+    }
+    if (tid == 32) {
+        for (int s = 0; s < STAGES2; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 8);    // lane 0 of the 4 epilogue warps of both CTAs
+        }
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // both CTAs read the same offsets, so both leave here together
+    if (*s_bad) {
+        if (tid == 0 && cid == 0 && leader) report(p.dev_status, MOE_DEV_BAD_OFFSETS);
+        return;
+    }
+    const int total0 = s_prefix[p.G];
+    const int total = total0 + (p.rows1 > 0 ? ((p.rows1 + BM2 - 1) / BM2) * p.nt1 : 0);
+
+    if (warp == 1) {
+        tmem_alloc_pair(s_tmem, TMEM2_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();          // barriers and TMEM of both CTAs are ready
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+    const uint32_t lead_full = mapa_shared(smem_u32(full), 0);
+    const uint32_t lead_tempty = mapa_shared(smem_u32(tempty), 0);
+
+    if (warp == 0) {
+        // ================= TMA producer (both CTAs)
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmA0);
+            tma_prefetch_desc(&p.tmB0);
+            if (p.rows1 > 0) {
+                tma_prefetch_desc(&p.tmA1);
+                tma_prefetch_desc(&p.tmB1);
+            }
+            int stage = 0;
+            uint32_t phase = 0;
+            int armed[STAGES2];
+            for (int s = 0; s < STAGES2; ++s) armed[s] = -1;
+            for (int tile = cid; tile < total && !*s_abort; tile += ncl) {
+                const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0);
+                const int arow = t.row0 + 128 * static_cast<int>(rank);
+                bool ok = true;
+                for (int kb = 0; kb < t.kblocks; ++kb) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1, s_abort, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    armed[stage] = static_cast<int>(phase);
+                    uint8_t *a_dst = smem + stage * STAGE2_BYTES;
+                    uint8_t *b_dst = a_dst + A_BYTES;
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE2_BYTES);
+                    const uint32_t fb = lead_full + 8u * static_cast<uint32_t>(stage);
+                    const int k0 = kb * BK;
+                    int brow;
+                    if (MODE == MODE_SWIGLU)
+                        brow = (rank == 0 ? 0 : (t.seg == 0 ? p.half0 : p.half1)) + t.n_blk * 128;
+                    else
+                        brow = t.n_blk * BN + 128 * static_cast<int>(rank);
+                    if (t.seg == 0) {
+                        tma_load_2d_pair(a_dst, &p.tmA0, fb, k0, arow);
+                        tma_load_3d_pair(b_dst, &p.tmB0, fb, k0, brow, t.g);
+                    } else {
+                        tma_load_2d_pair(a_dst, &p.tmA1, fb, k0, arow);
+                        tma_load_2d_pair(b_dst, &p.tmB1, fb, k0, brow);
+                    }
+                    if (++stage == STAGES2) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+            }
+            if (*s_abort && leader) {
+                for (int s = 0; s < STAGES2; ++s)
+                    if (armed[s] >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>(armed[s]));
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================= MMA issuer (even CTA only)
+        if (lane == 0 && leader) {
+            constexpr uint32_t IDESC = idesc_bf16_f32(BM2, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool issued = false;
+            for (int tile = cid; tile < total && !*s_abort; tile += ncl) {
+                const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0);
+                if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, s_abort, p.dev_status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                bool ok = true;
+                for (int kb = 0; kb < t.kblocks; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase, s_abort, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * STAGE2_BYTES);
+                    const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        tc_mma_bf16_pair(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32),
+                                         sdesc_kmajor_sw128(b_addr + kk * 32), IDESC,
+                                         (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    tc_commit_pair_mc(&empty[stage], 0x3);
+                    if (++stage == STAGES2) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair_mc(&tfull[acc], 0x3);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            if (*s_abort && issued) {
+                tc_commit_pair_mc(drain, 0x1);
+                mbar_wait_drain(drain, 0);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================= epilogue (warps 2..5 of both CTAs)
+        const int q = warp & 3;
+        const int row_in_tile = 128 * static_cast<int>(rank) + q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = cid; tile < total; tile += ncl) {
+            const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0);
+            if (!mbar_wait_bounded(&tfull[acc], acc_phase, s_abort, p.dev_status)) break;
+            tc_fence_after();
+            const int row = t.row0 + row_in_tile;
+            const bool ok = row < t.row_end;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            if (MODE == MODE_SWIGLU) {
+                uint16_t *out = static_cast<uint16_t *>(t.seg == 0 ? p.out0 : p.out1);
+                const int64_t ldo = t.seg == 0 ? p.ldo0 : p.ldo1;
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 32) {
+                    float g[32], u[32];
+                    __syncwarp();
+                    tmem_ld32(taddr + c, g);
+                    tmem_ld32(taddr + 128 + c, u);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float a0 = __fdiv_rn(g[2 * i], 1.0f + expf(-g[2 * i])) * u[2 * i];
+                        const float a1 =
+                            __fdiv_rn(g[2 * i + 1], 1.0f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+                        pk[i] = pack_bf16x2(a0, a1);
+                    }
+                    if (ok) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            out + static_cast<int64_t>(row) * ldo + t.n_blk * 128 + c);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                                                pk[4 * v + 3]);
+                    }
+                }
+            } else {
+                const bool f32 = t.seg == 1 && p.out1_f32;
+                void *outp = t.seg == 0 ? p.out0 : p.out1;
+                const int64_t ldo = t.seg == 0 ? p.ldo0 : p.ldo1;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    float v[32];
+                    __syncwarp();
+                    tmem_ld32(taddr + c, v);
+                    tmem_ld_wait();
+                    if (!ok) continue;
+                    const int64_t off = static_cast<int64_t>(row) * ldo + t.n_blk * BN + c;
+                    if (f32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(outp) + off);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    } else {
+                        uint4 *dst =
+                            reinterpret_cast<uint4 *>(static_cast<uint16_t *>(outp) + off);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]),
+                                                pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                                pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                                                pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+                    }
+                }
+            }
+            __syncwarp();
+            tc_fence_before();
+            if (lane == 0) mbar_arrive_cluster(lead_tempty + 8u * static_cast<uint32_t>(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();          // no CTA leaves while its peer may still signal or read it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM2_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -444,6 +784,17 @@ bool make_map(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims, i
     return r == CUDA_SUCCESS;
 }
 
+// The CTA-pair kernels are used unless MOE_GEMM_SINGLE_CTA=1 is set in the
+// environment (read once), which selects the one-CTA kernels: same results,
+// kept for comparison and as a fallback.
+bool use_pair_kernel() {
+    static const bool pair = [] {
+        const char *v = getenv("MOE_GEMM_SINGLE_CTA");
+        return !(v && v[0] == '1');
+    }();
+    return pair;
+}
+
 template <int MODE, int BN>
 cudaError_t launch(Params &p, int max_rows0, cudaStream_t stream) {
     using C = Cfg<BN>;
@@ -469,6 +820,30 @@ cudaError_t launch(Params &p, int max_rows0, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <int MODE>
+cudaError_t launch_pair(Params &p, int max_rows0, cudaStream_t stream) {
+    static std::mutex mu;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !attr_done[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 Cfg2::SMEM);
+            if (e != cudaSuccess) return e;
+            attr_done[dev] = true;
+        }
+    }
+    const int64_t mblocks0 = ceil_div(max_rows0, BM2) + p.G;
+    const int64_t tiles = mblocks0 * p.nt0 + (p.rows1 > 0 ? ceil_div(p.rows1, BM2) * p.nt1 : 0);
+    const int clusters =
+        static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms() / 2, tiles)));
+    grouped_gemm_pair_kernel<MODE><<<2 * clusters, THREADS, Cfg2::SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool tensor_maps_available() { return encode_fn() != nullptr; }
@@ -484,6 +859,7 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
                             static_cast<uint64_t>(G)};
     if (!make_map(&p.tmA0, A, 2, a0, BM) || !make_map(&p.tmB0, W13, 3, b0, 128))
         return cudaErrorInvalidValue;
+    const bool pair = use_pair_kernel();
     p.tmA1 = p.tmA0;
     p.tmB1 = p.tmB0;
     if (seg1.rows > 0) {
@@ -510,6 +886,7 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
     p.ldo1 = seg1.N1;
     p.out1_f32 = 0;
     p.dev_status = dev_status;
+    if (pair) return launch_pair<MODE_SWIGLU>(p, n, stream);
     return launch<MODE_SWIGLU, 256>(p, n, stream);
 }
 
@@ -518,18 +895,20 @@ cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, 
                               int32_t *dev_status, cudaStream_t stream) {
     if (G > MAX_GROUPS) return cudaErrorInvalidValue;
     const int BN = (N % 256 == 0 && (seg1.rows == 0 || seg1.N1 % 256 == 0)) ? 256 : 128;
+    const bool pair = BN == 256 && use_pair_kernel();
+    const int box_b = pair ? 128 : BN;   // a pair CTA stages half of the 256 B rows
     Params p{};
     const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
     const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
                             static_cast<uint64_t>(G)};
-    if (!make_map(&p.tmA0, A, 2, a0, BM) || !make_map(&p.tmB0, W, 3, b0, BN))
+    if (!make_map(&p.tmA0, A, 2, a0, BM) || !make_map(&p.tmB0, W, 3, b0, box_b))
         return cudaErrorInvalidValue;
     p.tmA1 = p.tmA0;
     p.tmB1 = p.tmB0;
     if (seg1.rows > 0) {
         const uint64_t a1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.rows)};
         const uint64_t b1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.N1)};
-        if (!make_map(&p.tmA1, seg1.A, 2, a1, BM) || !make_map(&p.tmB1, seg1.B, 2, b1, BN))
+        if (!make_map(&p.tmA1, seg1.A, 2, a1, BM) || !make_map(&p.tmB1, seg1.B, 2, b1, box_b))
             return cudaErrorInvalidValue;
     }
     p.offsets = offsets;
@@ -550,6 +929,7 @@ cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, 
     p.ldo1 = seg1.N1;
     p.out1_f32 = seg1.out_f32 ? 1 : 0;
     p.dev_status = dev_status;
+    if (pair) return launch_pair<MODE_STORE>(p, n, stream);
     if (BN == 256) return launch<MODE_STORE, 256>(p, n, stream);
     return launch<MODE_STORE, 128>(p, n, stream);
 }
