@@ -79,9 +79,9 @@ def test_layer_desc_checks(L):
     assert L.moe_layer_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 2
     d = moe.make_desc(T=16, H=128, E=8, k=2, I=128, I_shared=128, rmsnorm=True)
     assert L.moe_layer_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
-    # xn + idx + w + hist + counts + offsets + row_idx + ex + act + y + act_s + y_s
-    assert n.value >= 16 * 128 * 2 + 3 * 32 * 4 + 32 * 128 * 2 * 2 + 32 * 128 * 2 + \
-        16 * 128 * 6
+    # xn + idx + w + row_idx + act + y + act_s + y_s (+ hist, counts, offsets, and
+    # either the token map of the gathering GEMM or expanded_x)
+    assert n.value >= 16 * 128 * 2 + 3 * 32 * 4 + 32 * 128 * 2 * 2 + 16 * 128 * 6
     P = ctypes.c_void_p
     fake = P(0x1000)
     assert L.moe_layer_forward(ctypes.byref(d), fake, None, fake, None, fake, fake, fake, fake,
