@@ -364,7 +364,7 @@ def workload_of(args):
     if args.I is not None:
         wl = wl.replace(I=args.I)
     if args.Is is not None and wl.I_s > 0:
-        wl = wl.replace(I_s=args.Is)
+        wl = wl.replace(I_s=args.Is)    # 0 drops the shared expert
     return wl
 
 
