@@ -33,6 +33,7 @@
 // in-flight copies / MMAs finish before the TMEM is freed.
 #include <cuda.h>
 
+#include <stdio.h>
 #include <stdlib.h>
 
 #include <algorithm>
@@ -838,8 +839,30 @@ cudaError_t launch_pair(Params &p, int max_rows0, cudaStream_t stream) {
     }
     const int64_t mblocks0 = ceil_div(max_rows0, BM2) + p.G;
     const int64_t tiles = mblocks0 * p.nt0 + (p.rows1 > 0 ? ceil_div(p.rows1, BM2) * p.nt1 : 0);
-    const int clusters =
-        static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms() / 2, tiles)));
+    // The static round-robin tile walk relies on every cluster running from
+    // the start: launch no more clusters than can be resident at once (CTA
+    // pairs need two SMs of one TPC, so this can be below num_sms / 2).
+    static int max_clusters[64] = {};
+    if (dev < 64 && max_clusters[dev] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(num_sms()), 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Cfg2::SMEM;
+        cfg.stream = stream;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<MODE>, &cfg) != cudaSuccess ||
+            n <= 0) {
+            cudaGetLastError();
+            n = num_sms() / 2;
+        }
+        max_clusters[dev] = std::min(n, num_sms() / 2);
+        const char *dbg = getenv("MOE_DEBUG");
+        if (dbg && dbg[0] == '1')
+            fprintf(stderr, "libmoe: device %d: %d CTA-pair clusters resident at once (%d SMs)\n",
+                    dev, max_clusters[dev], num_sms());
+    }
+    const int limit = dev < 64 ? max_clusters[dev] : num_sms() / 2;
+    const int clusters = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(limit, tiles)));
     grouped_gemm_pair_kernel<MODE><<<2 * clusters, THREADS, Cfg2::SMEM, stream>>>(p);
     return cudaGetLastError();
 }
