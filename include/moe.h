@@ -25,8 +25,9 @@
  *     int32 the caller zeroes beforehand; NULL = not reported).  A kernel
  *     that detects one writes nothing out of bounds and returns early; the
  *     outputs of that call are then undefined.
- *   - Sizes: 1 <= k <= min(E, 32), E <= 1024, T*k < 2^31, H % 64 == 0,
- *     I % 128 == 0 (I_shared likewise).  Inputs must be finite.
+ *   - Sizes: 1 <= k <= min(E, 32), E <= 1024, T*k < 2^31, H % 64 == 0
+ *     (H % 128 == 0 for the grouped MLP and the layer), I % 128 == 0
+ *     (I_shared likewise).  Inputs must be finite.
  */
 #ifndef MOE_H
 #define MOE_H
@@ -251,6 +252,41 @@ moe_status_t moe_layer_forward_timed(const moe_desc_t *desc, const moe_bf16_t *x
                                      const moe_bf16_t *w2_s, void *out, void *workspace,
                                      size_t workspace_bytes, int32_t *dev_status,
                                      moe_stream_t stream, void *const *stage_events);
+
+/*
+ * EP DoubleRouting, the steps local to one rank ("MoE EP优化": LocalRerouting
+ * "在每个RANK内按照专家序对token进行重排", LocalFinalizeRerouting
+ * "排序回第二次all_to_all后的排布").  After the token all_to_all a rank holds
+ * the received rows grouped by source rank and, within a source rank,
+ * ordered by local expert:
+ *   recv_counts [ep_size, E_local] int32 device: rows from rank r for local
+ *               expert e (ep_size * E_local <= 8192)
+ *   recv_x      [R, H] bf16, R = capacity >= sum(recv_counts)
+ * moe_local_rerouting reorders them by local expert, then source rank, then
+ * arrival order:
+ *   local_x[d] = recv_x[local_src[d]] (local_x may be NULL: indices only)
+ *   local_src  [R] int32 out (-1 past the received rows)
+ *   local_counts [E_local], local_offsets [E_local+1] out (grouped-GEMM input)
+ * Negative counts or a total above R set MOE_DEV_BAD_OFFSETS.
+ * moe_local_finalize_rerouting moves expert outputs back to the received
+ * order: recv_y[local_src[d]] = local_y[d] for every d with local_src[d] >= 0.
+ */
+moe_status_t moe_local_rerouting(const moe_bf16_t *recv_x, const int32_t *recv_counts,
+                                 int32_t ep_size, int32_t E_local, int32_t R, int32_t H,
+                                 moe_bf16_t *local_x, int32_t *local_src,
+                                 int32_t *local_counts, int32_t *local_offsets,
+                                 int32_t *dev_status, moe_stream_t stream);
+moe_status_t moe_local_finalize_rerouting(const moe_bf16_t *local_y, const int32_t *local_src,
+                                          int32_t R, int32_t H, moe_bf16_t *recv_y,
+                                          moe_stream_t stream);
+
+/*
+ * Diagnostics (the page has no counterpart): enqueue a kernel that waits,
+ * through the same bounded wait every pipeline here uses, on a barrier that
+ * nothing completes.  After about one second it ORs MOE_DEV_TIMEOUT into
+ * *dev_status (required, device int32) and returns; the context stays usable.
+ */
+moe_status_t moe_selftest_wait_timeout(int32_t *dev_status, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

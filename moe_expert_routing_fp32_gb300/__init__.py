@@ -35,7 +35,8 @@ EXPORTS = ("moe_status_string", "moe_rmsnorm_gate", "moe_gate_topk",
            "moe_init_routing_workspace_size", "moe_init_routing", "moe_init_routing_noalloc",
            "moe_expert_tokens",
            "moe_grouped_mlp", "moe_finalize_routing", "moe_layer_workspace_size",
-           "moe_layer_forward", "moe_layer_forward_timed")
+           "moe_layer_forward", "moe_layer_forward_timed", "moe_local_rerouting",
+           "moe_local_finalize_rerouting", "moe_selftest_wait_timeout")
 NUM_STAGES = 6
 STAGE_NAMES = ("router", "route_scan_scatter", "permute", "gemm_w13_swiglu", "gemm_down",
                "finalize")
@@ -94,6 +95,12 @@ def lib() -> ctypes.CDLL:
                 fn = getattr(L, name)
                 fn.argtypes = args
                 fn.restype = ctypes.c_int
+            L.moe_local_rerouting.argtypes = [P, P, I32, I32, I32, I32, P, P, P, P, P, P]
+            L.moe_local_rerouting.restype = ctypes.c_int
+            L.moe_local_finalize_rerouting.argtypes = [P, P, I32, I32, P, P]
+            L.moe_local_finalize_rerouting.restype = ctypes.c_int
+            L.moe_selftest_wait_timeout.argtypes = [P, P]
+            L.moe_selftest_wait_timeout.restype = ctypes.c_int
             L.moe_status_string.argtypes = [ctypes.c_int]
             L.moe_status_string.restype = ctypes.c_char_p
             _lib = L
@@ -123,6 +130,38 @@ def _call(name: str, *args):
 def _check(t, dtype, name):
     if t is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def local_rerouting(recv_x, recv_counts, with_rows=True, status=None):
+    """EP local step: -> dict(local_x, local_src, local_counts, local_offsets)."""
+    _check(recv_x, torch.bfloat16, "recv_x")
+    _check(recv_counts, torch.int32, "recv_counts")
+    R, H = recv_x.shape
+    ep, El = recv_counts.shape
+    dev = recv_x.device
+    lx = torch.empty_like(recv_x) if with_rows else None
+    src = torch.empty(R, dtype=torch.int32, device=dev)
+    lc = torch.empty(El, dtype=torch.int32, device=dev)
+    lo = torch.empty(El + 1, dtype=torch.int32, device=dev)
+    _call("moe_local_rerouting", _ptr(recv_x), _ptr(recv_counts), ep, El, R, H, _ptr(lx),
+          _ptr(src), _ptr(lc), _ptr(lo), _ptr(status), _stream(dev))
+    return dict(local_x=lx, local_src=src, local_counts=lc, local_offsets=lo)
+
+
+def local_finalize_rerouting(local_y, local_src, recv_y=None):
+    """EP local step: recv_y[local_src[d]] = local_y[d]."""
+    _check(local_y, torch.bfloat16, "local_y")
+    R, H = local_y.shape
+    if recv_y is None:
+        recv_y = torch.zeros_like(local_y)
+    _call("moe_local_finalize_rerouting", _ptr(local_y), _ptr(local_src), R, H, _ptr(recv_y),
+          _stream(local_y.device))
+    return recv_y
+
+
+def selftest_wait_timeout(status):
+    """Enqueue the bounded-wait check (see include/moe.h); sets DEV_TIMEOUT."""
+    _call("moe_selftest_wait_timeout", _ptr(status), _stream(status.device))
 
 
 def new_status(device) -> torch.Tensor:

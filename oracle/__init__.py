@@ -61,6 +61,8 @@ def _bind(lib):
         "oracle_finalize": [P, P, P, P, I64, I64, I64, P],
         "oracle_layer_tokens": [P, I64, I64, I64, I64, I64, I64, INT, F, INT,
                                 P, P, P, P, P, P, P, P, I64, P, P, P],
+        "oracle_local_rerouting": [P, P, I64, I64, I64, I64, P, P, P, P],
+        "oracle_local_finalize_rerouting": [P, P, I64, I64, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -290,3 +292,32 @@ def layer_tokens(inputs: dict, wl, tokens=None):
         _p(w2_s), _p(tok), 0 if tok is None else tok.size, _p(out), _p(idx), _p(w))
     _check(rc, "oracle_layer_tokens")
     return out, idx, w
+
+
+# ------------------------------------------------------------ EP local steps
+def local_rerouting(recv_x, counts):
+    """counts [ep, E_local] (rows per source rank and local expert), recv_x
+    [R, H] in arrival order.  Returns (local_x, local_src, local_counts,
+    local_offsets)."""
+    x = _u16(recv_x)
+    R, H = x.shape
+    c = _arr(counts, np.int32)
+    ep, El = c.shape
+    lx = np.zeros_like(x)
+    src = np.full(R, -1, dtype=np.int32)
+    lc = np.empty(El, dtype=np.int32)
+    lo = np.empty(El + 1, dtype=np.int32)
+    _check(_load().oracle_local_rerouting(_p(x), _p(c), ep, El, R, H, _p(lx), _p(src), _p(lc),
+                                          _p(lo)), "oracle_local_rerouting")
+    return lx, src, lc, lo
+
+
+def local_finalize_rerouting(local_y, local_src, n, R):
+    """recv_y[local_src[d]] = local_y[d] for d < n; returns recv_y [R, H]."""
+    y = _u16(local_y)
+    H = y.shape[1]
+    src = _arr(local_src, np.int32)
+    out = np.zeros((R, H), dtype=np.uint16)
+    _check(_load().oracle_local_finalize_rerouting(_p(y), _p(src), n, H, _p(out)),
+           "oracle_local_finalize_rerouting")
+    return out

@@ -456,3 +456,70 @@ void oracle_bf16_to_float(const bf16_t *in, int64_t n, float *out)
     for (int64_t i = 0; i < n; ++i)
         out[i] = bf16_to_float(in[i]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* EP DoubleRouting, local steps ("MoE EP优化"): after the token all_to_all a */
+/* rank holds R received rows, grouped by source rank r = 0..ep-1, and within */
+/* a source rank ordered by local expert (each rank sent its rows sorted by */
+/* expert).  counts[r*E_local + e] = rows from rank r for local expert e.     */
+/*                                                                          */
+/* LocalRerouting ("在每个RANK内按照专家序对token进行重排"): reorder the rows */
+/* by local expert, source rank second, arrival order third:                 */
+/*   local_x[d] = recv_x[local_src[d]],                                      */
+/*   local_counts[e] = sum_r counts[r][e], local_offsets = exclusive scan.   */
+/* Rows past sum(counts) are left alone.                                     */
+int oracle_local_rerouting(const bf16_t *recv_x, const int32_t *counts, int64_t ep,
+                           int64_t E_local, int64_t R, int64_t H, bf16_t *local_x,
+                           int32_t *local_src, int32_t *local_counts, int32_t *local_offsets)
+{
+    if (!counts || !local_src || !local_counts || !local_offsets || ep <= 0 || E_local <= 0 ||
+        R < 0 || H < 0)
+        return ORACLE_BAD_ARG;
+    int64_t total = 0;
+    for (int64_t i = 0; i < ep * E_local; ++i) {
+        if (counts[i] < 0)
+            return ORACLE_BAD_ARG;
+        total += counts[i];
+    }
+    if (total > R)
+        return ORACLE_BAD_ARG;
+    for (int64_t e = 0; e < E_local; ++e) {
+        local_counts[e] = 0;
+        for (int64_t r = 0; r < ep; ++r)
+            local_counts[e] += counts[r * E_local + e];
+    }
+    local_offsets[0] = 0;
+    for (int64_t e = 0; e < E_local; ++e)
+        local_offsets[e + 1] = local_offsets[e] + local_counts[e];
+    /* walk the received rows in arrival order, placing each block */
+    int64_t src = 0;
+    for (int64_t r = 0; r < ep; ++r) {
+        for (int64_t e = 0; e < E_local; ++e) {
+            int64_t dst = local_offsets[e];
+            for (int64_t rr = 0; rr < r; ++rr)
+                dst += counts[rr * E_local + e];
+            if (dst + counts[r * E_local + e] > local_offsets[e + 1])
+                return ORACLE_BAD_ARG;       /* would leave expert e's rows */
+            for (int64_t i = 0; i < counts[r * E_local + e]; ++i) {
+                local_src[dst + i] = (int32_t)(src + i);
+                if (local_x && recv_x)
+                    memcpy(local_x + (dst + i) * H, recv_x + (src + i) * H,
+                           (size_t)H * sizeof(bf16_t));
+            }
+            src += counts[r * E_local + e];
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* LocalFinalizeRerouting ("排序回第二次all_to_all后的排布"): put the expert   */
+/* outputs back in the received order: recv_y[local_src[d]] = local_y[d].    */
+int oracle_local_finalize_rerouting(const bf16_t *local_y, const int32_t *local_src, int64_t n,
+                                    int64_t H, bf16_t *recv_y)
+{
+    if ((!local_y || !local_src || !recv_y) && n > 0)
+        return ORACLE_BAD_ARG;
+    for (int64_t d = 0; d < n; ++d)
+        memcpy(recv_y + (int64_t)local_src[d] * H, local_y + d * H, (size_t)H * sizeof(bf16_t));
+    return ORACLE_OK;
+}

@@ -272,9 +272,37 @@ def pin_layer_shared_rmsnorm():
     assert np.allclose(out - out0, ys, rtol=1e-12, atol=1e-15)
 
 
+def pin_ep_local_rerouting():
+    """EP local steps: the rerouted order equals numpy's stable sort of the
+    received rows by (local expert, source rank, arrival); finalize undoes it;
+    one source rank with everything for one expert is the identity."""
+    rng = np.random.default_rng(7)
+    ep, El, H = 4, 6, 8
+    counts = rng.integers(0, 5, (ep, El)).astype(np.int32)
+    counts[1, :] = 0                      # a rank that sent nothing
+    counts[2, 3] = 9
+    total = int(counts.sum())
+    R = total + 5
+    x = rng.integers(0, 60000, (R, H)).astype(np.uint16)
+    lx, src, lc, lo = oracle.local_rerouting(x, counts)
+    rank = np.repeat(np.repeat(np.arange(ep), El), counts.reshape(-1))
+    expert = np.repeat(np.tile(np.arange(El), ep), counts.reshape(-1))
+    order = np.lexsort((np.arange(total), rank, expert))   # expert, then rank, then arrival
+    assert np.array_equal(src[:total], order)
+    assert np.all(src[total:] == -1)
+    assert np.array_equal(lx[:total], x[order])
+    assert np.array_equal(lc, counts.sum(0)) and lo[0] == 0 and lo[-1] == total
+    assert np.array_equal(np.diff(lo), lc)
+    back = oracle.local_finalize_rerouting(lx[:total], src, total, R)
+    assert np.array_equal(back[:total], x[:total])
+    one = np.array([[7]], dtype=np.int32)
+    _, s1, _, _ = oracle.local_rerouting(x[:7], one)
+    assert np.array_equal(s1, np.arange(7))
+
+
 PINS = [pin_bf16_rounding, pin_rmsnorm, pin_gate, pin_topk, pin_routing,
         pin_expert_mlp, pin_finalize, pin_worked_example, pin_layer_brute_force,
-        pin_layer_shared_rmsnorm]
+        pin_layer_shared_rmsnorm, pin_ep_local_rerouting]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -306,6 +334,10 @@ MUTANTS = {
     "finalize_weight_index": ("(double)topk_w[t * k + j] *", "(double)topk_w[j] *"),
     "bf16_truncate": ("nearbyint(ldexp(m, 8))", "floor(ldexp(m, 8))"),
     "layer_shared_dropped": ("o[c] += ys[c];", "o[c] += 0.0;"),
+    "ep_rank_off_by_one": ("for (int64_t rr = 0; rr < r; ++rr)",
+                           "for (int64_t rr = 0; rr <= r; ++rr)"),
+    "ep_finalize_wrong_side": ("memcpy(recv_y + (int64_t)local_src[d] * H, local_y + d * H,",
+                               "memcpy(recv_y + d * H, local_y + (int64_t)local_src[d] * H,"),
 }
 
 
