@@ -55,6 +55,10 @@ def parse_args():
     ap.add_argument("--E", type=int, default=None, help="override the expert count")
     ap.add_argument("--I", type=int, default=None, help="override the expert inter size")
     ap.add_argument("--Is", type=int, default=None, help="override the shared inter size")
+    ap.add_argument("--shared-stream", action="store_true",
+                    help="run the shared expert on a second stream (moe_layer_forward_streams)")
+    ap.add_argument("--tp", type=int, default=1,
+                    help="time one MoE tensor-parallel shard: I and I_shared divided by tp")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU work of the oracle baseline sample")
     return ap.parse_args()
@@ -231,8 +235,15 @@ def run_ours(args, rank, world, local):
     for row in evs:
         for e in row:
             e.record()           # creates the event handles
+    extra = {}
+    if args.shared_stream and wl.I_s > 0:
+        s2 = torch.cuda.Stream(device=dev)
+        fj = [torch.cuda.Event(), torch.cuda.Event()]
+        for e in fj:
+            e.record()
+        extra = dict(shared_stream=s2, events=fj)
     for _ in range(W):
-        moe.layer_forward(desc, x, weights, out=out, workspace=ws, status=status)
+        moe.layer_forward(desc, x, weights, out=out, workspace=ws, status=status, **extra)
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during warm-up")
@@ -247,7 +258,7 @@ def run_ours(args, rank, world, local):
     start.record()
     for i in range(K):
         moe.layer_forward(desc, x, weights, out=out, workspace=ws, status=status,
-                          stage_events=evs[i])
+                          stage_events=evs[i], **extra)
     end.record()
     torch.cuda.synchronize()
     if dist:
@@ -329,6 +340,7 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) random-init weights)",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
                    "I_shared": wl.I_s, "rmsnorm": wl.rmsnorm, "out": "bf16",
+                   "shared_expert": "second stream" if args.shared_stream else "same launches",
                    "gate": "fp32", "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
@@ -365,6 +377,9 @@ def workload_of(args):
         wl = wl.replace(I=args.I)
     if args.Is is not None and wl.I_s > 0:
         wl = wl.replace(I_s=args.Is)    # 0 drops the shared expert
+    if args.tp > 1:
+        wl = wl.replace(name=f"{wl.name}-tp{args.tp}-shard", I=wl.I // args.tp,
+                        I_s=wl.I_s // args.tp)
     return wl
 
 

@@ -254,6 +254,27 @@ moe_status_t moe_layer_forward_timed(const moe_desc_t *desc, const moe_bf16_t *x
                                      moe_stream_t stream, void *const *stage_events);
 
 /*
+ * moe_layer_forward with the shared expert on a second stream
+ * ("MoE多流并行优化": the shared expert runs beside the routed experts on
+ * another stream).  Same results, bit for bit, as moe_layer_forward.  The
+ * routed path runs on `stream`; after the router, `fork_event` is recorded on
+ * `stream` and awaited by `shared_stream`, which runs the shared expert's two
+ * matmuls and records `join_event`; `stream` awaits it before finalize.
+ * The caller owns both streams and both events (cudaEvent_t, any flags) and
+ * must not use the events concurrently elsewhere.  Requires MOE_SHARED.
+ * stage_events: as in moe_layer_forward_timed (recorded on `stream`), or NULL.
+ */
+moe_status_t moe_layer_forward_streams(const moe_desc_t *desc, const moe_bf16_t *x,
+                                       const moe_bf16_t *gamma, const float *wg,
+                                       const float *gate_bias, const moe_bf16_t *w13,
+                                       const moe_bf16_t *w2, const moe_bf16_t *w13_s,
+                                       const moe_bf16_t *w2_s, void *out, void *workspace,
+                                       size_t workspace_bytes, int32_t *dev_status,
+                                       moe_stream_t stream, moe_stream_t shared_stream,
+                                       void *fork_event, void *join_event,
+                                       void *const *stage_events);
+
+/*
  * EP DoubleRouting, the steps local to one rank ("MoE EP优化": LocalRerouting
  * "在每个RANK内按照专家序对token进行重排", LocalFinalizeRerouting
  * "排序回第二次all_to_all后的排布").  After the token all_to_all a rank holds

@@ -35,7 +35,8 @@ EXPORTS = ("moe_status_string", "moe_rmsnorm_gate", "moe_gate_topk",
            "moe_init_routing_workspace_size", "moe_init_routing", "moe_init_routing_noalloc",
            "moe_expert_tokens",
            "moe_grouped_mlp", "moe_finalize_routing", "moe_layer_workspace_size",
-           "moe_layer_forward", "moe_layer_forward_timed", "moe_local_rerouting",
+           "moe_layer_forward", "moe_layer_forward_timed", "moe_layer_forward_streams",
+           "moe_local_rerouting",
            "moe_local_finalize_rerouting", "moe_selftest_wait_timeout")
 NUM_STAGES = 6
 STAGE_NAMES = ("router", "route_scan_scatter", "permute", "gemm_w13_swiglu", "gemm_down",
@@ -90,6 +91,8 @@ def lib() -> ctypes.CDLL:
                                       SZ, P, P],
                 "moe_layer_forward_timed": [ctypes.POINTER(MoeDesc), P, P, P, P, P, P, P, P, P,
                                             P, SZ, P, P, P],
+                "moe_layer_forward_streams": [ctypes.POINTER(MoeDesc), P, P, P, P, P, P, P, P, P,
+                                              P, SZ, P, P, P, P, P, P],
             }
             for name, args in sigs.items():
                 fn = getattr(L, name)
@@ -293,11 +296,13 @@ class LayerWeights:
 
 
 def layer_forward(desc: MoeDesc, x, weights: LayerWeights, out=None, workspace=None,
-                  status=None, stage_events=None):
+                  status=None, stage_events=None, shared_stream=None, events=None):
     """The whole MoE layer.  ``workspace`` (uint8, >= layer_workspace_size)
     and ``out`` are allocated when not given.  ``stage_events``: a list of
     NUM_STAGES + 1 recorded-once torch.cuda.Event (timing enabled) to time
-    the internal stages.  Returns ``out``."""
+    the internal stages.  ``shared_stream`` (a torch.cuda.Stream) with
+    ``events`` (two recorded-once torch.cuda.Event) runs the shared expert on
+    that stream.  Returns ``out``."""
     _check(x, torch.bfloat16, "x")
     dev = x.device
     if out is None:
@@ -311,11 +316,17 @@ def layer_forward(desc: MoeDesc, x, weights: LayerWeights, out=None, workspace=N
     args = [ctypes.byref(desc), _ptr(x), _ptr(w.gamma), _ptr(w.wg), _ptr(w.gate_bias),
             _ptr(w.w13), _ptr(w.w2), _ptr(w.w13_s), _ptr(w.w2_s), _ptr(out), _ptr(workspace),
             workspace.numel(), _ptr(status), _stream(dev)]
-    if stage_events is None:
-        _call("moe_layer_forward", *args)
-    else:
+    arr = None
+    if stage_events is not None:
         assert len(stage_events) == NUM_STAGES + 1
         arr = (ctypes.c_void_p * (NUM_STAGES + 1))(*[e.cuda_event for e in stage_events])
+    if shared_stream is not None:
+        fork, join = events
+        _call("moe_layer_forward_streams", *args, ctypes.c_void_p(shared_stream.cuda_stream),
+              ctypes.c_void_p(fork.cuda_event), ctypes.c_void_p(join.cuda_event), arr)
+    elif arr is None:
+        _call("moe_layer_forward", *args)
+    else:
         _call("moe_layer_forward_timed", *args, arr)
     return out
 

@@ -877,19 +877,27 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
                                cudaStream_t stream) {
     if (G > MAX_GROUPS) return cudaErrorInvalidValue;
     Params p{};
-    const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
-    const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(2 * N),
-                            static_cast<uint64_t>(G)};
-    if (!make_map(&p.tmA0, A, 2, a0, BM) || !make_map(&p.tmB0, W13, 3, b0, 128))
-        return cudaErrorInvalidValue;
     const bool pair = use_pair_kernel();
-    p.tmA1 = p.tmA0;
-    p.tmB1 = p.tmB0;
+    if (G > 0) {
+        const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
+        const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(2 * N),
+                                static_cast<uint64_t>(G)};
+        if (!make_map(&p.tmA0, A, 2, a0, BM) || !make_map(&p.tmB0, W13, 3, b0, 128))
+            return cudaErrorInvalidValue;
+        p.tmA1 = p.tmA0;
+        p.tmB1 = p.tmB0;
+    }
     if (seg1.rows > 0) {
         const uint64_t a1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.rows)};
         const uint64_t b1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(2 * seg1.N1)};
         if (!make_map(&p.tmA1, seg1.A, 2, a1, BM) || !make_map(&p.tmB1, seg1.B, 2, b1, 128))
             return cudaErrorInvalidValue;
+        if (G == 0) {   // no routed groups: the unused maps just need to be valid
+            p.tmA0 = p.tmA1;
+            p.tmB0 = p.tmB1;
+        }
+    } else if (G == 0) {
+        return cudaSuccess;
     }
     p.offsets = offsets;
     p.G = G;
@@ -921,18 +929,26 @@ cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, 
     const bool pair = BN == 256 && use_pair_kernel();
     const int box_b = pair ? 128 : BN;   // a pair CTA stages half of the 256 B rows
     Params p{};
-    const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
-    const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
-                            static_cast<uint64_t>(G)};
-    if (!make_map(&p.tmA0, A, 2, a0, BM) || !make_map(&p.tmB0, W, 3, b0, box_b))
-        return cudaErrorInvalidValue;
-    p.tmA1 = p.tmA0;
-    p.tmB1 = p.tmB0;
+    if (G > 0) {
+        const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
+        const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                                static_cast<uint64_t>(G)};
+        if (!make_map(&p.tmA0, A, 2, a0, BM) || !make_map(&p.tmB0, W, 3, b0, box_b))
+            return cudaErrorInvalidValue;
+        p.tmA1 = p.tmA0;
+        p.tmB1 = p.tmB0;
+    }
     if (seg1.rows > 0) {
         const uint64_t a1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.rows)};
         const uint64_t b1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.N1)};
         if (!make_map(&p.tmA1, seg1.A, 2, a1, BM) || !make_map(&p.tmB1, seg1.B, 2, b1, box_b))
             return cudaErrorInvalidValue;
+        if (G == 0) {
+            p.tmA0 = p.tmA1;
+            p.tmB0 = p.tmB1;
+        }
+    } else if (G == 0) {
+        return cudaSuccess;
     }
     p.offsets = offsets;
     p.G = G;

@@ -60,6 +60,7 @@ struct GemmSegment1 {       // an optional dense problem appended to the grouped
     bool out_f32 = false;
 };
 
+// G may be 0 (segment 1 only; `offsets` must still point at one readable int).
 // act[r, :] = bf16(SiLU(A W13g^T) * (A W13u^T)) per group; A [n, K], W13 [G, 2N, K]
 cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G, int n, int K,
                                const uint16_t *W13, int N, uint16_t *act,

@@ -257,23 +257,20 @@ moe_status_t moe_layer_workspace_size(const moe_desc_t *desc, size_t *bytes) {
     return MOE_OK;
 }
 
-moe_status_t moe_layer_forward(const moe_desc_t *desc, const moe_bf16_t *x,
-                               const moe_bf16_t *gamma, const float *wg, const float *gate_bias,
-                               const moe_bf16_t *w13, const moe_bf16_t *w2,
-                               const moe_bf16_t *w13_s, const moe_bf16_t *w2_s, void *out,
-                               void *workspace, size_t workspace_bytes, int32_t *dev_status,
-                               moe_stream_t stream) {
-    return moe_layer_forward_timed(desc, x, gamma, wg, gate_bias, w13, w2, w13_s, w2_s, out,
-                                   workspace, workspace_bytes, dev_status, stream, nullptr);
-}
+}  // extern "C"
 
-moe_status_t moe_layer_forward_timed(const moe_desc_t *desc, const moe_bf16_t *x,
-                                     const moe_bf16_t *gamma, const float *wg,
-                                     const float *gate_bias, const moe_bf16_t *w13,
-                                     const moe_bf16_t *w2, const moe_bf16_t *w13_s,
-                                     const moe_bf16_t *w2_s, void *out, void *workspace,
-                                     size_t workspace_bytes, int32_t *dev_status,
-                                     moe_stream_t stream, void *const *stage_events) {
+namespace {
+
+// The layer; `stage_events` as in moe_layer_forward_timed; with
+// `shared_stream` the shared expert's matmuls run on that stream between
+// `fork_event` (after the router) and `join_event` (before finalize).
+moe_status_t layer_forward_impl(const moe_desc_t *desc, const moe_bf16_t *x,
+                                const moe_bf16_t *gamma, const float *wg, const float *gate_bias,
+                                const moe_bf16_t *w13, const moe_bf16_t *w2,
+                                const moe_bf16_t *w13_s, const moe_bf16_t *w2_s, void *out,
+                                void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                moe_stream_t stream, void *const *stage_events,
+                                moe_stream_t shared_stream, void *fork_event, void *join_event) {
     moe_status_t st = check_desc(desc);
     if (st != MOE_OK) return st;
     const moe_desc_t d = *desc;
@@ -333,9 +330,37 @@ moe_status_t moe_layer_forward_timed(const moe_desc_t *desc, const moe_bf16_t *x
     MOE_TRY(launch_route_scatter(idx, hist, T, k, E, row_idx, nullptr, nullptr, dev_status, s));
     MOE_TRY(mark(2));
     MOE_TRY(launch_permute(xs, row_idx, T, H, k, ex, s));
+    // (shared expert on its own stream: fork after the router)
+    const bool two_streams = shared && shared_stream != nullptr;
+    if (two_streams) {
+        cudaStream_t s2 = reinterpret_cast<cudaStream_t>(shared_stream);
+        cudaEvent_t fork = static_cast<cudaEvent_t>(fork_event);
+        cudaEvent_t join = static_cast<cudaEvent_t>(join_event);
+        GemmSegment1 a1, a2;
+        a1.A = xs;
+        a1.B = w13_s;
+        a1.rows = T;
+        a1.K1 = H;
+        a1.N1 = d.I_shared;
+        a1.out = act_s;
+        a2.A = act_s;
+        a2.B = w2_s;
+        a2.rows = T;
+        a2.K1 = d.I_shared;
+        a2.N1 = H;
+        a2.out = y_s;
+        a2.out_f32 = true;
+        MOE_TRY(cudaEventRecord(fork, s));
+        MOE_TRY(cudaStreamWaitEvent(s2, fork, 0));
+        MOE_TRY(launch_gemm_swiglu(nullptr, offsets, 0, 0, H, nullptr, I, nullptr, a1, dev_status,
+                                   s2));
+        MOE_TRY(launch_gemm_store(nullptr, offsets, 0, 0, d.I_shared, nullptr, H, nullptr, a2,
+                                  dev_status, s2));
+        MOE_TRY(cudaEventRecord(join, s2));
+    }
     // 3. grouped w13 + SwiGLU (the shared expert rides along as a dense segment)
     GemmSegment1 s1;
-    if (shared) {
+    if (shared && !two_streams) {
         s1.A = xs;
         s1.B = w13_s;
         s1.rows = T;
@@ -347,7 +372,7 @@ moe_status_t moe_layer_forward_timed(const moe_desc_t *desc, const moe_bf16_t *x
     MOE_TRY(launch_gemm_swiglu(ex, offsets, E, N, H, w13, I, act, s1, dev_status, s));
     // 4. grouped down projection (shared expert output kept in fp32)
     GemmSegment1 s2;
-    if (shared) {
+    if (shared && !two_streams) {
         s2.A = act_s;
         s2.B = w2_s;
         s2.rows = T;
@@ -359,11 +384,55 @@ moe_status_t moe_layer_forward_timed(const moe_desc_t *desc, const moe_bf16_t *x
     MOE_TRY(mark(4));
     MOE_TRY(launch_gemm_store(act, offsets, E, N, I, w2, H, y, s2, dev_status, s));
     // 5. finalize: weighted sum in slot order + shared row
+    if (two_streams) MOE_TRY(cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(join_event), 0));
     MOE_TRY(mark(5));
     MOE_TRY(launch_finalize(y, row_idx, w, y_s, true, T, H, k, out,
                             (d.flags & MOE_OUT_F32) != 0, s));
     MOE_TRY(mark(6));
     return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_layer_forward(const moe_desc_t *desc, const moe_bf16_t *x,
+                               const moe_bf16_t *gamma, const float *wg, const float *gate_bias,
+                               const moe_bf16_t *w13, const moe_bf16_t *w2,
+                               const moe_bf16_t *w13_s, const moe_bf16_t *w2_s, void *out,
+                               void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                               moe_stream_t stream) {
+    return layer_forward_impl(desc, x, gamma, wg, gate_bias, w13, w2, w13_s, w2_s, out,
+                              workspace, workspace_bytes, dev_status, stream, nullptr, nullptr,
+                              nullptr, nullptr);
+}
+
+moe_status_t moe_layer_forward_timed(const moe_desc_t *desc, const moe_bf16_t *x,
+                                     const moe_bf16_t *gamma, const float *wg,
+                                     const float *gate_bias, const moe_bf16_t *w13,
+                                     const moe_bf16_t *w2, const moe_bf16_t *w13_s,
+                                     const moe_bf16_t *w2_s, void *out, void *workspace,
+                                     size_t workspace_bytes, int32_t *dev_status,
+                                     moe_stream_t stream, void *const *stage_events) {
+    return layer_forward_impl(desc, x, gamma, wg, gate_bias, w13, w2, w13_s, w2_s, out,
+                              workspace, workspace_bytes, dev_status, stream, stage_events,
+                              nullptr, nullptr, nullptr);
+}
+
+moe_status_t moe_layer_forward_streams(const moe_desc_t *desc, const moe_bf16_t *x,
+                                       const moe_bf16_t *gamma, const float *wg,
+                                       const float *gate_bias, const moe_bf16_t *w13,
+                                       const moe_bf16_t *w2, const moe_bf16_t *w13_s,
+                                       const moe_bf16_t *w2_s, void *out, void *workspace,
+                                       size_t workspace_bytes, int32_t *dev_status,
+                                       moe_stream_t stream, moe_stream_t shared_stream,
+                                       void *fork_event, void *join_event,
+                                       void *const *stage_events) {
+    if (!shared_stream || !fork_event || !join_event || shared_stream == stream)
+        return MOE_ERR_INVALID_ARG;
+    return layer_forward_impl(desc, x, gamma, wg, gate_bias, w13, w2, w13_s, w2_s, out,
+                              workspace, workspace_bytes, dev_status, stream, stage_events,
+                              shared_stream, fork_event, join_event);
 }
 
 }  // extern "C"

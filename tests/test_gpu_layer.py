@@ -139,3 +139,25 @@ def test_layer_full_size(name):
         out = _run_layer(wl, g, out_f32)
         got = t2f64(out[torch.from_numpy(tok).long().to(DEV)])
         check_out(got, ref, bf16_out=not out_f32, what=f"{name} f32={out_f32}")
+
+
+def test_shared_expert_on_second_stream_matches():
+    """The shared expert on its own stream ("MoE多流并行优化") gives the same
+    bits as the one-stream layer (same kernels, only the order of launches
+    across streams differs)."""
+    wl = SMALL[1]
+    d = make_inputs(wl, 6)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    desc = _desc(wl)
+    a = moe.layer_forward(desc, g["x"], _weights(g))
+    s2 = torch.cuda.Stream()
+    evs = [torch.cuda.Event(), torch.cuda.Event()]
+    for e in evs:
+        e.record()
+    st = moe.new_status(DEV)
+    b = moe.layer_forward(desc, g["x"], _weights(g), status=st, shared_stream=s2, events=evs)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(a, b)
+    ref, _, _ = oracle.layer_tokens(d, wl)
+    check_out(t2f64(b), ref, bf16_out=False, what="two streams")
