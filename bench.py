@@ -55,8 +55,10 @@ def parse_args():
     ap.add_argument("--E", type=int, default=None, help="override the expert count")
     ap.add_argument("--I", type=int, default=None, help="override the expert inter size")
     ap.add_argument("--Is", type=int, default=None, help="override the shared inter size")
-    ap.add_argument("--shared-stream", action="store_true",
-                    help="run the shared expert on a second stream (moe_layer_forward_streams)")
+    ap.add_argument("--shared-stream", default="off", choices=["on", "off"],
+                    help="run the shared expert on a second stream (moe_layer_forward_streams); "
+                         "off keeps it inside the same launches, so the dominant kernel's "
+                         "roofline is measured on its own")
     ap.add_argument("--tp", type=int, default=1,
                     help="time one MoE tensor-parallel shard: I and I_shared divided by tp")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -197,9 +199,15 @@ def cpu_oracle_rate(inputs_cpu, wl, seconds, first_token=0):
 
 
 # --------------------------------------------------------------- our arm
-def stage_bytes_flops(wl):
+def stage_bytes_flops(wl, two_streams=False):
+    """Algorithmic work of each timed stage.  With the shared expert on its
+    own stream the main stream's GEMM stages run the routed experts only (the
+    shared matmuls overlap on the second stream), so only routed flops are
+    credited to them: a conservative count."""
     T, H, E, k, I, Is = wl.T, wl.H, wl.E, wl.k, wl.I, wl.I_s
     N = T * k
+    if two_streams:
+        Is = 0
     # algorithmic work of each stage (what the step must touch or compute once)
     return {
         "router": {"bytes": T * H * 2 + (T * H * 2 if wl.rmsnorm else 0) + E * H * 4 + N * 8,
@@ -207,7 +215,7 @@ def stage_bytes_flops(wl):
         "permute": {"bytes": T * H * 2 + N * H * 2 + N * 4},
         "gemm_w13_swiglu": {"flops": 4.0 * N * H * I + 4.0 * T * H * Is},
         "gemm_down": {"flops": 2.0 * N * H * I + 2.0 * T * H * Is},
-        "finalize": {"bytes": N * H * 2 + (T * H * 4 if Is else 0) + T * H * 2 + N * 8},
+        "finalize": {"bytes": N * H * 2 + (T * H * 4 if wl.I_s else 0) + T * H * 2 + N * 8},
     }
 
 
@@ -236,7 +244,8 @@ def run_ours(args, rank, world, local):
         for e in row:
             e.record()           # creates the event handles
     extra = {}
-    if args.shared_stream and wl.I_s > 0:
+    two_streams = wl.I_s > 0 and args.shared_stream == "on"
+    if two_streams:
         s2 = torch.cuda.Stream(device=dev)
         fj = [torch.cuda.Event(), torch.cuda.Event()]
         for e in fj:
@@ -278,13 +287,14 @@ def run_ours(args, rank, world, local):
 
     # end to end on host buffers (pinned), through the same public call
     if args.no_e2e:
-        return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, None, g)
+        return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, None, g,
+                           two_streams)
     x_host = x.cpu().pin_memory()
     out_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, pin_memory=True)
     x_dev = torch.empty_like(x)
     for _ in range(2):
         moe.layer_forward_host(desc, x_host, weights, out_host, x_dev=x_dev, out_dev=out,
-                               workspace=ws, status=status)
+                               workspace=ws, status=status, **extra)
     Ke = max(3, min(K, 20))
     if dist:
         torch.distributed.barrier()
@@ -293,7 +303,7 @@ def run_ours(args, rank, world, local):
     e0.record()
     for _ in range(Ke):
         moe.layer_forward_host(desc, x_host, weights, out_host, x_dev=x_dev, out_dev=out,
-                               workspace=ws, status=status)
+                               workspace=ws, status=status, **extra)
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -302,15 +312,17 @@ def run_ours(args, rank, world, local):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(t.item())
     e2e_value = world * wl.T * Ke / (e2e_ms / 1e3)
-    return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g)
+    return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g,
+                       two_streams)
 
 
-def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g):
+def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g,
+                two_streams=False):
     import moe_expert_routing_fp32_gb300 as moe  # noqa: F401
     step_ms = elapsed_ms / K
     value = world * wl.T * K / (elapsed_ms / 1e3)
     peaks, peak_src = load_peaks()
-    work = stage_bytes_flops(wl)
+    work = stage_bytes_flops(wl, two_streams)
     dom = "gemm_w13_swiglu"
     dom_s = stage_ms[dom] / 1e3
     tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
@@ -318,6 +330,10 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
     achieved = work[dom]["flops"] / dom_s / 1e12
     gemm_s = (stage_ms["gemm_w13_swiglu"] + stage_ms["gemm_down"]) / 1e3
     gemm_tflops = (work["gemm_w13_swiglu"]["flops"] + work["gemm_down"]["flops"]) / gemm_s / 1e12
+    # whole-layer GEMM rate: every GEMM flop of the step (routed + shared) over the step
+    all_gemm_flops = stage_bytes_flops(wl, False)
+    layer_gemm_tflops = (all_gemm_flops["gemm_w13_swiglu"]["flops"] +
+                         all_gemm_flops["gemm_down"]["flops"]) / (step_ms / 1e3) / 1e12
     per_stage = {}
     for name, ms in stage_ms.items():
         e = {"ms": round(ms, 4), "share": round(ms / step_ms, 4)}
@@ -340,7 +356,8 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) random-init weights)",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
                    "I_shared": wl.I_s, "rmsnorm": wl.rmsnorm, "out": "bf16",
-                   "shared_expert": "second stream" if args.shared_stream else "same launches",
+                   "shared_expert": ("none" if not wl.I_s else
+                                     "second stream" if two_streams else "same launches"),
                    "gate": "fp32", "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
@@ -349,6 +366,7 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
                      "traffic": recorded_traffic(wl.name)},
         "gemm_tflops": round(gemm_tflops, 1),
         "gemm_frac_bf16_peak": round(gemm_tflops / tc_peak, 4),
+        "layer_gemm_tflops_over_step": round(layer_gemm_tflops, 1),
         "stages": per_stage,
         "e2e": None if e2e_value is None else {
             "value": round(e2e_value, 1), "unit": UNIT,

@@ -332,7 +332,7 @@ def layer_forward(desc: MoeDesc, x, weights: LayerWeights, out=None, workspace=N
 
 
 def layer_forward_host(desc: MoeDesc, x_host, weights: LayerWeights, out_host=None,
-                       x_dev=None, out_dev=None, workspace=None, status=None):
+                       x_dev=None, out_dev=None, workspace=None, status=None, **kw):
     """The layer on host buffers: copies x (pinned host) to the device, runs
     the layer and copies the result back into ``out_host`` (pinned), all on
     the current stream; synchronises before returning ``out_host``."""
@@ -341,7 +341,7 @@ def layer_forward_host(desc: MoeDesc, x_host, weights: LayerWeights, out_host=No
         x_dev = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev)
     x_dev.copy_(x_host, non_blocking=True)
     out_dev = layer_forward(desc, x_dev, weights, out=out_dev, workspace=workspace,
-                            status=status)
+                            status=status, **kw)
     if out_host is None:
         out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype, pin_memory=True)
     out_host.copy_(out_dev, non_blocking=True)

@@ -785,15 +785,26 @@ bool make_map(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims, i
     return r == CUDA_SUCCESS;
 }
 
-// The CTA-pair kernels are used unless MOE_GEMM_SINGLE_CTA=1 is set in the
-// environment (read once), which selects the one-CTA kernels: same results,
-// kept for comparison and as a fallback.
-bool use_pair_kernel() {
-    static const bool pair = [] {
-        const char *v = getenv("MOE_GEMM_SINGLE_CTA");
-        return !(v && v[0] == '1');
+// Which grouped-GEMM kernel runs: MOE_GEMM_KERNEL=pair or =single in the
+// environment (read once) forces one; the default picks per launch.
+enum GemmChoice { GEMM_AUTO, GEMM_PAIR, GEMM_SINGLE };
+GemmChoice gemm_choice() {
+    static const GemmChoice c = [] {
+        const char *v = getenv("MOE_GEMM_KERNEL");
+        if (v && v[0] == 'p') return GEMM_PAIR;
+        if (v && v[0] == 's') return GEMM_SINGLE;
+        return GEMM_AUTO;
     }();
-    return pair;
+    return c;
+}
+
+// 256-row pair tiles pay off when groups are large; with a few rows per
+// expert (weight streaming) the 128-row one-CTA tiles are faster.
+bool use_pair(int n, int G, int seg1_rows) {
+    const GemmChoice c = gemm_choice();
+    if (c != GEMM_AUTO) return c == GEMM_PAIR;
+    const int64_t avg = G > 0 ? n / G : seg1_rows;
+    return avg >= 256;
 }
 
 template <int MODE, int BN>
@@ -877,7 +888,7 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
                                cudaStream_t stream) {
     if (G > MAX_GROUPS) return cudaErrorInvalidValue;
     Params p{};
-    const bool pair = use_pair_kernel();
+    const bool pair = use_pair(n, G, seg1.rows);
     if (G > 0) {
         const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
         const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(2 * N),
@@ -926,7 +937,7 @@ cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, 
                               int32_t *dev_status, cudaStream_t stream) {
     if (G > MAX_GROUPS) return cudaErrorInvalidValue;
     const int BN = (N % 256 == 0 && (seg1.rows == 0 || seg1.N1 % 256 == 0)) ? 256 : 128;
-    const bool pair = BN == 256 && use_pair_kernel();
+    const bool pair = BN == 256 && use_pair(n, G, seg1.rows);
     const int box_b = pair ? 128 : BN;   // a pair CTA stages half of the 256 B rows
     Params p{};
     if (G > 0) {

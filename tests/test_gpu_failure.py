@@ -40,14 +40,16 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert torch.allclose(w.cpu(), torch.tensor([[0.5, 0.5]]))
 
 
-def test_single_cta_gemm_fallback_subprocess():
-    """The one-CTA GEMM kernels (MOE_GEMM_SINGLE_CTA=1) pass the grouped-GEMM
-    and small-layer parity tests too (run in a child process: the choice is
-    read once per process)."""
-    env = dict(os.environ, MOE_GEMM_SINGLE_CTA="1")
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+def test_each_gemm_kernel_subprocess(kernel):
+    """Both grouped-GEMM kernels (one CTA per 128-row tile, and CTA pairs on
+    256-row tiles) pass the grouped-GEMM and layer parity tests when forced
+    with MOE_GEMM_KERNEL (the default picks per launch; the choice is read
+    once per process, hence the child process)."""
+    env = dict(os.environ, MOE_GEMM_KERNEL=kernel)
     cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
            os.path.join(ROOT, "tests", "test_gpu_steps.py"),
            os.path.join(ROOT, "tests", "test_gpu_layer.py"),
-           "-k", "grouped or small_all"]
+           "-k", "grouped or small_all or second_stream"]
     r = subprocess.run(cmd, env=env, cwd=ROOT, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
