@@ -37,6 +37,7 @@
 #include <stdlib.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -73,6 +74,7 @@ struct Params {
     int64_t ldo1;
     int32_t out1_f32;
     int32_t *dev_status;
+    unsigned int *tile_counter;   // pair kernel: next tile to hand out (zeroed per launch)
 };
 
 struct Tile {
@@ -419,15 +421,27 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
 //     to both CTAs (stage release, accumulator ready);
 //   - each CTA's epilogue reads its own TMEM rows and arrives on the even
 //     CTA's accumulator-empty barrier.
+// Tiles are handed out dynamically, in order, from a counter in global
+// memory, so the tiles in flight stay a tight window of the list (a static
+// round-robin lets lagging clusters drift onto data that has left L2).  The
+// even CTA's producer claims each tile and publishes it through a QD-deep
+// queue in shared memory: it writes the index into both CTAs' queue slot and
+// arrives on both slots' full barriers; the 10 readers (even CTA: MMA thread
+// and 4 epilogue warps; odd CTA: producer and 4 epilogue warps) arrive on
+// the even CTA's empty barrier once they have read it.  An index >= the
+// tile count ends every role's loop.
 constexpr int BM2 = 256;
 constexpr int STAGES2 = 6;
 constexpr int STAGE2_BYTES = 2 * A_BYTES;   // 128x64 A + 128x64 B per CTA
 constexpr int TMEM2_COLS = 512;
+constexpr int QD = 4;                        // tile-queue depth
+constexpr int Q_CONSUMERS = 10;              // see the queue protocol below
 struct Cfg2 {
     static constexpr int BAR_OFF = STAGES2 * STAGE2_BYTES;
-    static constexpr int NBARS = 2 * STAGES2 + 5;
+    static constexpr int NBARS = 2 * STAGES2 + 5 + 2 * QD;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-    static constexpr int OFFS_OFF = MISC_OFF + 16;
+    static constexpr int QT_OFF = MISC_OFF + 16;
+    static constexpr int OFFS_OFF = QT_OFF + QD * 4;
     static constexpr int PREFIX_OFF = OFFS_OFF + (MAX_GROUPS + 1) * 4;
     static constexpr int SMEM = 1024 + PREFIX_OFF + (MAX_GROUPS + 2) * 4;
 };
@@ -483,6 +497,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint64_t *tfull = bars + 2 * STAGES2;
     uint64_t *tempty = tfull + 2;               // used in the even CTA only
     uint64_t *drain = tempty + 2;
+    uint64_t *q_full = drain + 1;               // [QD]
+    uint64_t *q_empty = q_full + QD;            // [QD], used in the even CTA only
+    volatile int *q_tile = reinterpret_cast<volatile int *>(smem + Cfg2::QT_OFF);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + Cfg2::MISC_OFF);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + Cfg2::MISC_OFF + 4);
     volatile int *s_bad = reinterpret_cast<volatile int *>(smem + Cfg2::MISC_OFF + 8);
@@ -495,7 +512,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t rank = cluster_ctarank();     // 0 = even CTA (issues the MMAs)
     const bool leader = rank == 0;
     const int cid = static_cast<int>(cluster_id_x());
-    const int ncl = static_cast<int>(num_clusters_x());
 
     if (tid == 0) {
         *s_abort = 0;
@@ -536,6 +552,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             mbar_init(&tempty[a], 8);    // lane 0 of the 4 epilogue warps of both CTAs
         }
         mbar_init(drain, 1);
+        for (int q = 0; q < QD; ++q) {
+            mbar_init(&q_full[q], 1);
+            mbar_init(&q_empty[q], Q_CONSUMERS);
+        }
         fence_barrier_init();
     }
     __syncthreads();
@@ -558,6 +578,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t tmem_base = *s_tmem;
     const uint32_t lead_full = mapa_shared(smem_u32(full), 0);
     const uint32_t lead_tempty = mapa_shared(smem_u32(tempty), 0);
+    const uint32_t lead_qempty = mapa_shared(smem_u32(q_empty), 0);
+    const uint32_t peer_qfull = mapa_shared(smem_u32(q_full), 1);
+    const uint32_t peer_qtile = mapa_shared(static_cast<uint32_t>(__cvta_generic_to_shared(
+                                                const_cast<int *>(q_tile))), 1);
+    // Reader side of the tile queue (all roles but the even CTA's producer).
+    // Returns false when a wait gave up.
+    auto next_tile = [&](int &qi, uint32_t &qph, int &tile) -> bool {
+        if (!mbar_wait_bounded_cluster(&q_full[qi], qph, s_abort, p.dev_status)) return false;
+        tile = q_tile[qi];
+        mbar_arrive_cluster(lead_qempty + 8u * static_cast<uint32_t>(qi));
+        if (++qi == QD) {
+            qi = 0;
+            qph ^= 1;
+        }
+        return true;
+    };
 
     if (warp == 0) {
         // ================= TMA producer (both CTAs)
@@ -572,7 +608,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             uint32_t phase = 0;
             int armed[STAGES2];
             for (int s = 0; s < STAGES2; ++s) armed[s] = -1;
-            for (int tile = cid; tile < total && !*s_abort; tile += ncl) {
+            int qi = 0;
+            uint32_t qph = 0;
+            while (!*s_abort) {
+                int tile;
+                if (leader) {
+                    // claim the next tile and publish it to both CTAs
+                    if (!mbar_wait_bounded_cluster(&q_empty[qi], qph ^ 1, s_abort, p.dev_status))
+                        break;
+                    tile = static_cast<int>(atomicAdd(p.tile_counter, 1u));
+                    q_tile[qi] = tile;
+                    mbar_arrive(&q_full[qi]);
+                    st_shared_cluster_u32(peer_qtile + 4u * static_cast<uint32_t>(qi),
+                                          static_cast<uint32_t>(tile));
+                    mbar_arrive_cluster(peer_qfull + 8u * static_cast<uint32_t>(qi));
+                    if (++qi == QD) {
+                        qi = 0;
+                        qph ^= 1;
+                    }
+                } else if (!next_tile(qi, qph, tile)) {
+                    break;
+                }
+                if (tile >= total) break;
                 const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0);
                 const int arow = t.row0 + 128 * static_cast<int>(rank);
                 bool ok = true;
@@ -621,7 +678,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool issued = false;
-            for (int tile = cid; tile < total && !*s_abort; tile += ncl) {
+            int qi = 0;
+            uint32_t qph = 0;
+            while (!*s_abort) {
+                int tile;
+                if (!next_tile(qi, qph, tile) || tile >= total) break;
                 const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0);
                 if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, s_abort, p.dev_status)) break;
                 tc_fence_after();
@@ -665,7 +726,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int row_in_tile = 128 * static_cast<int>(rank) + q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = cid; tile < total; tile += ncl) {
+        int qi = 0;
+        uint32_t qph = 0;
+        for (;;) {
+            int tile = 0, got = 1;
+            if (lane == 0) {
+                // one reader per warp: wait, read, release the slot
+                if (mbar_wait_bounded_cluster(&q_full[qi], qph, s_abort, p.dev_status)) {
+                    tile = q_tile[qi];
+                    mbar_arrive_cluster(lead_qempty + 8u * static_cast<uint32_t>(qi));
+                } else {
+                    got = 0;
+                }
+            }
+            got = __shfl_sync(0xffffffffu, got, 0);
+            tile = __shfl_sync(0xffffffffu, tile, 0);
+            if (++qi == QD) {
+                qi = 0;
+                qph ^= 1;
+            }
+            if (!got || tile >= total) break;
             const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0);
             if (!mbar_wait_bounded(&tfull[acc], acc_phase, s_abort, p.dev_status)) break;
             tc_fence_after();
@@ -832,6 +912,39 @@ cudaError_t launch(Params &p, int max_rows0, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Tile counters of the pair kernel.  Each launch takes the next slot of a
+// ring of counters that live in the library's own device memory (no
+// allocation, graph-capturable) and zeroes it on its stream right before the
+// kernel.  Launches in flight at the same time (different streams) get
+// different slots as long as fewer than kTileCounters of them overlap.
+constexpr int kTileCounters = 256;
+constexpr int kMaxDev = 64;
+static __device__ unsigned int g_tile_counters[kTileCounters];
+
+struct CounterRing {
+    std::once_flag once;
+    unsigned int *base = nullptr;
+    cudaError_t err = cudaSuccess;
+    std::atomic<unsigned int> next{0};
+};
+CounterRing g_rings[kMaxDev];
+
+cudaError_t next_tile_counter(unsigned int **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    CounterRing &r = g_rings[dev];
+    std::call_once(r.once, [&r] {
+        void *ptr = nullptr;
+        r.err = cudaGetSymbolAddress(&ptr, g_tile_counters);
+        if (r.err == cudaSuccess) r.base = static_cast<unsigned int *>(ptr);
+    });
+    if (r.err != cudaSuccess) return r.err;
+    *out = r.base + (r.next.fetch_add(1u, std::memory_order_relaxed) % kTileCounters);
+    return cudaSuccess;
+}
+
 template <int MODE>
 cudaError_t launch_pair(Params &p, int max_rows0, cudaStream_t stream) {
     static std::mutex mu;
@@ -850,9 +963,9 @@ cudaError_t launch_pair(Params &p, int max_rows0, cudaStream_t stream) {
     }
     const int64_t mblocks0 = ceil_div(max_rows0, BM2) + p.G;
     const int64_t tiles = mblocks0 * p.nt0 + (p.rows1 > 0 ? ceil_div(p.rows1, BM2) * p.nt1 : 0);
-    // The static round-robin tile walk relies on every cluster running from
-    // the start: launch no more clusters than can be resident at once (CTA
-    // pairs need two SMs of one TPC, so this can be below num_sms / 2).
+    // Launch no more clusters than can be resident at once (CTA pairs need
+    // two SMs of one TPC, so this can be below num_sms / 2): a persistent
+    // cluster that waits for a free TPC only delays the tail.
     static int max_clusters[64] = {};
     if (dev < 64 && max_clusters[dev] == 0) {
         cudaLaunchConfig_t cfg = {};
@@ -874,6 +987,10 @@ cudaError_t launch_pair(Params &p, int max_rows0, cudaStream_t stream) {
     }
     const int limit = dev < 64 ? max_clusters[dev] : num_sms() / 2;
     const int clusters = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(limit, tiles)));
+    cudaError_t e = next_tile_counter(&p.tile_counter);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(p.tile_counter, 0, sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return e;
     grouped_gemm_pair_kernel<MODE><<<2 * clusters, THREADS, Cfg2::SMEM, stream>>>(p);
     return cudaGetLastError();
 }
