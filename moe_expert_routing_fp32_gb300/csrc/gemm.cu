@@ -75,6 +75,8 @@ struct Params {
     int32_t out1_f32;
     int32_t *dev_status;
     unsigned int *tile_counter;   // pair kernel: next tile to hand out (zeroed per launch)
+    CUtensorMap tmO0;   // pair kernel: segment-0 output, 32-row x 64-byte boxes, 64-byte swizzle
+    CUtensorMap tmO1;   // pair kernel: segment-1 output (bf16 or fp32)
 };
 
 struct Tile {
@@ -436,8 +438,10 @@ constexpr int STAGE2_BYTES = 2 * A_BYTES;   // 128x64 A + 128x64 B per CTA
 constexpr int TMEM2_COLS = 512;
 constexpr int QD = 4;                        // tile-queue depth
 constexpr int Q_CONSUMERS = 10;              // see the queue protocol below
+constexpr int EPI_BYTES = 32 * 64;           // one 32-row x 64-byte output box
 struct Cfg2 {
-    static constexpr int BAR_OFF = STAGES2 * STAGE2_BYTES;
+    static constexpr int EPI_OFF = STAGES2 * STAGE2_BYTES;   // 4 warps x 2 boxes, 1 KB aligned
+    static constexpr int BAR_OFF = EPI_OFF + 4 * 2 * EPI_BYTES;
     static constexpr int NBARS = 2 * STAGES2 + 5 + 2 * QD;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int QT_OFF = MISC_OFF + 16;
@@ -728,6 +732,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         uint32_t acc_phase = 0;
         int qi = 0;
         uint32_t qph = 0;
+        // Two 2 KB staging boxes per warp.  A box holds 32 rows x 64 bytes in
+        // the 64-byte swizzle of the output tensor map (16-byte chunk c of
+        // row r sits at chunk c ^ ((r >> 1) & 3)), which also keeps the
+        // lanes' shared-memory writes free of bank conflicts.
+        uint8_t *ebox = smem + Cfg2::EPI_OFF + (warp - 2) * 2 * EPI_BYTES;
+        int eb = 0;
+        auto emit_box = [&](const uint32_t(&w)[16], const CUtensorMap *map, int col, int row0) {
+            uint8_t *box = ebox + eb * EPI_BYTES;
+            if (lane == 0) bulk_wait_read<1>();     // the store that last used this box has read it
+            __syncwarp();
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch)
+                *reinterpret_cast<uint4 *>(box + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4)) =
+                    make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(map, box, col, row0);
+                bulk_commit();
+            }
+            eb ^= 1;
+        };
         for (;;) {
             int tile = 0, got = 1;
             if (lane == 0) {
@@ -751,6 +777,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             tc_fence_after();
             const int row = t.row0 + row_in_tile;
             const bool ok = row < t.row_end;
+            // All 32 rows of this warp inside the group: the results leave
+            // through TMA stores of whole 32-row boxes; otherwise (a group's
+            // last block) each lane stores its own row if it is in range.
+            const int row_base = t.row0 + row_in_tile - lane;
+            const bool boxed = row_base + 32 <= t.row_end;
+            const CUtensorMap *omap = t.seg == 0 ? &p.tmO0 : &p.tmO1;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             if (MODE == MODE_SWIGLU) {
@@ -771,7 +803,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                             __fdiv_rn(g[2 * i + 1], 1.0f + expf(-g[2 * i + 1])) * u[2 * i + 1];
                         pk[i] = pack_bf16x2(a0, a1);
                     }
-                    if (ok) {
+                    if (boxed) {
+                        emit_box(pk, omap, t.n_blk * 128 + c, row_base);
+                    } else if (ok) {
                         uint4 *dst = reinterpret_cast<uint4 *>(
                             out + static_cast<int64_t>(row) * ldo + t.n_blk * 128 + c);
 #pragma unroll
@@ -790,8 +824,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     __syncwarp();
                     tmem_ld32(taddr + c, v);
                     tmem_ld_wait();
+                    const int col = t.n_blk * BN + c;
+                    if (boxed) {
+                        if (f32) {
+                            uint32_t w[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[i]);
+                            emit_box(w, omap, col, row_base);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[16 + i]);
+                            emit_box(w, omap, col + 16, row_base);
+                        } else {
+                            uint32_t w[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                            emit_box(w, omap, col, row_base);
+                        }
+                        continue;
+                    }
                     if (!ok) continue;
-                    const int64_t off = static_cast<int64_t>(row) * ldo + t.n_blk * BN + c;
+                    const int64_t off = static_cast<int64_t>(row) * ldo + col;
                     if (f32) {
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(outp) + off);
 #pragma unroll
@@ -815,6 +867,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
+        if (lane == 0) bulk_wait<0>();   // every output box written
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -863,6 +917,34 @@ bool make_map(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims, i
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Output [rows, cols] (row stride ld elements, bf16 or fp32) as 32-row x
+// 64-byte boxes with the 64-byte swizzle, for the pair kernel's TMA stores.
+bool make_out_map(CUtensorMap *m, void *ptr, int rows, int cols, int64_t ld, bool f32) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const int esz = f32 ? 4 : 2;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(std::max(rows, 1))};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ld) * esz};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / esz), 32};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r =
+        fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, gdim,
+           gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Both output maps of a launch (a missing segment reuses the other's map).
+bool make_out_maps(Params &p, int cols0, int cols1) {
+    const bool have0 = p.G > 0, have1 = p.rows1 > 0;
+    if (have0 && !make_out_map(&p.tmO0, p.out0, p.rows0, cols0, p.ldo0, false)) return false;
+    if (have1 && !make_out_map(&p.tmO1, p.out1, p.rows1, cols1, p.ldo1, p.out1_f32 != 0))
+        return false;
+    if (!have0) p.tmO0 = p.tmO1;
+    if (!have1) p.tmO1 = p.tmO0;
+    return true;
 }
 
 // Which grouped-GEMM kernel runs: MOE_GEMM_KERNEL=pair or =single in the
@@ -1045,7 +1127,10 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
     p.ldo1 = seg1.N1;
     p.out1_f32 = 0;
     p.dev_status = dev_status;
-    if (pair) return launch_pair<MODE_SWIGLU>(p, n, stream);
+    if (pair) {
+        if (!make_out_maps(p, N, seg1.N1)) return cudaErrorInvalidValue;
+        return launch_pair<MODE_SWIGLU>(p, n, stream);
+    }
     return launch<MODE_SWIGLU, 256>(p, n, stream);
 }
 
@@ -1096,7 +1181,10 @@ cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, 
     p.ldo1 = seg1.N1;
     p.out1_f32 = seg1.out_f32 ? 1 : 0;
     p.dev_status = dev_status;
-    if (pair) return launch_pair<MODE_STORE>(p, n, stream);
+    if (pair) {
+        if (!make_out_maps(p, N, seg1.N1)) return cudaErrorInvalidValue;
+        return launch_pair<MODE_STORE>(p, n, stream);
+    }
     if (BN == 256) return launch<MODE_STORE, 256>(p, n, stream);
     return launch<MODE_STORE, 128>(p, n, stream);
 }
