@@ -245,6 +245,10 @@ def run_ours(args, rank, world, local):
             e.record()           # creates the event handles
     extra = {}
     two_streams = wl.I_s > 0 and args.shared_stream == "on"
+    # the recorded DRAM bytes were captured on the named workload as-is, with
+    # the shared expert inside the w13 launch
+    from moe_inputs import WORKLOADS
+    traffic_applies = wl == WORKLOADS[args.workload] and not two_streams
     if two_streams:
         s2 = torch.cuda.Stream(device=dev)
         fj = [torch.cuda.Event(), torch.cuda.Event()]
@@ -363,7 +367,7 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": round(achieved / tc_peak, 4),
                      "peak_source": f"bf16_tflops_sustained ({peak_src})",
-                     "traffic": recorded_traffic(wl.name)},
+                     "traffic": recorded_traffic(wl.name) if traffic_applies else None},
         "gemm_tflops": round(gemm_tflops, 1),
         "gemm_frac_bf16_peak": round(gemm_tflops / tc_peak, 4),
         "layer_gemm_tflops_over_step": round(layer_gemm_tflops, 1),

@@ -960,13 +960,16 @@ GemmChoice gemm_choice() {
     return c;
 }
 
-// 256-row pair tiles pay off when groups are large; with a few rows per
-// expert (weight streaming) the 128-row one-CTA tiles are faster.
+// 256-row pair tiles pay off when groups are large.  Each group's last
+// block is padded to the tile height, so with a few hundred rows per group
+// (about 512 measured: 25% padding at 256 rows, 13% at 128) and in weight
+// streaming the 128-row one-CTA tiles are faster; at 2048 rows per group the
+// pair kernel is.
 bool use_pair(int n, int G, int seg1_rows) {
     const GemmChoice c = gemm_choice();
     if (c != GEMM_AUTO) return c == GEMM_PAIR;
     const int64_t avg = G > 0 ? n / G : seg1_rows;
-    return avg >= 256;
+    return avg >= 1024;
 }
 
 template <int MODE, int BN>
