@@ -73,6 +73,32 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value, world, device="cpu"):
+    """The largest of the ranks' values (every rank gets it): the job's time
+    is the slowest replica's."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, tokens_per_rank, steps, elapsed_ms):
+    """Whole-job tokens/s: every rank processed tokens_per_rank per step."""
+    return world * tokens_per_rank * steps / (elapsed_ms / 1e3)
+
+
+def rank_inputs(wl, seed, rank, device):
+    """One replica's inputs: the weights are the same on every rank (seed),
+    the tokens are the rank's own batch (seed + rank)."""
+    from moe_inputs import make_inputs
+    g = make_inputs(wl, seed, device=device)
+    if rank > 0:
+        g["x"] = make_inputs(wl, seed + rank, device=device, only=["x"])["x"]
+    return g
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -222,13 +248,12 @@ def stage_bytes_flops(wl, two_streams=False):
 def run_ours(args, rank, world, local):
     import torch
     import moe_expert_routing_fp32_gb300 as moe
-    from moe_inputs import make_inputs
 
     moe.build()
     wl = workload_of(args)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    g = make_inputs(wl, args.seed, device=str(dev))
+    g = rank_inputs(wl, args.seed, rank, str(dev))
     weights = moe.LayerWeights(wg=g["wg"], w13=g["w13"], w2=g["w2"], gamma=g["gamma"],
                                gate_bias=g["gate_bias"], w13_s=g["w13_s"], w2_s=g["w2_s"])
     desc = moe.make_desc(wl.T, wl.H, wl.E, wl.k, wl.I, wl.I_s, rmsnorm=wl.rmsnorm, eps=wl.eps,
@@ -277,11 +302,7 @@ def run_ours(args, rank, world, local):
     if dist:
         torch.distributed.barrier()
     clk = clocks.stop()
-    elapsed_ms = start.elapsed_time(end)
-    if dist:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the timed steps")
 
@@ -310,12 +331,8 @@ def run_ours(args, rank, world, local):
                                workspace=ws, status=status, **extra)
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * wl.T * Ke / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_throughput(world, wl.T, Ke, e2e_ms)
     return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g,
                        two_streams)
 
@@ -324,7 +341,7 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
                 two_streams=False):
     import moe_expert_routing_fp32_gb300 as moe  # noqa: F401
     step_ms = elapsed_ms / K
-    value = world * wl.T * K / (elapsed_ms / 1e3)
+    value = job_throughput(world, wl.T, K, elapsed_ms)
     peaks, peak_src = load_peaks()
     work = stage_bytes_flops(wl, two_streams)
     dom = "gemm_w13_swiglu"
