@@ -276,8 +276,8 @@ moe_status_t moe_layer_forward_streams(const moe_desc_t *desc, const moe_bf16_t 
 
 /*
  * EP DoubleRouting, the steps local to one rank ("MoE EP优化": LocalRerouting
- * "在每个RANK内按照专家序对token进行重排", LocalFinalizeRerouting
- * "排序回第二次all_to_all后的排布").  After the token all_to_all a rank holds
+ * orders a rank's received tokens by its local experts; LocalFinalizeRerouting
+ * restores the order the second all_to_all expects).  After the token all_to_all a rank holds
  * the received rows grouped by source rank and, within a source rank,
  * ordered by local expert:
  *   recv_counts [ep_size, E_local] int32 device: rows from rank r for local

@@ -463,7 +463,7 @@ void oracle_bf16_to_float(const bf16_t *in, int64_t n, float *out)
 /* a source rank ordered by local expert (each rank sent its rows sorted by */
 /* expert).  counts[r*E_local + e] = rows from rank r for local expert e.     */
 /*                                                                          */
-/* LocalRerouting ("在每个RANK内按照专家序对token进行重排"): reorder the rows */
+/* LocalRerouting ("MoE EP优化"): reorder a rank's received rows            */
 /* by local expert, source rank second, arrival order third:                 */
 /*   local_x[d] = recv_x[local_src[d]],                                      */
 /*   local_counts[e] = sum_r counts[r][e], local_offsets = exclusive scan.   */
@@ -512,7 +512,7 @@ int oracle_local_rerouting(const bf16_t *recv_x, const int32_t *counts, int64_t 
     return ORACLE_OK;
 }
 
-/* LocalFinalizeRerouting ("排序回第二次all_to_all后的排布"): put the expert   */
+/* LocalFinalizeRerouting ("MoE EP优化"): put the expert                    */
 /* outputs back in the received order: recv_y[local_src[d]] = local_y[d].    */
 int oracle_local_finalize_rerouting(const bf16_t *local_y, const int32_t *local_src, int64_t n,
                                     int64_t H, bf16_t *recv_y)
