@@ -275,6 +275,34 @@ moe_status_t moe_layer_forward_streams(const moe_desc_t *desc, const moe_bf16_t 
                                        void *const *stage_events);
 
 /*
+ * moe_layer_forward over n_batches token batches held in host memory, with
+ * the copies overlapped with the compute: while batch i runs on `stream`,
+ * batch i+1's tokens are copied in on `copy_in` and batch i-1's output is
+ * copied out on `copy_out` (two device staging buffers each way).  The
+ * results are those of moe_layer_forward on each batch.
+ *   x_host[i]   [T, H] bf16, host memory (pinned, or the copies serialise)
+ *   out_host[i] [T, H] host memory, bf16 (fp32 with MOE_OUT_F32)
+ *   x_dev       device, 2*T*H bf16 (staging), 16-byte aligned
+ *   out_dev     device, 2 * T*H output elements (staging), 16-byte aligned
+ *   workspace   as moe_layer_forward (one workspace serves every batch)
+ *   stream, copy_in, copy_out: three distinct streams owned by the caller
+ *   events      6 cudaEvent_t owned by the caller, used only by this call
+ * Returns once everything is enqueued (nothing is synchronised): the last
+ * output is in host memory when copy_out has drained.  All arguments are
+ * checked before the first copy; a launch or copy error returns MOE_ERR_CUDA
+ * with the earlier batches still enqueued.
+ */
+moe_status_t moe_layer_forward_host(const moe_desc_t *desc, int32_t n_batches,
+                                    const moe_bf16_t *const *x_host, void *const *out_host,
+                                    const moe_bf16_t *gamma, const float *wg,
+                                    const float *gate_bias, const moe_bf16_t *w13,
+                                    const moe_bf16_t *w2, const moe_bf16_t *w13_s,
+                                    const moe_bf16_t *w2_s, moe_bf16_t *x_dev, void *out_dev,
+                                    void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                    moe_stream_t stream, moe_stream_t copy_in,
+                                    moe_stream_t copy_out, void *const *events);
+
+/*
  * EP DoubleRouting, the steps local to one rank ("MoE EP优化": LocalRerouting
  * orders a rank's received tokens by its local experts; LocalFinalizeRerouting
  * restores the order the second all_to_all expects).  After the token all_to_all a rank holds

@@ -36,7 +36,7 @@ EXPORTS = ("moe_status_string", "moe_rmsnorm_gate", "moe_gate_topk",
            "moe_expert_tokens",
            "moe_grouped_mlp", "moe_finalize_routing", "moe_layer_workspace_size",
            "moe_layer_forward", "moe_layer_forward_timed", "moe_layer_forward_streams",
-           "moe_local_rerouting",
+           "moe_layer_forward_host", "moe_local_rerouting",
            "moe_local_finalize_rerouting", "moe_selftest_wait_timeout")
 NUM_STAGES = 6
 STAGE_NAMES = ("router", "route_scan_scatter", "permute", "gemm_w13_swiglu", "gemm_down",
@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
                                             P, SZ, P, P, P],
                 "moe_layer_forward_streams": [ctypes.POINTER(MoeDesc), P, P, P, P, P, P, P, P, P,
                                               P, SZ, P, P, P, P, P, P],
+                "moe_layer_forward_host": [ctypes.POINTER(MoeDesc), I32, P, P, P, P, P, P, P, P,
+                                           P, P, P, P, SZ, P, P, P, P, P],
             }
             for name, args in sigs.items():
                 fn = getattr(L, name)
@@ -331,19 +333,73 @@ def layer_forward(desc: MoeDesc, x, weights: LayerWeights, out=None, workspace=N
     return out
 
 
+_host_pipes = {}
+
+
+def _host_pipe(dev):
+    """Per device: the two copy streams and six events of the host pipeline
+    (created once; a torch event gets its CUDA handle on its first record)."""
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    pipe = _host_pipes.get(key)
+    if pipe is None:
+        with torch.cuda.device(key):
+            cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+            evs = [torch.cuda.Event() for _ in range(6)]
+            for e in evs:
+                e.record(cin)
+            cin.synchronize()
+        pipe = _host_pipes[key] = (cin, cout, evs)
+    return pipe
+
+
 def layer_forward_host(desc: MoeDesc, x_host, weights: LayerWeights, out_host=None,
-                       x_dev=None, out_dev=None, workspace=None, status=None, **kw):
-    """The layer on host buffers: copies x (pinned host) to the device, runs
-    the layer and copies the result back into ``out_host`` (pinned), all on
-    the current stream; synchronises before returning ``out_host``."""
-    dev = weights.w13.device
-    if x_dev is None:
-        x_dev = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev)
-    x_dev.copy_(x_host, non_blocking=True)
-    out_dev = layer_forward(desc, x_dev, weights, out=out_dev, workspace=workspace,
-                            status=status, **kw)
+                       staging=None, workspace=None, status=None):
+    """The layer on token batches in host memory (moe_layer_forward_host).
+    ``x_host``: one [T, H] bf16 CPU tensor (pinned) or a list of them, one
+    per batch; the outputs land in ``out_host`` (the same form; pinned CPU
+    tensors are allocated when None).  Batch i+1's tokens are copied in and
+    batch i-1's output copied out while batch i runs on the current stream.
+    ``staging`` = (x_dev, out_dev): device tensors of 2*T*H elements
+    (allocated when None).  Returns once the last output has arrived."""
+    single = isinstance(x_host, torch.Tensor)
+    xs = [x_host] if single else list(x_host)
+    T, H = desc.T, desc.H
+    odt = torch.float32 if desc.flags & OUT_F32 else torch.bfloat16
+    for t in xs:
+        if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or \
+                tuple(t.shape) != (T, H):
+            raise ValueError("x_host: contiguous [T, H] bf16 CPU tensors")
     if out_host is None:
-        out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype, pin_memory=True)
-    out_host.copy_(out_dev, non_blocking=True)
-    torch.cuda.current_stream(dev).synchronize()
-    return out_host
+        outs = [torch.empty((T, H), dtype=odt, pin_memory=True) for _ in xs]
+    else:
+        outs = [out_host] if single else list(out_host)
+    if len(outs) != len(xs):
+        raise ValueError("one output per batch")
+    for t in outs:
+        if t.is_cuda or t.dtype != odt or not t.is_contiguous() or tuple(t.shape) != (T, H):
+            raise ValueError(f"out_host: contiguous [T, H] {odt} CPU tensors")
+    dev = weights.w13.device
+    if staging is None:
+        staging = (torch.empty((2, T, H), dtype=torch.bfloat16, device=dev),
+                   torch.empty((2, T, H), dtype=odt, device=dev))
+    x_dev, out_dev = staging
+    if x_dev.numel() < 2 * T * H or out_dev.numel() < 2 * T * H or out_dev.dtype != odt:
+        raise ValueError("staging: (x_dev, out_dev) with 2*T*H elements each")
+    if workspace is None:
+        workspace = torch.empty(max(layer_workspace_size(desc), 256), dtype=torch.uint8,
+                                device=dev)
+    cin, cout, evs = _host_pipe(dev)
+    cur = torch.cuda.current_stream(dev)
+    cin.wait_stream(cur)          # staging buffers and workspace as the caller left them
+    cout.wait_stream(cur)
+    n = len(xs)
+    xa = (ctypes.c_void_p * n)(*[t.data_ptr() for t in xs])
+    oa = (ctypes.c_void_p * n)(*[t.data_ptr() for t in outs])
+    ea = (ctypes.c_void_p * 6)(*[e.cuda_event for e in evs])
+    w = weights
+    _call("moe_layer_forward_host", ctypes.byref(desc), n, xa, oa, _ptr(w.gamma), _ptr(w.wg),
+          _ptr(w.gate_bias), _ptr(w.w13), _ptr(w.w2), _ptr(w.w13_s), _ptr(w.w2_s),
+          _ptr(x_dev), _ptr(out_dev), _ptr(workspace), workspace.numel(), _ptr(status),
+          _stream(dev), ctypes.c_void_p(cin.cuda_stream), ctypes.c_void_p(cout.cuda_stream), ea)
+    cout.synchronize()
+    return outs[0] if single else outs

@@ -435,4 +435,72 @@ moe_status_t moe_layer_forward_streams(const moe_desc_t *desc, const moe_bf16_t 
                               shared_stream, fork_event, join_event);
 }
 
+moe_status_t moe_layer_forward_host(const moe_desc_t *desc, int32_t n_batches,
+                                    const moe_bf16_t *const *x_host, void *const *out_host,
+                                    const moe_bf16_t *gamma, const float *wg,
+                                    const float *gate_bias, const moe_bf16_t *w13,
+                                    const moe_bf16_t *w2, const moe_bf16_t *w13_s,
+                                    const moe_bf16_t *w2_s, moe_bf16_t *x_dev, void *out_dev,
+                                    void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                    moe_stream_t stream, moe_stream_t copy_in,
+                                    moe_stream_t copy_out, void *const *events) {
+    moe_status_t st = check_desc(desc);
+    if (st != MOE_OK) return st;
+    if (n_batches < 0) return MOE_ERR_INVALID_ARG;
+    if (n_batches == 0 || desc->T == 0) return MOE_OK;
+    if (!x_host || !out_host || !x_dev || !out_dev || !events || !copy_in || !copy_out ||
+        copy_in == stream || copy_out == stream || copy_in == copy_out)
+        return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; ++i)
+        if (!events[i]) return MOE_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n_batches; ++i)
+        if (!x_host[i] || !out_host[i]) return MOE_ERR_INVALID_ARG;
+    // the per-batch layer checks, once, before anything is enqueued
+    const bool shared = (desc->flags & MOE_SHARED) != 0;
+    if (!wg || !w13 || !w2 || (shared && (!w13_s || !w2_s))) return MOE_ERR_INVALID_ARG;
+    if (!a16(x_dev) || !a16(out_dev) || !a16(wg) || !a16(w13) || !a16(w2) ||
+        (gamma && !a16(gamma)) || (shared && (!a16(w13_s) || !a16(w2_s))))
+        return MOE_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < layer_layout(*desc).total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    const size_t rows = static_cast<size_t>(desc->T) * desc->H;
+    const size_t x_bytes = rows * 2;
+    const size_t o_bytes = rows * ((desc->flags & MOE_OUT_F32) ? 4 : 2);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t cin = reinterpret_cast<cudaStream_t>(copy_in);
+    cudaStream_t cout = reinterpret_cast<cudaStream_t>(copy_out);
+    cudaEvent_t in_ready[2] = {static_cast<cudaEvent_t>(events[0]),
+                               static_cast<cudaEvent_t>(events[1])};
+    cudaEvent_t computed[2] = {static_cast<cudaEvent_t>(events[2]),
+                               static_cast<cudaEvent_t>(events[3])};
+    cudaEvent_t copied_out[2] = {static_cast<cudaEvent_t>(events[4]),
+                                 static_cast<cudaEvent_t>(events[5])};
+    auto cuda = [](cudaError_t e) { return e == cudaSuccess; };
+    for (int32_t i = 0; i < n_batches; ++i) {
+        const int b = i & 1;
+        uint16_t *xb = reinterpret_cast<uint16_t *>(x_dev) + b * rows;
+        uint8_t *ob = static_cast<uint8_t *>(out_dev) + b * o_bytes;
+        // tokens in: staging buffer b was last read by batch i-2's layer
+        if (i >= 2 && !cuda(cudaStreamWaitEvent(cin, computed[b], 0))) return MOE_ERR_CUDA;
+        if (!cuda(cudaMemcpyAsync(xb, x_host[i], x_bytes, cudaMemcpyHostToDevice, cin)) ||
+            !cuda(cudaEventRecord(in_ready[b], cin)))
+            return MOE_ERR_CUDA;
+        // the layer: after its tokens landed and batch i-2's output left buffer b
+        if (!cuda(cudaStreamWaitEvent(s, in_ready[b], 0))) return MOE_ERR_CUDA;
+        if (i >= 2 && !cuda(cudaStreamWaitEvent(s, copied_out[b], 0))) return MOE_ERR_CUDA;
+        st = layer_forward_impl(desc, reinterpret_cast<const moe_bf16_t *>(xb), gamma, wg,
+                                gate_bias, w13, w2, w13_s, w2_s, ob, workspace, workspace_bytes,
+                                dev_status, stream, nullptr, nullptr, nullptr, nullptr);
+        if (st != MOE_OK) return st;
+        if (!cuda(cudaEventRecord(computed[b], s))) return MOE_ERR_CUDA;
+        // output out
+        if (!cuda(cudaStreamWaitEvent(cout, computed[b], 0)) ||
+            !cuda(cudaMemcpyAsync(out_host[i], ob, o_bytes, cudaMemcpyDeviceToHost, cout)) ||
+            !cuda(cudaEventRecord(copied_out[b], cout)))
+            return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
 }  // extern "C"

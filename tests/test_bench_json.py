@@ -1,0 +1,58 @@
+"""bench.py's JSON line, assembled on CPU from synthetic stage times: the
+keys the benchmark contract asks for, the roofline arithmetic and the
+traffic figure (only for the unmodified named workload)."""
+import argparse
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from moe_inputs import WORKLOADS  # noqa: E402
+
+
+def _args(**kw):
+    a = dict(workload="imagegen-16k", no_cpu_baseline=True, cpu_seconds=0.1, gpus=1, steps=10,
+             warmup=3, T=None, E=None, I=None, Is=None, tp=1, shared_stream="off", seed=0,
+             no_e2e=False, impl="ours")
+    a.update(kw)
+    return argparse.Namespace(**a)
+
+
+def _stages(ms):
+    import moe_expert_routing_fp32_gb300 as moe
+    return {n: ms for n in moe.STAGE_NAMES}
+
+
+CLK = {"sm_mhz": 1700.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+
+
+def test_json_line_keys_and_roofline():
+    args = _args()
+    wl = WORKLOADS["imagegen-16k"]
+    stages = _stages(1.0)
+    stages["gemm_w13_swiglu"] = 4.5
+    res = bench.finish_ours(args, wl, 1, 0, 10, 3, 80.0, stages, CLK, 1.9e6, {})
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "e2e", "gpu_launches", "clocks"):
+        assert key in res, key
+    assert res["value"] == pytest.approx(16384 * 10 / 0.080)
+    assert res["ms_per_step"] == pytest.approx(8.0)
+    r = res["roofline"]
+    flops = 4.0 * wl.T * wl.k * wl.H * wl.I + 4.0 * wl.T * wl.H * wl.I_s
+    assert r["achieved"] == pytest.approx(flops / 4.5e-3 / 1e12, rel=1e-3)
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"], rel=1e-3)
+    assert r["traffic"] is None or r["traffic"] > 4e9      # recorded for this workload
+    assert res["e2e"]["h2d_bytes_per_step"] == wl.T * wl.H * 2
+    assert res["config"]["workload"] == "imagegen-16k"
+
+
+def test_traffic_not_reported_for_a_resized_workload():
+    args = _args(I=128, Is=128)
+    wl = bench.workload_of(args)
+    res = bench.finish_ours(args, wl, 1, 0, 10, 3, 10.0, _stages(0.5), CLK, None, {})
+    assert res["roofline"]["traffic"] is None
+    assert res["e2e"] is None

@@ -161,3 +161,24 @@ def test_shared_expert_on_second_stream_matches():
     assert torch.equal(a, b)
     ref, _, _ = oracle.layer_tokens(d, wl)
     check_out(t2f64(b), ref, bf16_out=False, what="two streams")
+
+
+@pytest.mark.parametrize("out_f32", [False, True], ids=["bf16", "f32"])
+def test_host_pipeline_matches_device_layer(out_f32):
+    """moe_layer_forward_host over several host batches (copies overlapped
+    with the compute) gives, batch by batch, the device layer's bytes."""
+    wl = Workload("host-pipe", T=600, H=256, E=16, k=4, I=256, I_s=128, rmsnorm=True,
+                  gamma_std=0.1)
+    g = make_inputs(wl, 3, device=DEV)
+    xs = [make_inputs(wl, 10 + i, only=["x"])["x"].pin_memory() for i in range(5)]
+    desc = _desc(wl, out_f32=out_f32)
+    st = moe.new_status(DEV)
+    outs = moe.layer_forward_host(desc, xs, _weights(g), status=st)
+    assert int(st.item()) == 0
+    for x, o in zip(xs, outs):
+        ref = moe.layer_forward(desc, x.to(DEV), _weights(g))
+        torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16 if not out_f32 else torch.int32),
+                           ref.cpu().view(torch.int16 if not out_f32 else torch.int32))
+    one = moe.layer_forward_host(desc, xs[0], _weights(g))       # a single tensor in, out
+    assert torch.equal(one, outs[0])
