@@ -410,32 +410,70 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
 // Few tokens (T <= 512): one CTA per token and one thread per expert, so
 // that every logit's sequential FMA chain runs at the same time.  The row is
 // kept in shared memory as fp32; thread 0 takes the sum of squares in
-// ascending h; the gate weight streams through a SM_SLOTS-deep cp.async ring
+// ascending h; the gate weight streams through a SLOTS-deep cp.async ring
 // in 64-column chunks (rows padded to 68 floats: conflict-free 16-byte
-// reads), filled while the sum of squares runs.
+// reads), filled while the sum of squares runs.  Every CTA streams the whole
+// gate weight from L2: a chunk arrives as two TMA tensor boxes (E rows x 32
+// fp32 columns, 128-byte swizzle: 16-byte piece q of row e sits at piece
+// q ^ (e & 7)) completed on the slot's mbarrier, which keeps far more bytes
+// in flight per SM than per-thread 16-byte copies.  With at most one CTA per
+// SM the ring is as deep as shared memory allows (11 chunks in flight); with
+// more tokens it is sized for two CTAs per SM.
 // Same arithmetic, in the same order, as the tiled kernel above.
 constexpr int SM_HC = 64;
-constexpr int SM_LD = 68;
-constexpr int SM_SLOTS = 4;
+constexpr int SM_SMEM_CAP = 220 * 1024;
+// bytes of one 32-column half of a ring slot: E rows of 128 bytes, rounded to
+// whole 1 KB swizzle atoms
+__host__ __device__ inline int sm_half_bytes(int E) { return ((E + 7) / 8) * 1024; }
 constexpr int SMALL_MAX_T = 512;
 constexpr int SMALL_MAX_E = 128;
 constexpr int SMALL_MAX_H = 8192;
 
+template <int SLOTS>
 __global__ void __launch_bounds__(128)
 router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
                     const float *__restrict__ wg, const float *__restrict__ gate_bias, int H,
                     int E, float eps, int rmsnorm, uint16_t *__restrict__ xn,
                     float *__restrict__ logits, int fuse_topk, int k, int renorm,
-                    int32_t *__restrict__ topk_idx, float *__restrict__ topk_w) {
-    extern __shared__ __align__(16) float sm[];
-    float *xf = sm;                    // [H]
-    float *ring = sm + H;              // [SM_SLOTS][E][SM_LD]
+                    int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+                    int32_t *dev_status, const __grid_constant__ CUtensorMap tmw) {
+    extern __shared__ uint8_t sm_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int hb = sm_half_bytes(E);   // ring: [SLOTS][2 halves][hb]
+    float *xf = reinterpret_cast<float *>(ring + SLOTS * 2 * hb);   // [H]
     __shared__ float s_r;
     __shared__ float s_lg[SMALL_MAX_E];
+    __shared__ __align__(8) uint64_t s_full[SLOTS];
+    __shared__ int s_abort_v;
+    volatile int *s_abort = &s_abort_v;
     const int t = blockIdx.x;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const int nvec = H / 8;
+    const int nch = H / SM_HC;
+
+    if (tid == 0) {
+        *s_abort = 0;
+        for (int q = 0; q < SLOTS; ++q) mbar_init(&s_full[q], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // chunk c of the gate weight into slot c % SLOTS (thread 0: two boxes)
+    auto issue = [&](int c) {
+        if (tid != 0) return;
+        const int st = c % SLOTS;
+        mbar_arrive_expect_tx(&s_full[st], static_cast<uint32_t>(E) * SM_HC * 4);
+        uint8_t *slot = ring + st * 2 * hb;
+        tma_load_2d(slot, &tmw, &s_full[st], c * SM_HC, 0);
+        tma_load_2d(slot + hb, &tmw, &s_full[st], c * SM_HC + SM_HC / 2, 0);
+    };
+    // every thread waits for chunk c (bounded; a timeout is reported)
+    auto wait_chunk = [&](int c) {
+        mbar_wait_bounded(&s_full[c % SLOTS], static_cast<uint32_t>((c / SLOTS) & 1), s_abort,
+                          dev_status);
+    };
+    for (int c = 0; c < SLOTS - 1 && c < nch; ++c) issue(c);
 
     const uint4 *xq = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
     for (int v = tid; v < nvec; v += nthr) {
@@ -449,21 +487,6 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
         }
         *reinterpret_cast<float4 *>(xf + 8 * v) = make_float4(f[0], f[1], f[2], f[3]);
         *reinterpret_cast<float4 *>(xf + 8 * v + 4) = make_float4(f[4], f[5], f[6], f[7]);
-    }
-    const int nch = H / SM_HC;
-    auto issue = [&](int c) {
-        const int st = c % SM_SLOTS;
-        const int h0 = c * SM_HC;
-        for (int i = tid; i < E * (SM_HC / 4); i += nthr) {
-            const int e = i / (SM_HC / 4), q = i % (SM_HC / 4);
-            cp_async16(ring + (st * E + e) * SM_LD + 4 * q,
-                       wg + static_cast<size_t>(e) * H + h0 + 4 * q, 16);
-        }
-    };
-#pragma unroll
-    for (int c = 0; c < SM_SLOTS - 1; ++c) {
-        if (c < nch) issue(c);
-        cp_async_commit();
     }
     __syncthreads();
 
@@ -525,26 +548,52 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
         __syncthreads();
     }
 
+    // The logit's FMA chain is the critical path: its operands are read into
+    // registers half a chunk (32 columns) ahead, so the chain never waits on
+    // shared memory; chunk c+1's arrival is awaited between the two halves.
     const int e = tid;
+    const int er = e < E ? e : 0;             // threads past E follow along on row 0
+    constexpr int HQ = SM_HC / 8;             // float4s per half chunk
     float acc = 0.0f;
-    for (int c = 0; c < nch; ++c) {
-        if (c + SM_SLOTS - 1 < nch) issue(c + SM_SLOTS - 1);
-        cp_async_commit();
-        cp_async_wait<SM_SLOTS - 1>();
-        __syncthreads();
-        if (e < E) {
-            const float *wr = ring + ((c % SM_SLOTS) * E + e) * SM_LD;
-            const float *xc = xf + c * SM_HC;
+    float4 wa[HQ], xa[HQ], wb[HQ], xb[HQ];
+    auto load_half = [&](int c, int half, float4 (&w)[HQ], float4 (&xv)[HQ]) {
+        const uint8_t *wr = ring + ((c % SLOTS) * 2 + half) * hb + er * 128;
+        const float *xc = xf + c * SM_HC + half * (SM_HC / 2);
 #pragma unroll
-            for (int q = 0; q < SM_HC / 4; ++q) {
-                const float4 wv = *reinterpret_cast<const float4 *>(wr + 4 * q);
-                const float4 xv = *reinterpret_cast<const float4 *>(xc + 4 * q);
-                acc = __fmaf_rn(xv.x, wv.x, acc);
-                acc = __fmaf_rn(xv.y, wv.y, acc);
-                acc = __fmaf_rn(xv.z, wv.z, acc);
-                acc = __fmaf_rn(xv.w, wv.w, acc);
-            }
+        for (int q = 0; q < HQ; ++q) {
+            w[q] = *reinterpret_cast<const float4 *>(wr + ((q ^ (er & 7)) << 4));
+            xv[q] = *reinterpret_cast<const float4 *>(xc + 4 * q);
         }
+    };
+    auto fma_half = [&](const float4 (&w)[HQ], const float4 (&xv)[HQ]) {
+#pragma unroll
+        for (int q = 0; q < HQ; ++q) {
+            acc = __fmaf_rn(xv[q].x, w[q].x, acc);
+            acc = __fmaf_rn(xv[q].y, w[q].y, acc);
+            acc = __fmaf_rn(xv[q].z, w[q].z, acc);
+            acc = __fmaf_rn(xv[q].w, w[q].w, acc);
+        }
+    };
+    wait_chunk(0);
+    load_half(0, 0, wa, xa);
+    for (int c = 0; c < nch; ++c) {
+        // every thread has consumed the registers it read from chunk c-1's slot
+        __syncthreads();
+        if (c + SLOTS - 1 < nch) issue(c + SLOTS - 1);
+        load_half(c, 1, wb, xb);
+        fma_half(wa, xa);
+        if (c + 1 < nch) {
+            wait_chunk(c + 1);
+            load_half(c + 1, 0, wa, xa);
+        }
+        fma_half(wb, xb);
+    }
+    if (*s_abort) {
+        // unwinding after a timed-out wait: let the copies still in flight land
+        __syncthreads();
+        if (tid == 0)
+            for (int c = nch - SLOTS; c < nch; ++c)
+                if (c >= 0) mbar_wait_drain(&s_full[c % SLOTS], static_cast<uint32_t>((c / SLOTS) & 1));
         __syncthreads();
     }
     if (e < E) {
@@ -597,6 +646,32 @@ topk_kernel(const float *__restrict__ logits, int T, int E, int k, int renorm,
 
 }  // namespace
 
+// The gate weight [E, H] fp32 as 32-column x E-row boxes, 128-byte swizzle.
+typedef CUresult (*EncodeTiledFnR)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+bool make_wg_map(CUtensorMap *m, const float *wg, int H, int E) {
+    static EncodeTiledFnR fn = [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<EncodeTiledFnR>(ptr);
+        return static_cast<EncodeTiledFnR>(nullptr);
+    }();
+    if (!fn) return false;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(E)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(H) * 4};
+    cuuint32_t box[2] = {SM_HC / 2, static_cast<cuuint32_t>(E)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(wg), gdim, gstride, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float *wg,
                           const float *gate_bias, int T, int H, int E, float eps, bool rmsnorm,
                           uint16_t *xn, float *logits, bool fuse_topk, int k, bool renorm,
@@ -605,16 +680,35 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
     if (T == 0) return cudaSuccess;
     if (T <= SMALL_MAX_T && E <= SMALL_MAX_E && H <= SMALL_MAX_H) {
         const int threads = std::max(64, static_cast<int>(ceil_div(E, 32)) * 32);
-        const size_t smem = (static_cast<size_t>(H) + SM_SLOTS * E * SM_LD) * sizeof(float);
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(router_small_kernel,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
-            if (e != cudaSuccess) return e;
-        }
-        router_small_kernel<<<T, threads, smem, stream>>>(
-            x, gamma, wg, gate_bias, H, E, eps, rmsnorm ? 1 : 0, xn, logits, fuse_topk ? 1 : 0,
-            k, renorm ? 1 : 0, topk_idx, topk_w);
+        CUtensorMap tmw;
+        if (!make_wg_map(&tmw, wg, H, E)) return cudaErrorInvalidValue;
+        auto smem_for = [&](int slots) {
+            return 1024 + static_cast<size_t>(slots) * 2 * sm_half_bytes(E) +
+                   static_cast<size_t>(H) * sizeof(float);
+        };
+        auto run = [&](auto kernel, int slots) -> cudaError_t {
+            const size_t smem = smem_for(slots);
+            if (smem > 48 * 1024) {
+                cudaError_t e = cudaFuncSetAttribute(
+                    kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+                if (e != cudaSuccess) return e;
+            }
+            kernel<<<T, threads, smem, stream>>>(x, gamma, wg, gate_bias, H, E, eps,
+                                                 rmsnorm ? 1 : 0, xn, logits, fuse_topk ? 1 : 0,
+                                                 k, renorm ? 1 : 0, topk_idx, topk_w, dev_status,
+                                                 tmw);
+            return cudaSuccess;
+        };
+        // up to one CTA per SM: the deepest ring that fits; more tokens than
+        // SMs: a ring that lets two CTAs share an SM
+        cudaError_t le;
+        if (T <= num_sms() && smem_for(12) <= SM_SMEM_CAP)
+            le = run(router_small_kernel<12>, 12);
+        else if (smem_for(5) <= SM_SMEM_CAP / 2)
+            le = run(router_small_kernel<5>, 5);
+        else
+            le = run(router_small_kernel<3>, 3);
+        if (le != cudaSuccess) return le;
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess || !fuse_topk || hist == nullptr) return e;
         return launch_route_hist(topk_idx, T, k, E, hist, dev_status, stream);

@@ -239,29 +239,56 @@ expert_tokens_kernel(const int32_t *__restrict__ ids, int n, int E, int32_t *__r
     }
 }
 
+// out[t] = sum_j w[t,j] * y_exp[row_idx[t*k+j]] (+ shared[t]), fp32 in slot
+// order.  The token's k row indices and weights are read once into shared
+// memory; a lane then issues the loads of 8 slots' 16-byte pieces before it
+// accumulates them (in slot order).  blockIdx.y splits the row's columns
+// when there are few tokens.
 template <bool SHARED_F32, bool OUT_F32>
 __global__ void __launch_bounds__(128)
 finalize_kernel(const uint16_t *__restrict__ y_exp, const int32_t *__restrict__ row_idx,
                 const float *__restrict__ topk_w, const void *__restrict__ shared, int T, int H,
                 int k, void *__restrict__ out) {
+    __shared__ int s_row[32];
+    __shared__ float s_w[32];
     const int nvec = H / 8;
+    const int vchunk = (nvec + gridDim.y - 1) / gridDim.y;
+    const int v0 = blockIdx.y * vchunk;
+    const int v1 = min(nvec, v0 + vchunk);
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
-        for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+        __syncthreads();                       // the previous token's slots are consumed
+        if (threadIdx.x < k) {
+            s_row[threadIdx.x] = row_idx[static_cast<size_t>(t) * k + threadIdx.x];
+            s_w[threadIdx.x] = topk_w[static_cast<size_t>(t) * k + threadIdx.x];
+        }
+        __syncthreads();
+        for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
             float acc[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-            for (int j = 0; j < k; ++j) {
-                const int row = row_idx[static_cast<size_t>(t) * k + j];
-                if (row < 0) continue;
-                const float w = topk_w[static_cast<size_t>(t) * k + j];
-                const uint4 q =
-                    reinterpret_cast<const uint4 *>(y_exp + static_cast<size_t>(row) * H)[v];
-                const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+            for (int j0 = 0; j0 < k; j0 += 8) {
+                uint4 q[8];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] = __fmaf_rn(w, __uint_as_float(wd[i] << 16), acc[2 * i]);
-                    acc[2 * i + 1] =
-                        __fmaf_rn(w, __uint_as_float(wd[i] & 0xFFFF0000u), acc[2 * i + 1]);
+                for (int u = 0; u < 8; ++u) {
+                    const int j = j0 + u;
+                    const int row = j < k ? s_row[j] : -1;
+                    q[u] = row >= 0
+                               ? __ldg(reinterpret_cast<const uint4 *>(
+                                           y_exp + static_cast<size_t>(row) * H) + v)
+                               : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int j = j0 + u;
+                    if (j >= k || s_row[j] < 0) continue;
+                    const float w = s_w[j];
+                    const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[2 * i] = __fmaf_rn(w, __uint_as_float(wd[i] << 16), acc[2 * i]);
+                        acc[2 * i + 1] =
+                            __fmaf_rn(w, __uint_as_float(wd[i] & 0xFFFF0000u), acc[2 * i + 1]);
+                    }
                 }
             }
             if (shared) {
@@ -353,7 +380,14 @@ cudaError_t launch_finalize(const uint16_t *y_exp, const int32_t *row_idx, const
                             const void *shared, bool shared_f32, int T, int H, int k,
                             void *out, bool out_f32, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    const int grid = grid_for_rows(T, 16);
+    // few tokens: split each row's columns over blocks (>= 128 vectors each)
+    // so that about two blocks per SM run
+    const int nvec = H / 8;
+    const int want = num_sms() * 2;
+    const int ysplit = T >= want ? 1
+                                 : static_cast<int>(std::max<int64_t>(
+                                       1, std::min<int64_t>(ceil_div(want, T), nvec / 128)));
+    const dim3 grid(static_cast<unsigned>(grid_for_rows(T, 16)), static_cast<unsigned>(ysplit));
     if (shared_f32 && out_f32)
         finalize_kernel<true, true><<<grid, 128, 0, stream>>>(y_exp, row_idx, topk_w, shared, T,
                                                               H, k, out);
