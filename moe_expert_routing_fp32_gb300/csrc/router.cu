@@ -429,8 +429,16 @@ constexpr int SMALL_MAX_T = 512;
 constexpr int SMALL_MAX_E = 128;
 constexpr int SMALL_MAX_H = 8192;
 
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Threads [0, nc) are the consumers (one per expert, nc = max(64, E rounded
+// up to 32)); the warp after them only streams the gate weight: it refills a
+// slot once every consumer warp has arrived on the slot's empty barrier, so
+// the consumers' FMA chains never stop at a block-wide barrier.
 template <int SLOTS>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(160)
 router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
                     const float *__restrict__ wg, const float *__restrict__ gate_bias, int H,
                     int E, float eps, int rmsnorm, uint16_t *__restrict__ xn,
@@ -445,38 +453,54 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
     __shared__ float s_r;
     __shared__ float s_lg[SMALL_MAX_E];
     __shared__ __align__(8) uint64_t s_full[SLOTS];
+    __shared__ __align__(8) uint64_t s_empty[SLOTS];
     __shared__ int s_abort_v;
     volatile int *s_abort = &s_abort_v;
     const int t = blockIdx.x;
     const int tid = threadIdx.x;
-    const int nthr = blockDim.x;
+    const int nc = blockDim.x - 32;      // consumer threads
     const int nvec = H / 8;
     const int nch = H / SM_HC;
 
     if (tid == 0) {
         *s_abort = 0;
-        for (int q = 0; q < SLOTS; ++q) mbar_init(&s_full[q], 1);
+        for (int q = 0; q < SLOTS; ++q) {
+            mbar_init(&s_full[q], 1);
+            mbar_init(&s_empty[q], nc / 32);
+        }
         fence_barrier_init();
     }
     __syncthreads();
-    // chunk c of the gate weight into slot c % SLOTS (thread 0: two boxes)
-    auto issue = [&](int c) {
-        if (tid != 0) return;
-        const int st = c % SLOTS;
-        mbar_arrive_expect_tx(&s_full[st], static_cast<uint32_t>(E) * SM_HC * 4);
-        uint8_t *slot = ring + st * 2 * hb;
-        tma_load_2d(slot, &tmw, &s_full[st], c * SM_HC, 0);
-        tma_load_2d(slot + hb, &tmw, &s_full[st], c * SM_HC + SM_HC / 2, 0);
-    };
-    // every thread waits for chunk c (bounded; a timeout is reported)
-    auto wait_chunk = [&](int c) {
-        mbar_wait_bounded(&s_full[c % SLOTS], static_cast<uint32_t>((c / SLOTS) & 1), s_abort,
-                          dev_status);
-    };
-    for (int c = 0; c < SLOTS - 1 && c < nch; ++c) issue(c);
 
+    if (tid >= nc) {
+        // ---- producer warp: chunk c of the gate weight into slot c % SLOTS
+        if (tid == nc) {
+            int issued = 0;
+            for (int c = 0; c < nch; ++c) {
+                const int st = c % SLOTS;
+                if (c >= SLOTS &&
+                    !mbar_wait_bounded(&s_empty[st], static_cast<uint32_t>((c / SLOTS - 1) & 1),
+                                       s_abort, dev_status))
+                    break;
+                mbar_arrive_expect_tx(&s_full[st], static_cast<uint32_t>(E) * SM_HC * 4);
+                uint8_t *slot = ring + st * 2 * hb;
+                tma_load_2d(slot, &tmw, &s_full[st], c * SM_HC, 0);
+                tma_load_2d(slot + hb, &tmw, &s_full[st], c * SM_HC + SM_HC / 2, 0);
+                issued = c + 1;
+            }
+            if (*s_abort) {
+                // unwinding: let the copies still in flight land
+                for (int c = issued - SLOTS; c < issued; ++c)
+                    if (c >= 0)
+                        mbar_wait_drain(&s_full[c % SLOTS], static_cast<uint32_t>((c / SLOTS) & 1));
+            }
+        }
+        return;
+    }
+
+    // ---- consumers
     const uint4 *xq = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
-    for (int v = tid; v < nvec; v += nthr) {
+    for (int v = tid; v < nvec; v += nc) {
         const uint4 q = xq[v];
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
         float f[8];
@@ -488,37 +512,27 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
         *reinterpret_cast<float4 *>(xf + 8 * v) = make_float4(f[0], f[1], f[2], f[3]);
         *reinterpret_cast<float4 *>(xf + 8 * v + 4) = make_float4(f[4], f[5], f[6], f[7]);
     }
-    __syncthreads();
+    consumer_sync(nc);
 
     if (rmsnorm) {
         if (tid == 0) {
-            // one sequential chain; the 16-byte loads run ahead of it
+            // one sequential chain, fed by 16-byte shared loads
             float ss = 0.0f;
             const float4 *xv = reinterpret_cast<const float4 *>(xf);
-            float4 cur[4], nxt[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) cur[u] = xv[u];
-            for (int b = 0; b < H / 16; ++b) {
-                if (b + 1 < H / 16) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) nxt[u] = xv[4 * (b + 1) + u];
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    ss = __fmaf_rn(cur[u].x, cur[u].x, ss);
-                    ss = __fmaf_rn(cur[u].y, cur[u].y, ss);
-                    ss = __fmaf_rn(cur[u].z, cur[u].z, ss);
-                    ss = __fmaf_rn(cur[u].w, cur[u].w, ss);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+#pragma unroll 8
+            for (int b = 0; b < H / 4; ++b) {
+                const float4 q = xv[b];
+                ss = __fmaf_rn(q.x, q.x, ss);
+                ss = __fmaf_rn(q.y, q.y, ss);
+                ss = __fmaf_rn(q.z, q.z, ss);
+                ss = __fmaf_rn(q.w, q.w, ss);
             }
             const float mean = __fdiv_rn(ss, static_cast<float>(H));
             s_r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
         }
-        __syncthreads();
+        consumer_sync(nc);
         const float r = s_r;
-        for (int v = tid; v < nvec; v += nthr) {
+        for (int v = tid; v < nvec; v += nc) {
             float gm[8];
             if (gamma) {
                 const uint4 gq = reinterpret_cast<const uint4 *>(gamma)[v];
@@ -545,13 +559,15 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
                 reinterpret_cast<uint4 *>(xn + static_cast<size_t>(t) * H)[v] =
                     make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
-        __syncthreads();
+        consumer_sync(nc);
     }
 
     // The logit's FMA chain is the critical path: its operands are read into
     // registers half a chunk (32 columns) ahead, so the chain never waits on
-    // shared memory; chunk c+1's arrival is awaited between the two halves.
+    // shared memory.  A warp releases a slot (empty barrier) once its loads
+    // of the slot's second half are issued.
     const int e = tid;
+    const int lane = tid & 31;
     const int er = e < E ? e : 0;             // threads past E follow along on row 0
     constexpr int HQ = SM_HC / 8;             // float4s per half chunk
     float acc = 0.0f;
@@ -574,13 +590,16 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
             acc = __fmaf_rn(xv[q].w, w[q].w, acc);
         }
     };
+    auto wait_chunk = [&](int c) {
+        mbar_wait_bounded(&s_full[c % SLOTS], static_cast<uint32_t>((c / SLOTS) & 1), s_abort,
+                          dev_status);
+    };
     wait_chunk(0);
     load_half(0, 0, wa, xa);
     for (int c = 0; c < nch; ++c) {
-        // every thread has consumed the registers it read from chunk c-1's slot
-        __syncthreads();
-        if (c + SLOTS - 1 < nch) issue(c + SLOTS - 1);
         load_half(c, 1, wb, xb);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[c % SLOTS]);
         fma_half(wa, xa);
         if (c + 1 < nch) {
             wait_chunk(c + 1);
@@ -588,20 +607,12 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
         }
         fma_half(wb, xb);
     }
-    if (*s_abort) {
-        // unwinding after a timed-out wait: let the copies still in flight land
-        __syncthreads();
-        if (tid == 0)
-            for (int c = nch - SLOTS; c < nch; ++c)
-                if (c >= 0) mbar_wait_drain(&s_full[c % SLOTS], static_cast<uint32_t>((c / SLOTS) & 1));
-        __syncthreads();
-    }
     if (e < E) {
         if (gate_bias) acc = __fadd_rn(acc, gate_bias[e]);
         s_lg[e] = acc;
         if (logits) logits[static_cast<size_t>(t) * E + e] = acc;
     }
-    __syncthreads();
+    consumer_sync(nc);
     if (fuse_topk && tid < 32) {
         float v[4];
 #pragma unroll
@@ -679,7 +690,8 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
                           int32_t *dev_status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     if (T <= SMALL_MAX_T && E <= SMALL_MAX_E && H <= SMALL_MAX_H) {
-        const int threads = std::max(64, static_cast<int>(ceil_div(E, 32)) * 32);
+        // consumers (one per expert, at least two warps) + the producer warp
+        const int threads = std::max(64, static_cast<int>(ceil_div(E, 32)) * 32) + 32;
         CUtensorMap tmw;
         if (!make_wg_map(&tmw, wg, H, E)) return cudaErrorInvalidValue;
         auto smem_for = [&](int slots) {
