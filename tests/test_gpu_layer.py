@@ -53,6 +53,8 @@ SMALL = [
              gamma_std=0.1),
     # E > 64: separate top-k and histogram launches
     Workload("mid-wideE", T=640, H=128, E=80, k=5, I=128),
+    # the limits: 1024 experts (most of them empty), 32 slots per token
+    Workload("max-Ek", T=200, H=128, E=1024, k=32, I=128, I_s=128, rmsnorm=True),
 ]
 
 

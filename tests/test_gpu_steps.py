@@ -28,6 +28,12 @@ def _cuda(d):
     Workload("g-rms", T=77, H=320, E=13, k=3, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-bias", T=100, H=256, E=64, k=8, I=128, rmsnorm=True, skew_s=1.2, skew_beta=1.0),
     Workload("g-wideE", T=40, H=192, E=160, k=6, I=128, rmsnorm=True),
+    # the small-batch router's ring depths: 12 slots with refills (T <= SMs),
+    # 5 slots (T > SMs), 3 slots (E=128 at the largest H), one chunk (H=64)
+    Workload("g-small-deep", T=100, H=1024, E=64, k=8, I=128, rmsnorm=True, gamma_std=0.1),
+    Workload("g-small-2cta", T=300, H=512, E=32, k=4, I=128, rmsnorm=True),
+    Workload("g-small-maxH", T=24, H=8192, E=128, k=8, I=128, rmsnorm=True, gamma_std=0.1),
+    Workload("g-small-1chunk", T=5, H=64, E=6, k=2, I=128),
     # more than 512 tokens: the tiled router (32 tokens x 64 experts per CTA)
     Workload("g-tiled", T=700, H=256, E=64, k=8, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-tiled-plain", T=1025, H=128, E=8, k=2, I=128),
