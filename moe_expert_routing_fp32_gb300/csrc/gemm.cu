@@ -433,8 +433,14 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
 // the even CTA's empty barrier once they have read it.  An index >= the
 // tile count ends every role's loop.
 constexpr int BM2 = 256;
-constexpr int STAGES2 = 6;
-constexpr int STAGE2_BYTES = 2 * A_BYTES;   // 128x64 A + 128x64 B per CTA
+// A stage holds two 64-wide k-slices of A and of B (4 TMA boxes, 64 KB per
+// CTA): the producer's per-stage round trip (wait for the slot, arm the
+// barrier, issue) limits how fast TMA fills shared memory, and measured on
+// GB300 one 64 KB stage streams ~120 GB/s per SM against ~100 GB/s for two
+// 32 KB stages (and ~74 GB/s for 16 KB stages).
+constexpr int KSUB2 = 2;                      // 64-wide k-slices per stage
+constexpr int STAGES2 = 3;
+constexpr int STAGE2_BYTES = KSUB2 * 2 * A_BYTES;   // per CTA: KSUB2 x (128x64 A + 128x64 B)
 constexpr int TMEM2_COLS = 512;
 constexpr int QD = 4;                        // tile-queue depth
 constexpr int Q_CONSUMERS = 10;              // see the queue protocol below
@@ -473,7 +479,7 @@ __device__ __forceinline__ Tile decode_tile_pair(const Params &p, int tile, cons
         t.row0 = s_off[g] + m_blk * BM2;
         t.row_end = s_off[g + 1];
         t.n_blk = nfast ? local % p.nt0 : local / mt;
-        t.kblocks = p.K0 / BK;
+        t.kblocks = p.K0 / (BK * KSUB2);
     } else {
         const int local = tile - total0;
         const int mt = (p.rows1 + BM2 - 1) / BM2;
@@ -483,7 +489,7 @@ __device__ __forceinline__ Tile decode_tile_pair(const Params &p, int tile, cons
         t.row0 = (nfast ? local / p.nt1 : local % mt) * BM2;
         t.row_end = p.rows1;
         t.n_blk = nfast ? local % p.nt1 : local / mt;
-        t.kblocks = p.K1 / BK;
+        t.kblocks = p.K1 / (BK * KSUB2);
     }
     return t;
 }
@@ -644,21 +650,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     }
                     armed[stage] = static_cast<int>(phase);
                     uint8_t *a_dst = smem + stage * STAGE2_BYTES;
-                    uint8_t *b_dst = a_dst + A_BYTES;
+                    uint8_t *b_dst = a_dst + KSUB2 * A_BYTES;
                     if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE2_BYTES);
                     const uint32_t fb = lead_full + 8u * static_cast<uint32_t>(stage);
-                    const int k0 = kb * BK;
                     int brow;
                     if (MODE == MODE_SWIGLU)
                         brow = (rank == 0 ? 0 : (t.seg == 0 ? p.half0 : p.half1)) + t.n_blk * 128;
                     else
                         brow = t.n_blk * BN + 128 * static_cast<int>(rank);
-                    if (t.seg == 0) {
-                        tma_load_2d_pair(a_dst, &p.tmA0, fb, k0, arow);
-                        tma_load_3d_pair(b_dst, &p.tmB0, fb, k0, brow, t.g);
-                    } else {
-                        tma_load_2d_pair(a_dst, &p.tmA1, fb, k0, arow);
-                        tma_load_2d_pair(b_dst, &p.tmB1, fb, k0, brow);
+#pragma unroll
+                    for (int sub = 0; sub < KSUB2; ++sub) {
+                        const int k0 = (kb * KSUB2 + sub) * BK;
+                        if (t.seg == 0) {
+                            tma_load_2d_pair(a_dst + sub * A_BYTES, &p.tmA0, fb, k0, arow);
+                            tma_load_3d_pair(b_dst + sub * A_BYTES, &p.tmB0, fb, k0, brow, t.g);
+                        } else {
+                            tma_load_2d_pair(a_dst + sub * A_BYTES, &p.tmA1, fb, k0, arow);
+                            tma_load_2d_pair(b_dst + sub * A_BYTES, &p.tmB1, fb, k0, brow);
+                        }
                     }
                     if (++stage == STAGES2) {
                         stage = 0;
@@ -699,13 +708,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + stage * STAGE2_BYTES);
-                    const uint32_t b_addr = a_addr + A_BYTES;
+                    const uint32_t b_addr = a_addr + KSUB2 * A_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        tc_mma_bf16_pair(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32),
-                                         sdesc_kmajor_sw128(b_addr + kk * 32), IDESC,
-                                         (kb | kk) != 0 ? 1u : 0u);
-                    }
+                    for (int sub = 0; sub < KSUB2; ++sub)
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint32_t off = sub * A_BYTES + kk * 32;
+                            tc_mma_bf16_pair(d_tmem, sdesc_kmajor_sw128(a_addr + off),
+                                             sdesc_kmajor_sw128(b_addr + off), IDESC,
+                                             (kb | sub | kk) != 0 ? 1u : 0u);
+                        }
                     issued = true;
                     tc_commit_pair_mc(&empty[stage], 0x3);
                     if (++stage == STAGES2) {
@@ -1090,7 +1102,9 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
                                cudaStream_t stream) {
     if (G > MAX_GROUPS) return cudaErrorInvalidValue;
     Params p{};
-    const bool pair = use_pair(n, G, seg1.rows);
+    // the pair kernel's stages hold 128 columns of K
+    const bool pair = use_pair(n, G, seg1.rows) && K % 128 == 0 &&
+                      (seg1.rows == 0 || seg1.K1 % 128 == 0);
     if (G > 0) {
         const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
         const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(2 * N),
@@ -1142,7 +1156,8 @@ cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, 
                               int32_t *dev_status, cudaStream_t stream) {
     if (G > MAX_GROUPS) return cudaErrorInvalidValue;
     const int BN = (N % 256 == 0 && (seg1.rows == 0 || seg1.N1 % 256 == 0)) ? 256 : 128;
-    const bool pair = BN == 256 && use_pair(n, G, seg1.rows);
+    const bool pair = BN == 256 && use_pair(n, G, seg1.rows) && K % 128 == 0 &&
+                      (seg1.rows == 0 || seg1.K1 % 128 == 0);
     const int box_b = pair ? 128 : BN;   // a pair CTA stages half of the 256 B rows
     Params p{};
     if (G > 0) {
