@@ -3,6 +3,7 @@
 // Host side only: argument checks, workspace carving and the launch sequence
 // of each operation.  Nothing here allocates, frees or synchronises.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <mutex>
@@ -310,7 +311,25 @@ moe_status_t layer_forward_impl(const moe_desc_t *desc, const moe_bf16_t *x,
     const int N = T * k;
     const int B = static_cast<int>(ceil_div(T, kChunkTokens));
 
+    // Each stage is also an NVTX range on the host thread (closed when the
+    // next stage starts or the call returns), so a timeline tool shows which
+    // launches belong to which step of the layer.
+    static const char *const kStageNames[MOE_NUM_STAGES] = {
+        "moe/router", "moe/route_scan_scatter", "moe/permute", "moe/gemm_w13_swiglu",
+        "moe/gemm_down", "moe/finalize"};
+    struct NvtxStage {
+        bool open = false;
+        void next(int i) {
+            if (open) nvtxRangePop();
+            open = i < MOE_NUM_STAGES;
+            if (open) nvtxRangePushA(kStageNames[i]);
+        }
+        ~NvtxStage() {
+            if (open) nvtxRangePop();
+        }
+    } nvtx;
     auto mark = [&](int i) -> cudaError_t {
+        nvtx.next(i);
         if (!stage_events) return cudaSuccess;
         return cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s);
     };
