@@ -184,3 +184,38 @@ def test_host_pipeline_matches_device_layer(out_f32):
                            ref.cpu().view(torch.int16 if not out_f32 else torch.int32))
     one = moe.layer_forward_host(desc, xs[0], _weights(g))       # a single tensor in, out
     assert torch.equal(one, outs[0])
+
+
+GRAPH_WL = [
+    WORKLOADS["tiny"],
+    Workload("mid-tiled", T=700, H=256, E=32, k=4, I=128, I_s=128, rmsnorm=True, gamma_std=0.1),
+    # 1024 rows per group: the CTA-pair GEMM with its per-launch tile counter
+    Workload("graph-pair", T=2048, H=256, E=4, k=2, I=256, I_s=256, rmsnorm=True),
+]
+
+
+@pytest.mark.parametrize("wl", GRAPH_WL, ids=lambda w: w.name)
+def test_layer_in_cuda_graph(wl):
+    """The layer captured in a CUDA graph and replayed (new inputs copied into
+    the captured buffers) gives the eager call's bytes: every launch, memset
+    and tile counter of the step lives on the captured stream."""
+    g = make_inputs(wl, 4, device=DEV)
+    desc = _desc(wl, out_f32=False)
+    w = _weights(g)
+    x = g["x"].clone()
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(moe.layer_workspace_size(desc), dtype=torch.uint8, device=DEV)
+    st = moe.new_status(DEV)
+    moe.layer_forward(desc, x, w, out=out, workspace=ws, status=st)     # warm-up outside
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        moe.layer_forward(desc, x, w, out=out, workspace=ws, status=st)
+    for seed in (5, 6):
+        x.copy_(make_inputs(wl, seed, device=DEV, only=["x"])["x"])
+        graph.replay()
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        ref = moe.layer_forward(desc, x, w)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
