@@ -77,10 +77,14 @@ struct Params {
     unsigned int *tile_counter;   // pair kernel: next tile to hand out (zeroed per launch)
     CUtensorMap tmO0;   // pair kernel: segment-0 output, 32-row x 64-byte boxes, 64-byte swizzle
     CUtensorMap tmO1;   // pair kernel: segment-1 output (bf16 or fp32)
+    // pair kernel, half tiles: the same tensors as 64-row boxes (A of both
+    // segments; B of the SwiGLU mode, whose half tiles take 64 gate + 64 up rows)
+    CUtensorMap tmA0h, tmA1h, tmB0h, tmB1h;
 };
 
 struct Tile {
     int seg, g, row0, row_end, n_blk, kblocks;
+    bool half;   // pair kernel: at most 128 rows left -> an M=128 pair MMA
 };
 
 template <int BN>
@@ -491,6 +495,7 @@ __device__ __forceinline__ Tile decode_tile_pair(const Params &p, int tile, cons
         t.n_blk = nfast ? local % p.nt1 : local / mt;
         t.kblocks = p.K1 / (BK * KSUB2);
     }
+    t.half = t.row_end - t.row0 <= 128;
     return t;
 }
 
@@ -641,7 +646,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 }
                 if (tile >= total) break;
                 const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0);
-                const int arow = t.row0 + 128 * static_cast<int>(rank);
+                // a half tile (M=128) takes 64 rows per CTA
+                const int arow = t.row0 + (t.half ? 64 : 128) * static_cast<int>(rank);
+                const uint32_t stage_tx =
+                    t.half ? 2u * KSUB2 * (A_BYTES / 2 + A_BYTES) : 2u * STAGE2_BYTES;
                 bool ok = true;
                 for (int kb = 0; kb < t.kblocks; ++kb) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1, s_abort, p.dev_status)) {
@@ -651,22 +659,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     armed[stage] = static_cast<int>(phase);
                     uint8_t *a_dst = smem + stage * STAGE2_BYTES;
                     uint8_t *b_dst = a_dst + KSUB2 * A_BYTES;
-                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE2_BYTES);
+                    if (leader) mbar_arrive_expect_tx(&full[stage], stage_tx);
                     const uint32_t fb = lead_full + 8u * static_cast<uint32_t>(stage);
+                    const int whalf = t.seg == 0 ? p.half0 : p.half1;
                     int brow;
                     if (MODE == MODE_SWIGLU)
-                        brow = (rank == 0 ? 0 : (t.seg == 0 ? p.half0 : p.half1)) + t.n_blk * 128;
+                        brow = (rank == 0 ? 0 : whalf) + t.n_blk * 128;
                     else
                         brow = t.n_blk * BN + 128 * static_cast<int>(rank);
 #pragma unroll
                     for (int sub = 0; sub < KSUB2; ++sub) {
                         const int k0 = (kb * KSUB2 + sub) * BK;
-                        if (t.seg == 0) {
-                            tma_load_2d_pair(a_dst + sub * A_BYTES, &p.tmA0, fb, k0, arow);
-                            tma_load_3d_pair(b_dst + sub * A_BYTES, &p.tmB0, fb, k0, brow, t.g);
+                        uint8_t *ad = a_dst + sub * A_BYTES;
+                        uint8_t *bd = b_dst + sub * A_BYTES;
+                        if (!t.half) {
+                            if (t.seg == 0) {
+                                tma_load_2d_pair(ad, &p.tmA0, fb, k0, arow);
+                                tma_load_3d_pair(bd, &p.tmB0, fb, k0, brow, t.g);
+                            } else {
+                                tma_load_2d_pair(ad, &p.tmA1, fb, k0, arow);
+                                tma_load_2d_pair(bd, &p.tmB1, fb, k0, brow);
+                            }
+                        } else if (MODE == MODE_SWIGLU) {
+                            // this CTA's half of B: 64 gate rows then the 64 matching up rows
+                            const int grow = t.n_blk * 128 + 64 * static_cast<int>(rank);
+                            if (t.seg == 0) {
+                                tma_load_2d_pair(ad, &p.tmA0h, fb, k0, arow);
+                                tma_load_3d_pair(bd, &p.tmB0h, fb, k0, grow, t.g);
+                                tma_load_3d_pair(bd + A_BYTES / 2, &p.tmB0h, fb, k0, whalf + grow,
+                                                 t.g);
+                            } else {
+                                tma_load_2d_pair(ad, &p.tmA1h, fb, k0, arow);
+                                tma_load_2d_pair(bd, &p.tmB1h, fb, k0, grow);
+                                tma_load_2d_pair(bd + A_BYTES / 2, &p.tmB1h, fb, k0, whalf + grow);
+                            }
                         } else {
-                            tma_load_2d_pair(a_dst + sub * A_BYTES, &p.tmA1, fb, k0, arow);
-                            tma_load_2d_pair(b_dst + sub * A_BYTES, &p.tmB1, fb, k0, brow);
+                            if (t.seg == 0) {
+                                tma_load_2d_pair(ad, &p.tmA0h, fb, k0, arow);
+                                tma_load_3d_pair(bd, &p.tmB0, fb, k0, brow, t.g);
+                            } else {
+                                tma_load_2d_pair(ad, &p.tmA1h, fb, k0, arow);
+                                tma_load_2d_pair(bd, &p.tmB1, fb, k0, brow);
+                            }
                         }
                     }
                     if (++stage == STAGES2) {
@@ -686,6 +720,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // ================= MMA issuer (even CTA only)
         if (lane == 0 && leader) {
             constexpr uint32_t IDESC = idesc_bf16_f32(BM2, BN);
+            // M=128 over the pair (64 rows per CTA) takes half the MMA time;
+            // its accumulator occupies 128 columns: rows in lanes 0-63 with
+            // columns 0-127 of N, the same rows again in lanes 64-127 with
+            // columns 128-255 (measured on GB300)
+            constexpr uint32_t IDESC_HALF = idesc_bf16_f32(BM2 / 2, BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -715,7 +754,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         for (int kk = 0; kk < BK / 16; ++kk) {
                             const uint32_t off = sub * A_BYTES + kk * 32;
                             tc_mma_bf16_pair(d_tmem, sdesc_kmajor_sw128(a_addr + off),
-                                             sdesc_kmajor_sw128(b_addr + off), IDESC,
+                                             sdesc_kmajor_sw128(b_addr + off), t.half ? IDESC_HALF : IDESC,
                                              (kb | sub | kk) != 0 ? 1u : 0u);
                         }
                     issued = true;
@@ -787,12 +826,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0);
             if (!mbar_wait_bounded(&tfull[acc], acc_phase, s_abort, p.dev_status)) break;
             tc_fence_after();
-            const int row = t.row0 + row_in_tile;
+            // full tile: this CTA's 128 rows, warp quadrant q = rows 32q..;
+            // half tile: this CTA's 64 rows, quadrant q = rows 32(q & 1).. of
+            // the columns' half q >> 1 (see the MMA's TMEM layout)
+            const int hq = q >> 1;
+            const int row = t.half ? t.row0 + 64 * static_cast<int>(rank) + 32 * (q & 1) + lane
+                                   : t.row0 + row_in_tile;
             const bool ok = row < t.row_end;
             // All 32 rows of this warp inside the group: the results leave
             // through TMA stores of whole 32-row boxes; otherwise (a group's
             // last block) each lane stores its own row if it is in range.
-            const int row_base = t.row0 + row_in_tile - lane;
+            const int row_base = row - lane;
             const bool boxed = row_base + 32 <= t.row_end;
             const CUtensorMap *omap = t.seg == 0 ? &p.tmO0 : &p.tmO1;
             const uint32_t taddr =
@@ -800,12 +844,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             if (MODE == MODE_SWIGLU) {
                 uint16_t *out = static_cast<uint16_t *>(t.seg == 0 ? p.out0 : p.out1);
                 const int64_t ldo = t.seg == 0 ? p.ldo0 : p.ldo1;
+                // gate in columns [0, w), up in [w, 2w): w = 128 (full) or 64 (half)
+                const int uoff = t.half ? 64 : 128;
+                const int col0 = t.n_blk * 128 + (t.half ? 64 * hq : 0);
 #pragma unroll 1
-                for (int c = 0; c < 128; c += 32) {
+                for (int c = 0; c < uoff; c += 32) {
                     float g[32], u[32];
                     __syncwarp();
                     tmem_ld32(taddr + c, g);
-                    tmem_ld32(taddr + 128 + c, u);
+                    tmem_ld32(taddr + uoff + c, u);
                     tmem_ld_wait();
                     uint32_t pk[16];
 #pragma unroll
@@ -816,10 +863,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         pk[i] = pack_bf16x2(a0, a1);
                     }
                     if (boxed) {
-                        emit_box(pk, omap, t.n_blk * 128 + c, row_base);
+                        emit_box(pk, omap, col0 + c, row_base);
                     } else if (ok) {
                         uint4 *dst = reinterpret_cast<uint4 *>(
-                            out + static_cast<int64_t>(row) * ldo + t.n_blk * 128 + c);
+                            out + static_cast<int64_t>(row) * ldo + col0 + c);
 #pragma unroll
                         for (int v = 0; v < 4; ++v)
                             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
@@ -830,13 +877,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 const bool f32 = t.seg == 1 && p.out1_f32;
                 void *outp = t.seg == 0 ? p.out0 : p.out1;
                 const int64_t ldo = t.seg == 0 ? p.ldo0 : p.ldo1;
+                const int ncol = t.half ? BN / 2 : BN;
+                const int col0 = t.n_blk * BN + (t.half ? (BN / 2) * hq : 0);
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = 0; c < ncol; c += 32) {
                     float v[32];
                     __syncwarp();
                     tmem_ld32(taddr + c, v);
                     tmem_ld_wait();
-                    const int col = t.n_blk * BN + c;
+                    const int col = col0 + c;
                     if (boxed) {
                         if (f32) {
                             uint32_t w[16];
@@ -1146,6 +1195,28 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
     p.dev_status = dev_status;
     if (pair) {
         if (!make_out_maps(p, N, seg1.N1)) return cudaErrorInvalidValue;
+        // 64-row boxes for half tiles: A, and B as 64 gate + 64 up rows
+        if (G > 0) {
+            const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
+            const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(2 * N),
+                                    static_cast<uint64_t>(G)};
+            if (!make_map(&p.tmA0h, A, 2, a0, 64) || !make_map(&p.tmB0h, W13, 3, b0, 64))
+                return cudaErrorInvalidValue;
+        }
+        if (seg1.rows > 0) {
+            const uint64_t a1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.rows)};
+            const uint64_t b1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(2 * seg1.N1)};
+            if (!make_map(&p.tmA1h, seg1.A, 2, a1, 64) || !make_map(&p.tmB1h, seg1.B, 2, b1, 64))
+                return cudaErrorInvalidValue;
+        }
+        if (G == 0) {
+            p.tmA0h = p.tmA1h;
+            p.tmB0h = p.tmB1h;
+        }
+        if (seg1.rows == 0) {
+            p.tmA1h = p.tmA0h;
+            p.tmB1h = p.tmB0h;
+        }
         return launch_pair<MODE_SWIGLU>(p, n, stream);
     }
     return launch<MODE_SWIGLU, 256>(p, n, stream);
@@ -1201,6 +1272,19 @@ cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, 
     p.dev_status = dev_status;
     if (pair) {
         if (!make_out_maps(p, N, seg1.N1)) return cudaErrorInvalidValue;
+        // 64-row A boxes for half tiles (B keeps its 128-row boxes)
+        if (G > 0) {
+            const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
+            if (!make_map(&p.tmA0h, A, 2, a0, 64)) return cudaErrorInvalidValue;
+        }
+        if (seg1.rows > 0) {
+            const uint64_t a1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.rows)};
+            if (!make_map(&p.tmA1h, seg1.A, 2, a1, 64)) return cudaErrorInvalidValue;
+        }
+        if (G == 0) p.tmA0h = p.tmA1h;
+        if (seg1.rows == 0) p.tmA1h = p.tmA0h;
+        p.tmB0h = p.tmB0;
+        p.tmB1h = p.tmB1;
         return launch_pair<MODE_STORE>(p, n, stream);
     }
     if (BN == 256) return launch<MODE_STORE, 256>(p, n, stream);
