@@ -65,7 +65,9 @@ enum {
     MOE_RMSNORM = 1u << 1,     /* RMSNorm before the gate */
     MOE_SHARED = 1u << 2,      /* add the shared expert */
     MOE_OUT_F32 = 1u << 3,     /* layer / finalize output in fp32 (else bf16) */
-    MOE_SHARED_F32 = 1u << 4   /* finalize: `shared` is fp32 (else bf16) */
+    MOE_SHARED_F32 = 1u << 4,  /* finalize: `shared` is fp32 (else bf16) */
+    MOE_GATE_SEQUENTIAL = 1u << 5  /* layer: the sequential fp32 gate for every T
+                                      (see moe_gate_tensor for the default) */
 };
 
 typedef struct {
@@ -76,7 +78,8 @@ typedef struct {
     int32_t I;          /* routed expert intermediate size */
     int32_t I_shared;   /* shared expert intermediate size (MOE_SHARED) */
     float rms_eps;      /* RMSNorm epsilon (MOE_RMSNORM) */
-    uint32_t flags;     /* MOE_RENORM | MOE_RMSNORM | MOE_SHARED | MOE_OUT_F32 */
+    uint32_t flags;     /* MOE_RENORM | MOE_RMSNORM | MOE_SHARED | MOE_OUT_F32 |
+                           MOE_GATE_SEQUENTIAL */
 } moe_desc_t;
 
 /* Human-readable name of a moe_status_t value. */
@@ -102,6 +105,29 @@ moe_status_t moe_rmsnorm_gate(const moe_bf16_t *x, const moe_bf16_t *gamma,
                               const float *wg, const float *gate_bias, int32_t T,
                               int32_t H, int32_t E, float eps, uint32_t flags,
                               moe_bf16_t *xn, float *logits, moe_stream_t stream);
+
+/*
+ * The same fp32 gate on the tensor cores ("消除gate计算冗余cast算子": an fp32
+ * linear layer).  Every fp32 weight is split exactly into three bf16 parts,
+ * wg = w1 + w2 + w3; each product of a bf16 xs value with a part is exact,
+ * the grouped GEMM accumulates the three partial dot products in fp32 and a
+ * combine kernel adds them, (p1 + p2) + p3, plus gate_bias[e].  The logits
+ * are fp32-accurate but summed in another order than moe_rmsnorm_gate's, so
+ * they may differ from it in the last bits (and a top-k decision between
+ * two logits that close may differ).  moe_layer_forward uses this gate for
+ * T > 512 unless MOE_GATE_SEQUENTIAL is set.
+ *   xs     [T, H] bf16 in: the (already normalised) hidden states
+ *   wg     [E, H] fp32 in;  gate_bias [E] fp32 or NULL
+ *   logits [T, E] fp32 out
+ * H % 128 == 0, E <= 1024.  T may be 0.  Workspace (the split weight and
+ * the partial logits): moe_gate_tensor_workspace_size() bytes, 256-byte
+ * aligned, caller-owned.  A device-side wait that runs out sets *dev_status
+ * (may be NULL).
+ */
+moe_status_t moe_gate_tensor_workspace_size(int32_t T, int32_t H, int32_t E, size_t *bytes);
+moe_status_t moe_gate_tensor(const moe_bf16_t *xs, const float *wg, const float *gate_bias,
+                             int32_t T, int32_t H, int32_t E, float *logits, void *workspace,
+                             size_t workspace_bytes, int32_t *dev_status, moe_stream_t stream);
 
 /*
  * GatingTopK ("MoE EP优化"): per token, the k largest logits (descending;
@@ -219,7 +245,10 @@ moe_status_t moe_finalize_routing(const moe_bf16_t *y_exp, const int32_t *expand
  *   w13_s [2I_s,H], w2_s [H,I_s] bf16 (MOE_SHARED, else NULL);
  *   out [T,H] bf16 (fp32 with MOE_OUT_F32).
  * The shared expert runs on the normalised rows with weight 1 and its output
- * enters the final sum in fp32.  Workspace: moe_layer_workspace_size() bytes,
+ * enters the final sum in fp32.  For T > 512 the gate is moe_gate_tensor's
+ * (fp32-accurate, another summation order) unless MOE_GATE_SEQUENTIAL is set;
+ * smaller batches always use the sequential gate of moe_rmsnorm_gate.
+ * Workspace: moe_layer_workspace_size() bytes,
  * 256-byte aligned; its contents are scratch.
  */
 moe_status_t moe_layer_workspace_size(const moe_desc_t *desc, size_t *bytes);

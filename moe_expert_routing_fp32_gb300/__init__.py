@@ -28,10 +28,11 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
                 3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_NO_DEVICE"}
 DEV_BAD_EXPERT_ID, DEV_TIMEOUT, DEV_BAD_OFFSETS, DEV_UNSORTED = 1, 2, 4, 8
-RENORM, RMSNORM, SHARED, OUT_F32, SHARED_F32 = 1, 2, 4, 8, 16
+RENORM, RMSNORM, SHARED, OUT_F32, SHARED_F32, GATE_SEQUENTIAL = 1, 2, 4, 8, 16, 32
 
 # every symbol include/moe.h declares
-EXPORTS = ("moe_status_string", "moe_rmsnorm_gate", "moe_gate_topk",
+EXPORTS = ("moe_status_string", "moe_rmsnorm_gate", "moe_gate_tensor_workspace_size",
+           "moe_gate_tensor", "moe_gate_topk",
            "moe_init_routing_workspace_size", "moe_init_routing", "moe_init_routing_noalloc",
            "moe_expert_tokens",
            "moe_grouped_mlp", "moe_finalize_routing", "moe_layer_workspace_size",
@@ -79,6 +80,8 @@ def lib() -> ctypes.CDLL:
             PSZ = ctypes.POINTER(ctypes.c_size_t)
             sigs = {
                 "moe_rmsnorm_gate": [P, P, P, P, I32, I32, I32, F, U32, P, P, P],
+                "moe_gate_tensor_workspace_size": [I32, I32, I32, PSZ],
+                "moe_gate_tensor": [P, P, P, I32, I32, I32, P, P, SZ, P, P],
                 "moe_gate_topk": [P, I32, I32, I32, U32, P, P, P],
                 "moe_init_routing_workspace_size": [I32, I32, I32, PSZ],
                 "moe_init_routing": [P, P, I32, I32, I32, I32, P, P, P, P, P, P, P, SZ, P, P],
@@ -190,6 +193,28 @@ def rmsnorm_gate(x, wg, gamma=None, gate_bias=None, eps=1e-6, rmsnorm=True):
     return xn, logits
 
 
+def gate_tensor_workspace_size(T, H, E) -> int:
+    n = ctypes.c_size_t(0)
+    _call("moe_gate_tensor_workspace_size", T, H, E, ctypes.byref(n))
+    return n.value
+
+
+def gate_tensor(xs, wg, gate_bias=None, workspace=None, status=None):
+    """The tensor-core fp32 gate on already-normalised rows -> logits fp32 [T, E]."""
+    _check(xs, torch.bfloat16, "xs")
+    _check(wg, torch.float32, "wg")
+    _check(gate_bias, torch.float32, "gate_bias")
+    T, H = xs.shape
+    E = wg.shape[0]
+    logits = torch.empty((T, E), dtype=torch.float32, device=xs.device)
+    need = gate_tensor_workspace_size(T, H, E)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=xs.device)
+    _call("moe_gate_tensor", _ptr(xs), _ptr(wg), _ptr(gate_bias), T, H, E, _ptr(logits),
+          _ptr(workspace), workspace.numel(), _ptr(status), _stream(xs.device))
+    return logits
+
+
 def gate_topk(logits, k, renorm=True):
     """-> (topk_idx int32 [T, k], topk_w fp32 [T, k])."""
     _check(logits, torch.float32, "logits")
@@ -274,9 +299,12 @@ def finalize_routing(y_exp, row_idx, topk_w, shared=None, out_f32=False):
 
 
 def make_desc(T, H, E, k, I, I_shared=0, rmsnorm=False, eps=1e-6, renorm=True,
-              out_f32=False) -> MoeDesc:
+              out_f32=False, gate_sequential=False) -> MoeDesc:
+    """``gate_sequential``: the sequential fp32 gate (moe_rmsnorm_gate's
+    logits, bit for bit) instead of the tensor-core gate for T > 512."""
     flags = (RENORM if renorm else 0) | (RMSNORM if rmsnorm else 0) | \
-        (SHARED if I_shared > 0 else 0) | (OUT_F32 if out_f32 else 0)
+        (SHARED if I_shared > 0 else 0) | (OUT_F32 if out_f32 else 0) | \
+        (GATE_SEQUENTIAL if gate_sequential else 0)
     return MoeDesc(T, H, E, k, I, I_shared, eps, flags)
 
 

@@ -14,6 +14,10 @@ namespace moe {
 constexpr int kChunkTokens = 32;
 // largest E for which the router fuses top-k and the routing histogram
 constexpr int kRouterExperts = 64;
+// batches of at most this many tokens use the one-CTA-per-token router (the
+// sequential fp32 gate); larger ones take the tensor-core gate unless the
+// caller asks for the sequential one
+constexpr int kGateSmallMaxT = 512;
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -29,6 +33,21 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
                           int32_t *topk_idx, float *topk_w, int32_t *hist,
                           int32_t *dev_status, cudaStream_t stream);
 
+// output columns of the tensor-core gate's GEMM: the three parts of every
+// expert's weights, padded to whole 128-column blocks
+inline int gate_tc_cols(int E) { return static_cast<int>(ceil_div(3 * E, 128) * 128); }
+// Tensor-core gate: RMSNorm alone (xn), the exact three-way bf16 split of
+// the gate weight (rows [0,E) part 1, [E,2E) part 2, [2E,3E) part 3, zero
+// rows up to NW), and the combine of the three partial logits (+ top-k and
+// the chunk histograms when E <= kRouterExperts and fuse_topk).
+cudaError_t launch_rmsnorm(const uint16_t *x, const uint16_t *gamma, int T, int H, float eps,
+                           uint16_t *xn, int32_t *dev_status, cudaStream_t stream);
+cudaError_t launch_gate_split(const float *wg, int E, int H, uint16_t *wsplit, int NW,
+                              cudaStream_t stream);
+cudaError_t launch_gate_combine(const float *parts, int NW, int T, int E, const float *gate_bias,
+                                float *logits, bool fuse_topk, int k, bool renorm,
+                                int32_t *topk_idx, float *topk_w, int32_t *hist,
+                                cudaStream_t stream);
 cudaError_t launch_topk(const float *logits, int T, int E, int k, bool renorm,
                         int32_t *topk_idx, float *topk_w, cudaStream_t stream);
 

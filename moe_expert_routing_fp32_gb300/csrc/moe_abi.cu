@@ -56,9 +56,50 @@ inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255);
 
 // Layout of the layer workspace (offsets in bytes, each 256-aligned).
 struct LayerWs {
-    size_t xn = 0, logits = 0, idx = 0, w = 0, hist = 0, counts = 0, offsets = 0, row_idx = 0,
-           expanded_x = 0, act = 0, y = 0, act_s = 0, y_s = 0, total = 0;
+    size_t xn = 0, logits = 0, wsplit = 0, parts = 0, idx = 0, w = 0, hist = 0, counts = 0,
+           offsets = 0, row_idx = 0, expanded_x = 0, act = 0, y = 0, act_s = 0, y_s = 0,
+           total = 0;
 };
+
+// The layer's gate runs on the tensor cores for batches above the small
+// router's range unless the caller asks for the sequential one.
+bool layer_gate_tc(const moe_desc_t &d) {
+    return d.T > kGateSmallMaxT && !(d.flags & MOE_GATE_SEQUENTIAL);
+}
+
+// Tensor-core gate scratch: the split weight [NW, H] bf16, then the partial
+// logits [T, NW] fp32 (NW = gate_tc_cols(E)).
+size_t gate_tc_split_bytes(int H, int E) {
+    return align256(static_cast<size_t>(gate_tc_cols(E)) * H * 2);
+}
+size_t gate_tc_parts_bytes(int T, int E) {
+    return align256(static_cast<size_t>(T) * gate_tc_cols(E) * 4);
+}
+
+// Split, GEMM, combine.  With fuse (E <= kRouterExperts) the combine also
+// takes the top-k and the chunk histograms; `logits` may then be NULL.
+cudaError_t launch_gate_tc(const uint16_t *xs, const float *wg, const float *gate_bias, int T,
+                           int H, int E, uint16_t *wsplit, float *parts, float *logits,
+                           bool fuse, int k, bool renorm, int32_t *idx, float *w,
+                           int32_t *hist, int32_t *dev_status, cudaStream_t s) {
+    const int NW = gate_tc_cols(E);
+    cudaError_t e = launch_gate_split(wg, E, H, wsplit, NW, s);
+    if (e != cudaSuccess) return e;
+    GemmSegment1 g;
+    g.A = xs;
+    g.B = wsplit;
+    g.rows = T;
+    g.K1 = H;
+    g.N1 = NW;
+    g.out = parts;
+    g.out_f32 = true;
+    // no grouped problem (G = 0): the offsets pointer only has to be readable
+    e = launch_gemm_store(nullptr, reinterpret_cast<const int32_t *>(wsplit), 0, 0, H, nullptr,
+                          NW, nullptr, g, dev_status, s);
+    if (e != cudaSuccess) return e;
+    return launch_gate_combine(parts, NW, T, E, gate_bias, logits, fuse, k, renorm, idx, w,
+                               hist, s);
+}
 
 LayerWs layer_layout(const moe_desc_t &d) {
     LayerWs L;
@@ -73,6 +114,10 @@ LayerWs layer_layout(const moe_desc_t &d) {
     };
     if (d.flags & MOE_RMSNORM) L.xn = take(T * H * 2);
     if (d.E > kRouterExperts) L.logits = take(T * E * 4);
+    if (layer_gate_tc(d)) {
+        L.wsplit = take(gate_tc_split_bytes(d.H, d.E));
+        L.parts = take(gate_tc_parts_bytes(d.T, d.E));
+    }
     L.idx = take(N * 4);
     L.w = take(N * 4);
     L.hist = take(B * E * 4);
@@ -146,6 +191,34 @@ moe_status_t moe_rmsnorm_gate(const moe_bf16_t *x, const moe_bf16_t *gamma, cons
     MOE_TRY(launch_router(x, rms ? gamma : nullptr, wg, gate_bias, T, H, E, eps, rms,
                           rms ? xn : nullptr, logits, false, 1, false, nullptr, nullptr, nullptr,
                           nullptr, reinterpret_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+moe_status_t moe_gate_tensor_workspace_size(int32_t T, int32_t H, int32_t E, size_t *bytes) {
+    if (!bytes || T < 0 || H <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+    if (H % 128 != 0 || E > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+    *bytes = gate_tc_split_bytes(H, E) + gate_tc_parts_bytes(T, E);
+    return MOE_OK;
+}
+
+moe_status_t moe_gate_tensor(const moe_bf16_t *xs, const float *wg, const float *gate_bias,
+                             int32_t T, int32_t H, int32_t E, float *logits, void *workspace,
+                             size_t workspace_bytes, int32_t *dev_status, moe_stream_t stream) {
+    size_t need = 0;
+    const moe_status_t st = moe_gate_tensor_workspace_size(T, H, E, &need);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    if (!xs || !wg || !logits) return MOE_ERR_INVALID_ARG;
+    if (!a16(xs) || !a16(wg)) return MOE_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (!current_device_ok()) return MOE_ERR_NO_DEVICE;
+    if (!tensor_maps_available()) return MOE_ERR_CUDA;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    MOE_TRY(launch_gate_tc(xs, wg, gate_bias, T, H, E, reinterpret_cast<uint16_t *>(ws),
+                           reinterpret_cast<float *>(ws + gate_tc_split_bytes(H, E)), logits,
+                           false, 1, false, nullptr, nullptr, nullptr, dev_status,
+                           reinterpret_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
 
@@ -337,8 +410,17 @@ moe_status_t layer_forward_impl(const moe_desc_t *desc, const moe_bf16_t *x,
     // 1. RMSNorm + gate (+ top-k + routing histogram when E <= 64)
     MOE_TRY(mark(0));
     const bool fuse = E <= kRouterExperts;
-    MOE_TRY(launch_router(x, rms ? gamma : nullptr, wg, gate_bias, T, H, E, d.rms_eps, rms, xn,
-                          logits, fuse, k, renorm, idx, w, fuse ? hist : nullptr, dev_status, s));
+    if (layer_gate_tc(d)) {
+        // RMSNorm alone, then the gate as a tensor-core GEMM on the normalised rows
+        if (rms) MOE_TRY(launch_rmsnorm(x, gamma, T, H, d.rms_eps, xn, dev_status, s));
+        MOE_TRY(launch_gate_tc(xs, wg, gate_bias, T, H, E, static_cast<uint16_t *>(at(L.wsplit)),
+                               static_cast<float *>(at(L.parts)), logits, fuse, k, renorm, idx, w,
+                               fuse ? hist : nullptr, dev_status, s));
+    } else {
+        MOE_TRY(launch_router(x, rms ? gamma : nullptr, wg, gate_bias, T, H, E, d.rms_eps, rms,
+                              xn, logits, fuse, k, renorm, idx, w, fuse ? hist : nullptr,
+                              dev_status, s));
+    }
     if (!fuse) {
         MOE_TRY(launch_topk(logits, T, E, k, renorm, idx, w, s));
         MOE_TRY(launch_route_hist(idx, T, k, E, hist, dev_status, s));

@@ -131,6 +131,9 @@ __device__ __forceinline__ float slot_weight(const float (&v)[NV], int k, bool r
     return ej / den;
 }
 
+// GATE = false: RMSNorm only (phases 1 and the xn write of phase 2), for the
+// tensor-core gate, which reads xn back.
+template <bool GATE>
 __global__ void __launch_bounds__(RT_THREADS)
 router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
               const float *__restrict__ wg, const float *__restrict__ gate_bias, int T, int H,
@@ -272,6 +275,7 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
         const bool okt = lt < ntok;
         const uint16_t *xsrc = okt ? x + static_cast<size_t>(tok0 + lt) * H + h0 + 8 * lg4 : x;
         cp_async16(xr_ring + st * XR_STAGE + lt * (G_HC * 2) + lg4 * 16, xsrc, okt ? 16 : 0);
+        if (!GATE) return;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const int e = p * 16 + (tid >> 3);
@@ -338,6 +342,7 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
     for (int c = 0; c < nslices; ++c) {
         if (c + G_STAGES - 1 < nslices) issue(c + G_STAGES - 1);
         cp_async_commit();
+        if (GATE) {
         const float *xb = xs + (c & 1) * RT_TOK * G_LD;
         const float *wb = reinterpret_cast<const float *>(wg_ring + (c % G_STAGES) * WG_STAGE);
 #pragma unroll
@@ -359,12 +364,14 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
                     acc[i][j] = __fmaf_rn(xv[i].w, wv[j].w, acc[i][j]);
                 }
         }
+        }
         cp_async_wait<G_STAGES - 2>();
         __syncthreads();
         if (c + 1 < nslices) convert(c + 1, (c + 1) & 1);
         __syncthreads();
     }
 
+    if (!GATE) return;
     // ---------------- phase 3: bias, logits out, top-k, histogram
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -425,7 +432,7 @@ constexpr int SM_SMEM_CAP = 220 * 1024;
 // bytes of one 32-column half of a ring slot: E rows of 128 bytes, rounded to
 // whole 1 KB swizzle atoms
 __host__ __device__ inline int sm_half_bytes(int E) { return ((E + 7) / 8) * 1024; }
-constexpr int SMALL_MAX_T = 512;
+constexpr int SMALL_MAX_T = kGateSmallMaxT;
 constexpr int SMALL_MAX_E = 128;
 constexpr int SMALL_MAX_H = 8192;
 
@@ -655,6 +662,93 @@ topk_kernel(const float *__restrict__ logits, int T, int E, int k, int renorm,
     }
 }
 
+// ---------------------------------------------------------------- tensor-core gate
+// The gate on the tensor cores at fp32 accuracy: each fp32 weight splits
+// exactly into three bf16 parts, w = w1 + w2 + w3 (w1 = bf16(w), w2 =
+// bf16(w - w1), w3 = bf16(w - w1 - w2); the two differences are exact in
+// fp32 and the last part holds the remaining bits), and every product of a
+// bf16 xn value with a part is exact.  The grouped GEMM computes the three
+// partial dot products as separate output columns (fp32 accumulation in the
+// tensor core) and the combine kernel adds them: logit = (p1 + p2) + p3.
+// The sum is fp32-accurate but not in the sequential order of the plain
+// definition, so a logit can differ from it in the last bits.
+__global__ void __launch_bounds__(256)
+gate_split_kernel(const float *__restrict__ wg, int E, int H, uint16_t *__restrict__ ws,
+                  int NW) {
+    const int64_t n = static_cast<int64_t>(NW) * H;
+    for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n; i += gridDim.x * 256ll) {
+        const int row = static_cast<int>(i / H), h = static_cast<int>(i % H);
+        const int part = row / E, e = row % E;
+        uint16_t out = 0;
+        if (part < 3) {
+            const float w = wg[static_cast<size_t>(e) * H + h];
+            const uint16_t b1 = float_to_bf16_bits(w);
+            const float r1 = __fsub_rn(w, bf16_bits_to_float(b1));
+            const uint16_t b2 = float_to_bf16_bits(r1);
+            const float r2 = __fsub_rn(r1, bf16_bits_to_float(b2));
+            out = part == 0 ? b1 : part == 1 ? b2 : float_to_bf16_bits(r2);
+        }
+        ws[i] = out;
+    }
+}
+
+// One CTA per 32-token chunk, a warp per token: logit = (p1 + p2) + p3
+// (+ bias); with E <= 64 also the top-k / softmax and the chunk's routing
+// histogram (as the router's phase 3).
+__global__ void __launch_bounds__(128)
+gate_combine_kernel(const float *__restrict__ parts, int NW, int T, int E,
+                    const float *__restrict__ gate_bias, float *__restrict__ logits,
+                    int fuse_topk, int k, int renorm, int32_t *__restrict__ topk_idx,
+                    float *__restrict__ topk_w, int32_t *__restrict__ hist) {
+    __shared__ int s_cnt[RT_EXP];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tok0 = blockIdx.x * RT_TOK;
+    const int ntok = min(RT_TOK, T - tok0);
+    if (fuse_topk)
+        for (int e = threadIdx.x; e < RT_EXP; e += 128) s_cnt[e] = 0;
+    __syncthreads();
+    for (int tl = warp; tl < ntok; tl += 4) {
+        const int t = tok0 + tl;
+        const float *pr = parts + static_cast<size_t>(t) * NW;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            if (e < E) {
+                float v = __fadd_rn(__fadd_rn(pr[e], pr[E + e]), pr[2 * E + e]);
+                if (gate_bias) v = __fadd_rn(v, gate_bias[e]);
+                if (logits) logits[static_cast<size_t>(t) * E + e] = v;
+            }
+        }
+        if (fuse_topk) {
+            float v[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int e = lane + 32 * i;
+                float val = -INFINITY;
+                if (e < E) {
+                    val = __fadd_rn(__fadd_rn(pr[e], pr[E + e]), pr[2 * E + e]);
+                    if (gate_bias) val = __fadd_rn(val, gate_bias[e]);
+                }
+                v[i] = val;
+            }
+            int sel_e;
+            float sel_v;
+            warp_topk<2>(v, k, &sel_e, &sel_v);
+            const float w = slot_weight<2>(v, k, renorm != 0, sel_v);
+            if (lane < k) {
+                const size_t a = static_cast<size_t>(t) * k + lane;
+                topk_idx[a] = sel_e;
+                topk_w[a] = w;
+                atomicAdd(&s_cnt[sel_e], 1);
+            }
+        }
+    }
+    if (fuse_topk && hist) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += 128)
+            hist[static_cast<size_t>(blockIdx.x) * E + e] = s_cnt[e];
+    }
+}
+
 }  // namespace
 
 // The gate weight [E, H] fp32 as 32-column x E-row boxes, 128-byte swizzle.
@@ -729,7 +823,7 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(router_kernel,
+        cudaError_t e = cudaFuncSetAttribute(router_kernel<true>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SMEM_TOTAL);
         if (e != cudaSuccess) return e;
@@ -737,7 +831,7 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
     }
     dim3 grid(static_cast<unsigned>(ceil_div(T, RT_TOK)),
               static_cast<unsigned>(ceil_div(E, RT_EXP)));
-    router_kernel<<<grid, RT_THREADS, SMEM_TOTAL, stream>>>(
+    router_kernel<true><<<grid, RT_THREADS, SMEM_TOTAL, stream>>>(
         x, gamma, wg, gate_bias, T, H, E, eps, rmsnorm ? 1 : 0, xn, logits,
         fuse_topk ? 1 : 0, k, renorm ? 1 : 0, topk_idx, topk_w, hist, dev_status);
     return cudaGetLastError();
@@ -762,6 +856,46 @@ cudaError_t launch_topk(const float *logits, int T, int E, int k, bool renorm,
         topk_kernel<16><<<blocks, threads, 0, stream>>>(logits, T, E, k, rn, topk_idx, topk_w);
     else
         topk_kernel<32><<<blocks, threads, 0, stream>>>(logits, T, E, k, rn, topk_idx, topk_w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const uint16_t *x, const uint16_t *gamma, int T, int H, float eps,
+                           uint16_t *xn, int32_t *dev_status, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(router_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_TOTAL);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    router_kernel<false><<<static_cast<unsigned>(ceil_div(T, RT_TOK)), RT_THREADS, SMEM_TOTAL,
+                           stream>>>(x, gamma, nullptr, nullptr, T, H, RT_EXP, eps, 1, xn, nullptr,
+                                     0, 1, 0, nullptr, nullptr, nullptr, dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gate_split(const float *wg, int E, int H, uint16_t *wsplit, int NW,
+                              cudaStream_t stream) {
+    const int64_t n = static_cast<int64_t>(NW) * H;
+    const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(n, 256),
+                                                                             num_sms() * 8)));
+    gate_split_kernel<<<blocks, 256, 0, stream>>>(wg, E, H, wsplit, NW);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gate_combine(const float *parts, int NW, int T, int E, const float *gate_bias,
+                                float *logits, bool fuse_topk, int k, bool renorm,
+                                int32_t *topk_idx, float *topk_w, int32_t *hist,
+                                cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const bool fuse = fuse_topk && E <= RT_EXP;
+    gate_combine_kernel<<<static_cast<unsigned>(ceil_div(T, RT_TOK)), 128, 0, stream>>>(
+        parts, NW, T, E, gate_bias, logits, fuse ? 1 : 0, k, renorm ? 1 : 0, topk_idx, topk_w,
+        fuse ? hist : nullptr);
     return cudaGetLastError();
 }
 

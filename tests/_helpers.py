@@ -75,3 +75,72 @@ def check_bf16_close(gpu_bits: np.ndarray, ref_bits: np.ndarray, max_flip_frac: 
     flips = float(np.mean(d > 0)) if d.size else 0.0
     assert flips <= max_flip_frac, f"{what}: {flips:.2e} of values flipped one ulp"
     return flips
+
+
+# ------------------------------------------------ the tensor-core gate
+# The tensor-core gate (moe_gate_tensor, the layer's gate for T > 512) adds
+# the same exact products as the oracle's sequential fp32 dot product in
+# another order, so the two logits differ by rounding only.  Bound on that
+# difference per logit, with S = sum_h |xs_h * wg_eh| and u = 2^-24:
+#   oracle, one rounding per fused multiply-add:      H * u * S
+#   tensor core, per K=16 step a block sum and one accumulation, each
+#   rounded at most one fp32 ulp (2u, truncation allowed): (H/16 + 16) * 2u * S
+#   (the second and third weight parts carry 2^-8 and 2^-16 of the first's
+#   magnitude: a factor 1.01 covers them)
+#   the combine (p1 + p2) + p3 + bias, three roundings:  4u * |logit|
+# The root-mean-square difference over many logits, with independent
+# rounding errors, is far smaller: at most 2 sqrt(H) u times the RMS of S.
+# A gate that drops the second weight part misses by ~2^-9 / sqrt(3) of the
+# logit's spread and fails that; the exact split itself (w = w1 + w2 + w3)
+# is checked on its own.
+def gate_tc_bound(xs_bits, wg, lg_ref):
+    """-> (per-logit bound [T, E], rms bound) on |tensor-core - oracle| logits."""
+    xs = bf16_to_f64(xs_bits)
+    w = np.asarray(wg, dtype=np.float64)
+    H = xs.shape[1]
+    S = np.abs(xs) @ np.abs(w).T
+    u = 2.0 ** -24
+    per = ((H / 16 + 16) * 2 * u * 1.01 + H * u) * S + 4 * u * np.abs(lg_ref.astype(np.float64))
+    rms = 2 * np.sqrt(H) * u * float(np.sqrt(np.mean(S * S))) if S.size else 0.0
+    return per, rms
+
+
+def check_gate_tc_logits(lg_gpu, lg_ref, per, rms_bound, what=""):
+    d = np.abs(lg_gpu.astype(np.float64) - lg_ref.astype(np.float64))
+    bad = d > per
+    assert not bad.any(), (f"{what}: {int(bad.sum())} logits beyond the fp32 rounding bound, "
+                           f"worst excess {float((d - per).max())}")
+    rms = float(np.sqrt(np.mean(d * d))) if d.size else 0.0
+    assert rms <= rms_bound, f"{what}: RMS logit difference {rms} > {rms_bound}"
+    return float(d.max()) if d.size else 0.0, rms
+
+
+def routing_flips(idx_gpu, idx_ref, lg_ref, per):
+    """Tokens whose set of chosen experts differs from the oracle's.  Each
+    such choice must be a valid top-k of the oracle's logits once every logit
+    may move by its rounding bound (an ambiguous near-tie), and the slot
+    order of every token must be consistent with the oracle's logits up to
+    the same bound.  Returns the flipped tokens (sorted)."""
+    idx_gpu = np.asarray(idx_gpu)
+    idx_ref = np.asarray(idx_ref)
+    T, k = idx_ref.shape
+    E = lg_ref.shape[1]
+    lg = lg_ref.astype(np.float64)
+    assert idx_gpu.shape == (T, k)
+    assert ((idx_gpu >= 0) & (idx_gpu < E)).all(), "expert id out of range"
+    srt = np.sort(idx_gpu, axis=1)
+    assert (np.diff(srt, axis=1) > 0).all(), "an expert chosen twice"
+    flipped = np.nonzero((srt != np.sort(idx_ref, axis=1)).any(axis=1))[0]
+    reordered = np.nonzero((idx_gpu != idx_ref).any(axis=1))[0]
+    for t in reordered:
+        g = idx_gpu[t]
+        hi = lg[t] + per[t]
+        lo = lg[t] - per[t]
+        # slot order: descending up to the bound
+        assert (hi[g[:-1]] >= lo[g[1:]]).all(), f"token {t}: slot order {g} not descending"
+        # every chosen expert at least as large as every other, up to the bound
+        rest = np.ones(E, dtype=bool)
+        rest[g] = False
+        if rest.any():
+            assert hi[g].min() >= lo[rest].max(), f"token {t}: {g} is not a top-{k}"
+    return flipped

@@ -8,6 +8,14 @@ top-k and routing for every token (bit-exact comparison of the step entry
 points on the same inputs) and the layer output for a sample of tokens.
 Inputs of the full-size workloads are drawn on the GPU by the seeded
 generator and copied to the host for the oracle.
+
+Above 512 tokens the layer's gate is the tensor-core one (moe_gate_tensor):
+fp32-accurate logits in another summation order than the oracle's.  Its
+routing is compared with the oracle's through the step entry points; a
+token whose oracle choice lies within the fp32 rounding bound of a tie may
+take another valid set of experts (checked for validity) and is then left
+out of the output comparison.  The same layer with MOE_GATE_SEQUENTIAL
+(the oracle's summation order) is compared on every token.
 """
 import numpy as np
 import pytest
@@ -16,7 +24,8 @@ import torch
 import moe_expert_routing_fp32_gb300 as moe
 import oracle
 from moe_inputs import WORKLOADS, Workload, make_inputs
-from tests._helpers import check_out, t2f64, u16
+from tests._helpers import (check_gate_tc_logits, check_out, gate_tc_bound, routing_flips, t2f64,
+                            u16)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -27,17 +36,45 @@ def _weights(g):
                             gate_bias=g["gate_bias"], w13_s=g["w13_s"], w2_s=g["w2_s"])
 
 
-def _desc(wl, T=None, out_f32=True):
+def _desc(wl, T=None, out_f32=True, seq=False):
     return moe.make_desc(wl.T if T is None else T, wl.H, wl.E, wl.k, wl.I, wl.I_s,
-                         rmsnorm=wl.rmsnorm, eps=wl.eps, renorm=wl.renorm, out_f32=out_f32)
+                         rmsnorm=wl.rmsnorm, eps=wl.eps, renorm=wl.renorm, out_f32=out_f32,
+                         gate_sequential=seq)
 
 
-def _run_layer(wl, g, out_f32, T=None):
+def _run_layer(wl, g, out_f32, T=None, seq=False):
     st = moe.new_status(DEV)
-    out = moe.layer_forward(_desc(wl, T, out_f32), g["x"], _weights(g), status=st)
+    out = moe.layer_forward(_desc(wl, T, out_f32, seq), g["x"], _weights(g), status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0, f"device status {int(st.item())}"
     return out
+
+
+def _tc_flips(wl, g, cpu, xs_ref=None, lg_ref=None, ridx=None):
+    """Tokens for which the tensor-core gate (the layer's gate for T > 512)
+    picks another valid set of experts than the oracle; empty for T <= 512.
+    Also checks its logits against the oracle's within the rounding bound."""
+    if wl.T <= 512:
+        return np.zeros(0, dtype=np.int64)
+    if xs_ref is None:
+        xs_ref = oracle.rmsnorm(cpu["x"], cpu["gamma"], wl.eps) if wl.rmsnorm else u16(cpu["x"])
+    if lg_ref is None:
+        lg_ref = oracle.gate_logits(xs_ref, cpu["wg"], cpu["gate_bias"])
+    if ridx is None:
+        ridx, _ = oracle.topk_softmax(lg_ref, wl.k, wl.renorm)
+    xs = g["x"]
+    if wl.rmsnorm:
+        xs, _ = moe.rmsnorm_gate(g["x"], g["wg"], g["gamma"], g["gate_bias"], wl.eps)
+    lg = moe.gate_tensor(xs, g["wg"], g["gate_bias"])
+    idx, _ = moe.gate_topk(lg, wl.k, wl.renorm)
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(xs), xs_ref)
+    per, rms_b = gate_tc_bound(xs_ref, cpu["wg"], lg_ref)
+    check_gate_tc_logits(lg.cpu().numpy(), lg_ref, per, rms_b, wl.name)
+    flips = routing_flips(idx.cpu().numpy(), ridx, lg_ref, per)
+    if len(flips):
+        print(f"{wl.name}: {len(flips)} tokens take another valid expert set")
+    return flips
 
 
 SMALL = [
@@ -65,7 +102,11 @@ def test_layer_small_all_tokens(wl, out_f32):
     g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
     out = _run_layer(wl, g, out_f32)
     ref, ridx, rw = oracle.layer_tokens(d, wl)
-    check_out(t2f64(out), ref, bf16_out=not out_f32, what=wl.name)
+    keep = np.setdiff1d(np.arange(wl.T), _tc_flips(wl, g, d, ridx=ridx))
+    check_out(t2f64(out)[keep], ref[keep], bf16_out=not out_f32, what=wl.name)
+    if wl.T > 512:
+        seq = _run_layer(wl, g, out_f32, seq=True)
+        check_out(t2f64(seq), ref, bf16_out=not out_f32, what=f"{wl.name} sequential gate")
 
 
 def test_layer_deterministic_and_workspace_reuse():
@@ -130,17 +171,25 @@ def test_layer_full_size(name):
         print(f"{name}: {int((counts == 0).sum())} idle experts, top share "
               f"{counts.max() / counts.sum():.4f}")
 
-    # layer output on sampled tokens (fp32 mode strict, bf16 mode + half ulp)
+    # the tensor-core gate's routing (the layer's for T > 512)
+    flips = _tc_flips(wl, g, cpu, xs_ref, lg_ref, ridx)
+
+    # layer output on sampled tokens (fp32 mode strict, bf16 mode + half ulp),
+    # with the layer's own gate and with the sequential one
     tok = _sample_tokens(wl.T, 48, 7)
     # include tokens routed to the busiest expert
     busiest = int(np.argmax(counts))
     hot = np.nonzero((ridx == busiest).any(axis=1))[0][:4]
     tok = np.unique(np.concatenate([tok, hot]).astype(np.int32))
     ref, _, _ = oracle.layer_tokens(cpu, wl, tok)
-    for out_f32 in (True, False):
-        out = _run_layer(wl, g, out_f32)
-        got = t2f64(out[torch.from_numpy(tok).long().to(DEV)])
-        check_out(got, ref, bf16_out=not out_f32, what=f"{name} f32={out_f32}")
+    keep = ~np.isin(tok, flips)
+    for seq in ((False, True) if wl.T > 512 else (False,)):
+        for out_f32 in (True, False):
+            out = _run_layer(wl, g, out_f32, seq=seq)
+            got = t2f64(out[torch.from_numpy(tok).long().to(DEV)])
+            sel = np.ones(len(tok), dtype=bool) if seq else keep
+            check_out(got[sel], ref[sel], bf16_out=not out_f32,
+                      what=f"{name} f32={out_f32} sequential={seq}")
 
 
 def test_shared_expert_on_second_stream_matches():
