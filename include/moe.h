@@ -100,6 +100,9 @@ const char *moe_status_string(int status);
  *          gate_bias[e].  These are bit-identical to the same steps done
  *          sequentially on any IEEE fp32 machine.
  * flags: MOE_RMSNORM.  T may be 0.
+ * With wg and logits both NULL (and MOE_RMSNORM) only xn is computed, by the
+ * RMSNorm pass the layer runs ahead of the tensor-core gate (H % 128 == 0);
+ * same bits as above.
  */
 moe_status_t moe_rmsnorm_gate(const moe_bf16_t *x, const moe_bf16_t *gamma,
                               const float *wg, const float *gate_bias, int32_t T,

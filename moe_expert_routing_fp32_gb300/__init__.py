@@ -179,12 +179,18 @@ def new_status(device) -> torch.Tensor:
 
 # ----------------------------------------------------------------- operations
 def rmsnorm_gate(x, wg, gamma=None, gate_bias=None, eps=1e-6, rmsnorm=True):
-    """-> (xn or None, logits fp32 [T, E])."""
+    """-> (xn or None, logits fp32 [T, E]); with wg None: (xn, None) from the
+    RMSNorm-only pass."""
     _check(x, torch.bfloat16, "x")
     _check(wg, torch.float32, "wg")
     _check(gamma, torch.bfloat16, "gamma")
     _check(gate_bias, torch.float32, "gate_bias")
     T, H = x.shape
+    if wg is None:
+        xn = torch.empty_like(x)
+        _call("moe_rmsnorm_gate", _ptr(x), _ptr(gamma), None, None, T, H, 1, float(eps),
+              RMSNORM, _ptr(xn), None, _stream(x.device))
+        return xn, None
     E = wg.shape[0]
     logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
     xn = torch.empty_like(x) if rmsnorm else None

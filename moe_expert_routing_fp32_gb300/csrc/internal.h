@@ -36,10 +36,11 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
 // output columns of the tensor-core gate's GEMM: the three parts of every
 // expert's weights, padded to whole 128-column blocks
 inline int gate_tc_cols(int E) { return static_cast<int>(ceil_div(3 * E, 128) * 128); }
-// Tensor-core gate: RMSNorm alone (xn), the exact three-way bf16 split of
-// the gate weight (rows [0,E) part 1, [E,2E) part 2, [2E,3E) part 3, zero
-// rows up to NW), and the combine of the three partial logits (+ top-k and
-// the chunk histograms when E <= kRouterExperts and fuse_topk).
+// Tensor-core gate: RMSNorm alone (xn; H % 128 == 0), the exact three-way
+// bf16 split of the gate weight (rows [0,E) part 1, [E,2E) part 2, [2E,3E)
+// part 3, zero rows up to NW), and the combine of the three partial logits:
+// with fuse_topk and E <= kRouterExperts the top-k and the chunk histograms
+// (logits not written), else the logits.
 cudaError_t launch_rmsnorm(const uint16_t *x, const uint16_t *gamma, int T, int H, float eps,
                            uint16_t *xn, int32_t *dev_status, cudaStream_t stream);
 cudaError_t launch_gate_split(const float *wg, int E, int H, uint16_t *wsplit, int NW,

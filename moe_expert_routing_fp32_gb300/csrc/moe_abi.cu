@@ -184,6 +184,16 @@ moe_status_t moe_rmsnorm_gate(const moe_bf16_t *x, const moe_bf16_t *gamma, cons
     if (T < 0 || H <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
     if (H % 64 != 0 || E > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (T == 0) return MOE_OK;
+    if (!wg && !logits) {
+        // RMSNorm alone (the pass ahead of the tensor-core gate)
+        if (!rms || !x || !xn || !a16(x) || !a16(xn) || (gamma && !a16(gamma)) || !(eps >= 0))
+            return MOE_ERR_INVALID_ARG;
+        if (H % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+        if (!current_device_ok()) return MOE_ERR_NO_DEVICE;
+        MOE_TRY(launch_rmsnorm(x, gamma, T, H, eps, xn, nullptr,
+                               reinterpret_cast<cudaStream_t>(stream)));
+        return MOE_OK;
+    }
     if (!x || !wg || !logits || (rms && !xn)) return MOE_ERR_INVALID_ARG;
     if (!a16(x) || !a16(wg) || (rms && !a16(xn)) || (gamma && !a16(gamma)) || (rms && !(eps >= 0)))
         return MOE_ERR_INVALID_ARG;

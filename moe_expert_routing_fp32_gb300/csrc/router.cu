@@ -23,6 +23,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -131,9 +132,6 @@ __device__ __forceinline__ float slot_weight(const float (&v)[NV], int k, bool r
     return ej / den;
 }
 
-// GATE = false: RMSNorm only (phases 1 and the xn write of phase 2), for the
-// tensor-core gate, which reads xn back.
-template <bool GATE>
 __global__ void __launch_bounds__(RT_THREADS)
 router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
               const float *__restrict__ wg, const float *__restrict__ gate_bias, int T, int H,
@@ -275,7 +273,6 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
         const bool okt = lt < ntok;
         const uint16_t *xsrc = okt ? x + static_cast<size_t>(tok0 + lt) * H + h0 + 8 * lg4 : x;
         cp_async16(xr_ring + st * XR_STAGE + lt * (G_HC * 2) + lg4 * 16, xsrc, okt ? 16 : 0);
-        if (!GATE) return;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const int e = p * 16 + (tid >> 3);
@@ -342,7 +339,6 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
     for (int c = 0; c < nslices; ++c) {
         if (c + G_STAGES - 1 < nslices) issue(c + G_STAGES - 1);
         cp_async_commit();
-        if (GATE) {
         const float *xb = xs + (c & 1) * RT_TOK * G_LD;
         const float *wb = reinterpret_cast<const float *>(wg_ring + (c % G_STAGES) * WG_STAGE);
 #pragma unroll
@@ -364,14 +360,12 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
                     acc[i][j] = __fmaf_rn(xv[i].w, wv[j].w, acc[i][j]);
                 }
         }
-        }
         cp_async_wait<G_STAGES - 2>();
         __syncthreads();
         if (c + 1 < nslices) convert(c + 1, (c + 1) & 1);
         __syncthreads();
     }
 
-    if (!GATE) return;
     // ---------------- phase 3: bias, logits out, top-k, histogram
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -662,6 +656,198 @@ topk_kernel(const float *__restrict__ logits, int T, int E, int k, int renorm,
     }
 }
 
+// ---------------------------------------------------------------- RMSNorm alone
+// Used ahead of the tensor-core gate.  The sum of squares of a row is one
+// sequential fused multiply-add chain in ascending h (lane t of warp 0 takes
+// row t of a batch), so what bounds the kernel is how many rows are summed
+// at once: each CTA keeps a batch of whole rows resident in shared memory
+// (as many as fit, at most 32) and normalises them from there once their
+// factors are known, so x is read from memory once.
+//   warp 0     the chains; after a batch it publishes the factors (named
+//              barrier 2, with the workers) and starts on the next batch;
+//   warps 1..7 the workers: normalise the finished batch chunk by chunk
+//              and refill each chunk with the next batch's rows as soon as
+//              every worker is done reading it (named barrier 1), with
+//              16-byte cp.async copies; a chunk's mbarrier completes when
+//              every worker's copies of it have landed.
+// Every worker thread owns one 16-byte column group of a chunk and a
+// stride of rows, so the gamma values it needs are loaded once per chunk.
+// Row stride H*2 + 16 bytes keeps the 32 lanes' 16-byte reads of one
+// column in distinct banks.
+constexpr int RN_THREADS = 256;
+constexpr int RN_WORKERS = RN_THREADS - 32;
+constexpr int RN_MAX_CHUNKS = 64;
+constexpr int RN_SMEM_CAP = 220 * 1024;
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__global__ void __launch_bounds__(RN_THREADS)
+rmsnorm_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma, int T, int H,
+               float eps, uint16_t *__restrict__ xn, int rows, int chunk_cols, int nchunks,
+               int stride, int32_t *dev_status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full[RN_MAX_CHUNKS];
+    __shared__ float s_r[2][32];
+    __shared__ int s_stop[2];    // per batch parity: the chains gave up (bounded wait ran out)
+    __shared__ int s_abort_v;
+    volatile int *s_abort = &s_abort_v;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        *s_abort = 0;
+        for (int c = 0; c < nchunks; ++c) mbar_init(&full[c], RN_WORKERS);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int nbatch = (T + rows - 1) / rows;
+    const int nb = blockIdx.x < nbatch ? (nbatch - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (warp == 0) {
+        for (int b = 0; b < nb; ++b) {
+            const int t0 = (blockIdx.x + b * gridDim.x) * rows;
+            const int nr = min(rows, T - t0);
+            const uint32_t parity = b & 1;
+            float ss = 0.0f;
+            bool ok = true;
+            for (int c = 0; c < nchunks; ++c) {
+                if (!mbar_wait_bounded(&full[c], parity, s_abort, dev_status)) {
+                    ok = false;
+                    break;
+                }
+                if (lane < nr) {
+                    const int h0 = c * chunk_cols;
+                    const int nv = min(chunk_cols, H - h0) / 8;   // even: chunks are 128k columns
+                    const uint4 *row = reinterpret_cast<const uint4 *>(smem + lane * stride + h0 * 2);
+                    uint4 q0 = row[0], q1 = row[1];
+                    for (int v = 0; v < nv; v += 2) {
+                        const int vn = v + 2 < nv ? v + 2 : v;  // ahead of the chain
+                        const uint4 n0 = row[vn], n1 = row[vn + 1];
+                        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float a = __uint_as_float(w[i] << 16);
+                            const float bb = __uint_as_float(w[i] & 0xFFFF0000u);
+                            ss = __fmaf_rn(a, a, ss);
+                            ss = __fmaf_rn(bb, bb, ss);
+                        }
+                        q0 = n0;
+                        q1 = n1;
+                    }
+                }
+            }
+            if (ok && lane < nr) {
+                const float mean = __fdiv_rn(ss, static_cast<float>(H));
+                s_r[parity][lane] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+            }
+            if (lane == 0) s_stop[parity] = ok ? 0 : 1;
+            __syncwarp();
+            named_bar_arrive(2, RN_THREADS);    // factors of batch b (or the stop) published
+            if (!ok) return;
+        }
+        return;
+    }
+
+    // workers
+    const int lt = tid - 32;
+    auto load_chunk = [&](int b, int c) {
+        const int t0 = (blockIdx.x + b * gridDim.x) * rows;
+        const int nr = min(rows, T - t0);
+        const int h0 = c * chunk_cols;
+        const int cg = min(chunk_cols, H - h0) / 8;
+        const int rstep = RN_WORKERS / cg;
+        const int g = lt % cg;
+        if (lt < rstep * cg)
+            for (int r = lt / cg; r < nr; r += rstep)
+                cp_async16(smem + r * stride + h0 * 2 + g * 16,
+                           x + static_cast<size_t>(t0 + r) * H + h0 + g * 8, 16);
+        cp_async_arrive_noinc(&full[c]);
+    };
+    if (nb > 0)
+        for (int c = 0; c < nchunks; ++c) load_chunk(0, c);
+    for (int b = 0; b < nb; ++b) {
+        named_bar_sync(2, RN_THREADS);
+        // s_stop[b & 1] is not written again before every worker has passed
+        // the next barrier 2, so all workers see the same value
+        if (s_stop[b & 1]) break;
+        const int t0 = (blockIdx.x + b * gridDim.x) * rows;
+        const int nr = min(rows, T - t0);
+        const float *rr = s_r[b & 1];
+        // gamma of the thread's column group, one chunk ahead
+        auto gamma_of = [&](int c) {
+            const int h0 = c * chunk_cols;
+            const int cg = min(chunk_cols, H - h0) / 8;
+            return gamma && lt < (RN_WORKERS / cg) * cg
+                       ? __ldg(reinterpret_cast<const uint4 *>(gamma + h0) + lt % cg)
+                       : make_uint4(0u, 0u, 0u, 0u);
+        };
+        uint4 gq_next = gamma_of(0);
+        for (int c = 0; c < nchunks; ++c) {
+            const int h0 = c * chunk_cols;
+            const int cg = min(chunk_cols, H - h0) / 8;
+            const int rstep = RN_WORKERS / cg;
+            const int g = lt % cg;
+            const uint4 gq = gq_next;
+            if (c + 1 < nchunks) gq_next = gamma_of(c + 1);
+            if (lt < rstep * cg) {
+                float gm[8];
+                if (gamma) {
+                    const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        gm[2 * i] = __uint_as_float(gw[i] << 16);
+                        gm[2 * i + 1] = __uint_as_float(gw[i] & 0xFFFF0000u);
+                    }
+                }
+                for (int r0 = lt / cg; r0 < nr; r0 += 4 * rstep) {
+                    uint4 q[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = r0 + j * rstep;
+                        if (r < nr)
+                            q[j] = *reinterpret_cast<const uint4 *>(smem + r * stride + h0 * 2 +
+                                                                    g * 16);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = r0 + j * rstep;
+                        if (r >= nr) break;
+                        const float rv = rr[r];
+                        const uint32_t w[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+                        uint32_t packed[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float lo = __fmul_rn(__uint_as_float(w[i] << 16), rv);
+                            float hi = __fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), rv);
+                            if (gamma) {
+                                lo = __fmul_rn(lo, gm[2 * i]);
+                                hi = __fmul_rn(hi, gm[2 * i + 1]);
+                            }
+                            const __nv_bfloat162 p2 = __floats2bfloat162_rn(lo, hi);
+                            packed[i] = *reinterpret_cast<const uint32_t *>(&p2);
+                        }
+                        *reinterpret_cast<uint4 *>(xn + static_cast<size_t>(t0 + r) * H + h0 +
+                                                   g * 8) =
+                            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    }
+                }
+            }
+            if (b + 1 < nb) {
+                named_bar_sync(1, RN_WORKERS);   // every worker is done reading chunk c
+                load_chunk(b + 1, c);
+            }
+        }
+    }
+    cp_async_wait<0>();    // nothing of this CTA's copies is left in flight
+}
+
 // ---------------------------------------------------------------- tensor-core gate
 // The gate on the tensor cores at fp32 accuracy: each fp32 weight splits
 // exactly into three bf16 parts, w = w1 + w2 + w3 (w1 = bf16(w), w2 =
@@ -672,61 +858,66 @@ topk_kernel(const float *__restrict__ logits, int T, int E, int k, int renorm,
 // tensor core) and the combine kernel adds them: logit = (p1 + p2) + p3.
 // The sum is fp32-accurate but not in the sequential order of the plain
 // definition, so a logit can differ from it in the last bits.
+//
+// Split: blockIdx.y = output row (part * E + e, zero rows up to NW), four
+// columns per thread.
 __global__ void __launch_bounds__(256)
-gate_split_kernel(const float *__restrict__ wg, int E, int H, uint16_t *__restrict__ ws,
-                  int NW) {
-    const int64_t n = static_cast<int64_t>(NW) * H;
-    for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n; i += gridDim.x * 256ll) {
-        const int row = static_cast<int>(i / H), h = static_cast<int>(i % H);
-        const int part = row / E, e = row % E;
-        uint16_t out = 0;
-        if (part < 3) {
-            const float w = wg[static_cast<size_t>(e) * H + h];
+gate_split_kernel(const float *__restrict__ wg, int E, int H, uint16_t *__restrict__ ws) {
+    const int row = blockIdx.y;
+    const int part = row / E, e = row - part * E;
+    const int h = 4 * (blockIdx.x * 256 + threadIdx.x);
+    if (h >= H) return;
+    uint32_t out[2] = {0u, 0u};
+    if (part < 3) {
+        const float4 wv = __ldg(reinterpret_cast<const float4 *>(wg + static_cast<size_t>(e) * H + h));
+        const float w4[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float w = w4[i];
             const uint16_t b1 = float_to_bf16_bits(w);
             const float r1 = __fsub_rn(w, bf16_bits_to_float(b1));
             const uint16_t b2 = float_to_bf16_bits(r1);
             const float r2 = __fsub_rn(r1, bf16_bits_to_float(b2));
-            out = part == 0 ? b1 : part == 1 ? b2 : float_to_bf16_bits(r2);
+            const uint16_t v = part == 0 ? b1 : part == 1 ? b2 : float_to_bf16_bits(r2);
+            out[i >> 1] |= static_cast<uint32_t>(v) << (16 * (i & 1));
         }
-        ws[i] = out;
     }
+    *reinterpret_cast<uint2 *>(ws + static_cast<size_t>(row) * H + h) = make_uint2(out[0], out[1]);
 }
 
-// One CTA per 32-token chunk, a warp per token: logit = (p1 + p2) + p3
-// (+ bias); with E <= 64 also the top-k / softmax and the chunk's routing
-// histogram (as the router's phase 3).
-__global__ void __launch_bounds__(128)
+// Combine: one CTA per 32-token chunk, one warp per token: logit = (p1 +
+// p2) + p3 (+ bias); with E <= 64 also the top-k / softmax and the chunk's
+// routing histogram (as the router's phase 3), else the logits.
+constexpr int GC_THREADS = 32 * RT_TOK;
+
+__global__ void __launch_bounds__(GC_THREADS)
 gate_combine_kernel(const float *__restrict__ parts, int NW, int T, int E,
                     const float *__restrict__ gate_bias, float *__restrict__ logits,
                     int fuse_topk, int k, int renorm, int32_t *__restrict__ topk_idx,
                     float *__restrict__ topk_w, int32_t *__restrict__ hist) {
     __shared__ int s_cnt[RT_EXP];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tok0 = blockIdx.x * RT_TOK;
-    const int ntok = min(RT_TOK, T - tok0);
-    if (fuse_topk)
-        for (int e = threadIdx.x; e < RT_EXP; e += 128) s_cnt[e] = 0;
-    __syncthreads();
-    for (int tl = warp; tl < ntok; tl += 4) {
-        const int t = tok0 + tl;
+    const int t = blockIdx.x * RT_TOK + warp;
+    if (fuse_topk && threadIdx.x < RT_EXP) s_cnt[threadIdx.x] = 0;
+    if (fuse_topk) __syncthreads();
+    if (t < T) {
         const float *pr = parts + static_cast<size_t>(t) * NW;
-        for (int e0 = 0; e0 < E; e0 += 32) {
-            const int e = e0 + lane;
-            if (e < E) {
-                float v = __fadd_rn(__fadd_rn(pr[e], pr[E + e]), pr[2 * E + e]);
-                if (gate_bias) v = __fadd_rn(v, gate_bias[e]);
-                if (logits) logits[static_cast<size_t>(t) * E + e] = v;
-            }
-        }
         if (fuse_topk) {
             float v[2];
+            float p[2][3];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int e = lane + 32 * i;
+#pragma unroll
+                for (int j = 0; j < 3; ++j) p[i][j] = e < E ? __ldg(pr + j * E + e) : 0.0f;
+            }
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int e = lane + 32 * i;
                 float val = -INFINITY;
                 if (e < E) {
-                    val = __fadd_rn(__fadd_rn(pr[e], pr[E + e]), pr[2 * E + e]);
-                    if (gate_bias) val = __fadd_rn(val, gate_bias[e]);
+                    val = __fadd_rn(__fadd_rn(p[i][0], p[i][1]), p[i][2]);
+                    if (gate_bias) val = __fadd_rn(val, __ldg(gate_bias + e));
                 }
                 v[i] = val;
             }
@@ -740,11 +931,17 @@ gate_combine_kernel(const float *__restrict__ parts, int NW, int T, int E,
                 topk_w[a] = w;
                 atomicAdd(&s_cnt[sel_e], 1);
             }
+        } else {
+            for (int e = lane; e < E; e += 32) {
+                float v = __fadd_rn(__fadd_rn(__ldg(pr + e), __ldg(pr + E + e)), __ldg(pr + 2 * E + e));
+                if (gate_bias) v = __fadd_rn(v, __ldg(gate_bias + e));
+                logits[static_cast<size_t>(t) * E + e] = v;
+            }
         }
     }
     if (fuse_topk && hist) {
         __syncthreads();
-        for (int e = threadIdx.x; e < E; e += 128)
+        for (int e = threadIdx.x; e < E; e += GC_THREADS)
             hist[static_cast<size_t>(blockIdx.x) * E + e] = s_cnt[e];
     }
 }
@@ -823,7 +1020,7 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(router_kernel<true>,
+        cudaError_t e = cudaFuncSetAttribute(router_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SMEM_TOTAL);
         if (e != cudaSuccess) return e;
@@ -831,7 +1028,7 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
     }
     dim3 grid(static_cast<unsigned>(ceil_div(T, RT_TOK)),
               static_cast<unsigned>(ceil_div(E, RT_EXP)));
-    router_kernel<true><<<grid, RT_THREADS, SMEM_TOTAL, stream>>>(
+    router_kernel<<<grid, RT_THREADS, SMEM_TOTAL, stream>>>(
         x, gamma, wg, gate_bias, T, H, E, eps, rmsnorm ? 1 : 0, xn, logits,
         fuse_topk ? 1 : 0, k, renorm ? 1 : 0, topk_idx, topk_w, hist, dev_status);
     return cudaGetLastError();
@@ -862,28 +1059,43 @@ cudaError_t launch_topk(const float *logits, int T, int E, int k, bool renorm,
 cudaError_t launch_rmsnorm(const uint16_t *x, const uint16_t *gamma, int T, int H, float eps,
                            uint16_t *xn, int32_t *dev_status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    static bool attr_done[64] = {};
+    if (H <= 0 || H % 128 != 0) return cudaErrorInvalidValue;
+    const int stride = H * 2 + 16;
+    const int rows = std::min(32, RN_SMEM_CAP / stride);
+    if (rows < 1) return cudaErrorInvalidValue;
+    // chunks of 256 columns (at most RN_MAX_CHUNKS of them, and at most 8 *
+    // RN_WORKERS columns, so that every worker owns at most one column group)
+    const int chunk_cols = std::max(256, static_cast<int>(ceil_div(H, RN_MAX_CHUNKS * 128)) * 128);
+    const int nchunks = static_cast<int>(ceil_div(H, chunk_cols));
+    if (chunk_cols / 8 > RN_WORKERS || nchunks > RN_MAX_CHUNKS) return cudaErrorInvalidValue;
+    const int smem = rows * stride;
+    static std::mutex mu;
+    static int attr_smem[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(router_kernel<false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_TOTAL);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && attr_smem[dev] < smem) {
+            cudaError_t e = cudaFuncSetAttribute(rmsnorm_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 RN_SMEM_CAP);
+            if (e != cudaSuccess) return e;
+            attr_smem[dev] = RN_SMEM_CAP;
+        }
     }
-    router_kernel<false><<<static_cast<unsigned>(ceil_div(T, RT_TOK)), RT_THREADS, SMEM_TOTAL,
-                           stream>>>(x, gamma, nullptr, nullptr, T, H, RT_EXP, eps, 1, xn, nullptr,
-                                     0, 1, 0, nullptr, nullptr, nullptr, dev_status);
+    const int per_sm = std::max(1, std::min(8, (227 * 1024) / (smem + 1024)));
+    const int64_t nbatch = ceil_div(T, rows);
+    const int grid = static_cast<int>(std::min<int64_t>(nbatch, int64_t{num_sms()} * per_sm));
+    rmsnorm_kernel<<<grid, RN_THREADS, smem, stream>>>(x, gamma, T, H, eps, xn, rows, chunk_cols,
+                                                       nchunks, stride, dev_status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gate_split(const float *wg, int E, int H, uint16_t *wsplit, int NW,
                               cudaStream_t stream) {
-    const int64_t n = static_cast<int64_t>(NW) * H;
-    const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(n, 256),
-                                                                             num_sms() * 8)));
-    gate_split_kernel<<<blocks, 256, 0, stream>>>(wg, E, H, wsplit, NW);
+    if (H % 4 != 0 || NW < 3 * E) return cudaErrorInvalidValue;
+    dim3 grid(static_cast<unsigned>(ceil_div(H / 4, 256)), static_cast<unsigned>(NW));
+    gate_split_kernel<<<grid, 256, 0, stream>>>(wg, E, H, wsplit);
     return cudaGetLastError();
 }
 
@@ -893,7 +1105,8 @@ cudaError_t launch_gate_combine(const float *parts, int NW, int T, int E, const 
                                 cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     const bool fuse = fuse_topk && E <= RT_EXP;
-    gate_combine_kernel<<<static_cast<unsigned>(ceil_div(T, RT_TOK)), 128, 0, stream>>>(
+    if (!fuse && !logits) return cudaErrorInvalidValue;
+    gate_combine_kernel<<<static_cast<unsigned>(ceil_div(T, RT_TOK)), GC_THREADS, 0, stream>>>(
         parts, NW, T, E, gate_bias, logits, fuse ? 1 : 0, k, renorm ? 1 : 0, topk_idx, topk_w,
         fuse ? hist : nullptr);
     return cudaGetLastError();

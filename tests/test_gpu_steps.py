@@ -53,6 +53,25 @@ def test_rmsnorm_gate_bitexact(wl):
     assert np.array_equal(logits.cpu().numpy().view(np.uint32), lg_ref.view(np.uint32))
 
 
+# the RMSNorm-only pass (ahead of the tensor-core gate): rows resident in
+# shared memory, 27 rows per CTA at H=4096, 32 below; chunked fills; many
+# batches per CTA; a ragged last batch; gamma absent (all ones)
+@pytest.mark.parametrize("T,H,gamma_std,with_gamma", [
+    (1, 128, 0.1, True), (33, 4096, 0.1, True), (5000, 4096, 0.1, True),
+    (1000, 1024, 0.0, False), (700, 8192, 0.2, True), (64, 384, 0.1, True),
+    (20000, 256, 0.1, True)])
+def test_rmsnorm_only_bitexact(T, H, gamma_std, with_gamma):
+    wl = Workload("rn", T=T, H=H, E=4, k=1, I=128, rmsnorm=True, gamma_std=gamma_std)
+    d = make_inputs(wl, 3, only=("x", "gamma"))
+    gamma = d["gamma"] if with_gamma else None
+    xn, lg = moe.rmsnorm_gate(d["x"].to(DEV), None, gamma.to(DEV) if gamma is not None else None,
+                              None, wl.eps)
+    torch.cuda.synchronize()
+    assert lg is None
+    ones = torch.ones(H, dtype=torch.bfloat16)
+    assert np.array_equal(u16(xn), oracle.rmsnorm(d["x"], gamma if with_gamma else ones, wl.eps))
+
+
 def test_rmsnorm_gate_empty():
     x = torch.empty((0, 128), dtype=torch.bfloat16, device=DEV)
     wg = torch.zeros((8, 128), dtype=torch.float32, device=DEV)
