@@ -286,12 +286,15 @@ moe_status_t moe_layer_forward_timed(const moe_desc_t *desc, const moe_bf16_t *x
                                      moe_stream_t stream, void *const *stage_events);
 
 /*
- * moe_layer_forward with the shared expert on a second stream
- * ("MoE多流并行优化": the shared expert runs beside the routed experts on
- * another stream).  Same results, bit for bit, as moe_layer_forward.  The
- * routed path runs on `stream`; after the router, `fork_event` is recorded on
- * `stream` and awaited by `shared_stream`, which runs the shared expert's two
- * matmuls and records `join_event`; `stream` awaits it before finalize.
+ * moe_layer_forward on two streams ("MoE多流并行优化": the shared expert
+ * runs beside the routed path on another stream).  Same results, bit for
+ * bit, as moe_layer_forward.  After the routing indices, `fork_event` is
+ * recorded on `stream` and awaited by `shared_stream`, which copies the rows
+ * into expert order (memory-bound) and records `join_event`; meanwhile
+ * `stream` computes the shared expert's w13 matmul (tensor-bound), then
+ * awaits `join_event` and runs the routed matmuls and finalize.  (On GB300
+ * this beat running the shared expert's matmuls themselves on the second
+ * stream: two persistent matmul kernels cannot share the SMs.)
  * The caller owns both streams and both events (cudaEvent_t, any flags) and
  * must not use the events concurrently elsewhere.  Requires MOE_SHARED.
  * stage_events: as in moe_layer_forward_timed (recorded on `stream`), or NULL.

@@ -346,8 +346,9 @@ moe_status_t moe_layer_workspace_size(const moe_desc_t *desc, size_t *bytes) {
 namespace {
 
 // The layer; `stage_events` as in moe_layer_forward_timed; with
-// `shared_stream` the shared expert's matmuls run on that stream between
-// `fork_event` (after the router) and `join_event` (before finalize).
+// `shared_stream` the row copies of init_routing run on that stream (between
+// `fork_event` and `join_event`) while `stream` computes the shared expert's
+// w13, so the memory-bound copies overlap a tensor-bound matmul.
 moe_status_t layer_forward_impl(const moe_desc_t *desc, const moe_bf16_t *x,
                                 const moe_bf16_t *gamma, const float *wg, const float *gate_bias,
                                 const moe_bf16_t *w13, const moe_bf16_t *w2,
@@ -440,50 +441,42 @@ moe_status_t layer_forward_impl(const moe_desc_t *desc, const moe_bf16_t *x,
     MOE_TRY(launch_route_scan(hist, B, E, counts, offsets, s));
     MOE_TRY(launch_route_scatter(idx, hist, T, k, E, row_idx, nullptr, nullptr, dev_status, s));
     MOE_TRY(mark(2));
-    MOE_TRY(launch_permute(xs, row_idx, T, H, k, ex, s));
-    // (shared expert on its own stream: fork after the router)
     const bool two_streams = shared && shared_stream != nullptr;
+    GemmSegment1 sh13;       // the shared expert's w13 + SwiGLU as a dense segment
+    if (shared) {
+        sh13.A = xs;
+        sh13.B = w13_s;
+        sh13.rows = T;
+        sh13.K1 = H;
+        sh13.N1 = d.I_shared;
+        sh13.out = act_s;
+    }
     if (two_streams) {
+        // The row copies (memory-bound) run on the second stream while this
+        // stream computes the shared expert's w13 (tensor-bound); the routed
+        // w13 waits for both.
         cudaStream_t s2 = reinterpret_cast<cudaStream_t>(shared_stream);
         cudaEvent_t fork = static_cast<cudaEvent_t>(fork_event);
         cudaEvent_t join = static_cast<cudaEvent_t>(join_event);
-        GemmSegment1 a1, a2;
-        a1.A = xs;
-        a1.B = w13_s;
-        a1.rows = T;
-        a1.K1 = H;
-        a1.N1 = d.I_shared;
-        a1.out = act_s;
-        a2.A = act_s;
-        a2.B = w2_s;
-        a2.rows = T;
-        a2.K1 = d.I_shared;
-        a2.N1 = H;
-        a2.out = y_s;
-        a2.out_f32 = true;
         MOE_TRY(cudaEventRecord(fork, s));
         MOE_TRY(cudaStreamWaitEvent(s2, fork, 0));
-        MOE_TRY(launch_gemm_swiglu(nullptr, offsets, 0, 0, H, nullptr, I, nullptr, a1, dev_status,
-                                   s2));
-        MOE_TRY(launch_gemm_store(nullptr, offsets, 0, 0, d.I_shared, nullptr, H, nullptr, a2,
-                                  dev_status, s2));
+        MOE_TRY(launch_permute(xs, row_idx, T, H, k, ex, s2));
         MOE_TRY(cudaEventRecord(join, s2));
+        MOE_TRY(mark(3));
+        MOE_TRY(launch_gemm_swiglu(nullptr, offsets, 0, 0, H, nullptr, I, nullptr, sh13,
+                                   dev_status, s));
+        MOE_TRY(cudaStreamWaitEvent(s, join, 0));
+        const GemmSegment1 none{};
+        MOE_TRY(launch_gemm_swiglu(ex, offsets, E, N, H, w13, I, act, none, dev_status, s));
+    } else {
+        MOE_TRY(launch_permute(xs, row_idx, T, H, k, ex, s));
+        // 3. grouped w13 + SwiGLU (the shared expert rides along as a dense segment)
+        MOE_TRY(mark(3));
+        MOE_TRY(launch_gemm_swiglu(ex, offsets, E, N, H, w13, I, act, sh13, dev_status, s));
     }
-    // 3. grouped w13 + SwiGLU (the shared expert rides along as a dense segment)
-    GemmSegment1 s1;
-    if (shared && !two_streams) {
-        s1.A = xs;
-        s1.B = w13_s;
-        s1.rows = T;
-        s1.K1 = H;
-        s1.N1 = d.I_shared;
-        s1.out = act_s;
-    }
-    MOE_TRY(mark(3));
-    MOE_TRY(launch_gemm_swiglu(ex, offsets, E, N, H, w13, I, act, s1, dev_status, s));
-    // 4. grouped down projection (shared expert output kept in fp32)
+    // 4. grouped down projection (the shared expert's as a dense segment, kept in fp32)
     GemmSegment1 s2;
-    if (shared && !two_streams) {
+    if (shared) {
         s2.A = act_s;
         s2.B = w2_s;
         s2.rows = T;
@@ -495,7 +488,6 @@ moe_status_t layer_forward_impl(const moe_desc_t *desc, const moe_bf16_t *x,
     MOE_TRY(mark(4));
     MOE_TRY(launch_gemm_store(act, offsets, E, N, I, w2, H, y, s2, dev_status, s));
     // 5. finalize: weighted sum in slot order + shared row
-    if (two_streams) MOE_TRY(cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(join_event), 0));
     MOE_TRY(mark(5));
     MOE_TRY(launch_finalize(y, row_idx, w, y_s, true, T, H, k, out,
                             (d.flags & MOE_OUT_F32) != 0, s));
