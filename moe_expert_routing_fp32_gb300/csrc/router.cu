@@ -885,61 +885,72 @@ gate_split_kernel(const float *__restrict__ wg, int E, int H, uint16_t *__restri
     *reinterpret_cast<uint2 *>(ws + static_cast<size_t>(row) * H + h) = make_uint2(out[0], out[1]);
 }
 
-// Combine: one CTA per 32-token chunk, one warp per token: logit = (p1 +
-// p2) + p3 (+ bias); with E <= 64 also the top-k / softmax and the chunk's
-// routing histogram (as the router's phase 3), else the logits.
-constexpr int GC_THREADS = 32 * RT_TOK;
+// Combine: one CTA per 32-token chunk.  All threads form the chunk's logits,
+// logit = (p1 + p2) + p3 (+ bias), coalesced over (token, expert); without
+// fuse_topk they go to `logits`.  With it (E <= 64) they stay in shared
+// memory and lane t of warp 0 takes token t's top-k by k argmax passes over
+// its row (ascending expert index, a later value wins only if strictly
+// larger, so equal logits go to the lower index), then its softmax weights
+// and the chunk's routing histogram.  (A warp-wide argmax per token spent
+// the kernel's time on shuffles.)
+constexpr int GC_THREADS = 256;
 
 __global__ void __launch_bounds__(GC_THREADS)
 gate_combine_kernel(const float *__restrict__ parts, int NW, int T, int E,
                     const float *__restrict__ gate_bias, float *__restrict__ logits,
                     int fuse_topk, int k, int renorm, int32_t *__restrict__ topk_idx,
                     float *__restrict__ topk_w, int32_t *__restrict__ hist) {
+    __shared__ float s_lg[RT_TOK][RT_EXP + 1];
+    __shared__ int s_sel[RT_TOK][33];
     __shared__ int s_cnt[RT_EXP];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * RT_TOK + warp;
+    const int tok0 = blockIdx.x * RT_TOK;
+    const int ntok = min(RT_TOK, T - tok0);
     if (fuse_topk && threadIdx.x < RT_EXP) s_cnt[threadIdx.x] = 0;
-    if (fuse_topk) __syncthreads();
-    if (t < T) {
-        const float *pr = parts + static_cast<size_t>(t) * NW;
-        if (fuse_topk) {
-            float v[2];
-            float p[2][3];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int e = lane + 32 * i;
-#pragma unroll
-                for (int j = 0; j < 3; ++j) p[i][j] = e < E ? __ldg(pr + j * E + e) : 0.0f;
-            }
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int e = lane + 32 * i;
-                float val = -INFINITY;
-                if (e < E) {
-                    val = __fadd_rn(__fadd_rn(p[i][0], p[i][1]), p[i][2]);
-                    if (gate_bias) val = __fadd_rn(val, __ldg(gate_bias + e));
+    for (int i = threadIdx.x; i < ntok * E; i += GC_THREADS) {
+        const int t = i / E, e = i - t * E;
+        const float *pr = parts + static_cast<size_t>(tok0 + t) * NW;
+        float v = __fadd_rn(__fadd_rn(__ldg(pr + e), __ldg(pr + E + e)), __ldg(pr + 2 * E + e));
+        if (gate_bias) v = __fadd_rn(v, __ldg(gate_bias + e));
+        if (fuse_topk)
+            s_lg[t][e] = v;
+        else
+            logits[static_cast<size_t>(tok0 + t) * E + e] = v;
+    }
+    if (!fuse_topk) return;
+    __syncthreads();
+    if (threadIdx.x < RT_TOK && static_cast<int>(threadIdx.x) < ntok) {
+        const int t = threadIdx.x;
+        const float *row = s_lg[t];
+        uint64_t taken = 0;
+        for (int j = 0; j < k; ++j) {
+            int bi = -1;
+            float bv = -INFINITY;
+            for (int e = 0; e < E; ++e) {
+                const float v = row[e];
+                if (!((taken >> e) & 1ull) && (bi < 0 || v > bv)) {
+                    bv = v;
+                    bi = e;
                 }
-                v[i] = val;
             }
-            int sel_e;
-            float sel_v;
-            warp_topk<2>(v, k, &sel_e, &sel_v);
-            const float w = slot_weight<2>(v, k, renorm != 0, sel_v);
-            if (lane < k) {
-                const size_t a = static_cast<size_t>(t) * k + lane;
-                topk_idx[a] = sel_e;
-                topk_w[a] = w;
-                atomicAdd(&s_cnt[sel_e], 1);
-            }
+            taken |= 1ull << bi;
+            s_sel[t][j] = bi;
+        }
+        const float m = row[s_sel[t][0]];
+        float den = 0.0f;
+        if (renorm) {
+            for (int j = 0; j < k; ++j) den += expf(row[s_sel[t][j]] - m);
         } else {
-            for (int e = lane; e < E; e += 32) {
-                float v = __fadd_rn(__fadd_rn(__ldg(pr + e), __ldg(pr + E + e)), __ldg(pr + 2 * E + e));
-                if (gate_bias) v = __fadd_rn(v, __ldg(gate_bias + e));
-                logits[static_cast<size_t>(t) * E + e] = v;
-            }
+            for (int e = 0; e < E; ++e) den += expf(row[e] - m);
+        }
+        const size_t a0 = static_cast<size_t>(tok0 + t) * k;
+        for (int j = 0; j < k; ++j) {
+            const int e = s_sel[t][j];
+            topk_idx[a0 + j] = e;
+            topk_w[a0 + j] = expf(row[e] - m) / den;
+            atomicAdd(&s_cnt[e], 1);
         }
     }
-    if (fuse_topk && hist) {
+    if (hist) {
         __syncthreads();
         for (int e = threadIdx.x; e < E; e += GC_THREADS)
             hist[static_cast<size_t>(blockIdx.x) * E + e] = s_cnt[e];
