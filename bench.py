@@ -64,6 +64,9 @@ def parse_args():
                     help="run the shared expert on a second stream (moe_layer_forward_streams); "
                          "off keeps it inside the same launches, so the dominant kernel's "
                          "roofline is measured on its own")
+    ap.add_argument("--gate-sequential", action="store_true",
+                    help="the sequential fp32 gate (MOE_GATE_SEQUENTIAL) instead of the "
+                         "tensor-core gate for T > 512")
     ap.add_argument("--tp", type=int, default=1,
                     help="time one MoE tensor-parallel shard: I and I_shared divided by tp")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -236,23 +239,36 @@ def cpu_oracle_rate(inputs_cpu, wl, seconds, first_token=0):
 
 # --------------------------------------------------------------- our arm
 def stage_bytes_flops(wl, two_streams=False):
-    """Algorithmic work of each timed stage.  With the shared expert on its
-    own stream the main stream's GEMM stages run the routed experts only (the
-    shared matmuls overlap on the second stream), so only routed flops are
-    credited to them: a conservative count."""
+    """Algorithmic work of each timed stage.  With two streams the row copies
+    run on the second stream beside the shared expert's w13, so the permute
+    stage of the main stream is empty and gets no bytes; both matmul stages
+    still run every matmul on the main stream."""
     T, H, E, k, I, Is = wl.T, wl.H, wl.E, wl.k, wl.I, wl.I_s
     N = T * k
-    if two_streams:
-        Is = 0
     # algorithmic work of each stage (what the step must touch or compute once)
     return {
         "router": {"bytes": T * H * 2 + (T * H * 2 if wl.rmsnorm else 0) + E * H * 4 + N * 8,
                    "gate_flops": 2.0 * T * H * E},
-        "permute": {"bytes": T * H * 2 + N * H * 2 + N * 4},
+        "permute": {"bytes": 0 if two_streams else T * H * 2 + N * H * 2 + N * 4},
         "gemm_w13_swiglu": {"flops": 4.0 * N * H * I + 4.0 * T * H * Is},
         "gemm_down": {"flops": 2.0 * N * H * I + 2.0 * T * H * Is},
         "finalize": {"bytes": N * H * 2 + (T * H * 4 if wl.I_s else 0) + T * H * 2 + N * 8},
     }
+
+
+def launches_per_step(wl, gate_sequential=False, two_streams=False):
+    """Library kernel launches of one layer pass (the tile-counter memsets
+    before the CTA-pair matmuls are not kernels)."""
+    E, T = wl.E, wl.T
+    if T <= 512 and E <= 128 and wl.H <= 8192:
+        router = 2 if E <= 64 else 3            # small-batch router + histogram (+ top-k)
+    elif T > 512 and not gate_sequential:
+        # RMSNorm, split, gate GEMM, combine (+ top-k and histogram for E > 64)
+        router = (1 if wl.rmsnorm else 0) + 3 + (2 if E > 64 else 0)
+    else:
+        router = 1 + (2 if E > 64 else 0)       # sequential router (+ top-k, histogram)
+    # scan, scatter, permute, w13 (two launches on two streams), down, finalize
+    return router + 6 + (1 if two_streams else 0)
 
 
 def run_ours(args, rank, world, local):
@@ -267,7 +283,7 @@ def run_ours(args, rank, world, local):
     weights = moe.LayerWeights(wg=g["wg"], w13=g["w13"], w2=g["w2"], gamma=g["gamma"],
                                gate_bias=g["gate_bias"], w13_s=g["w13_s"], w2_s=g["w2_s"])
     desc = moe.make_desc(wl.T, wl.H, wl.E, wl.k, wl.I, wl.I_s, rmsnorm=wl.rmsnorm, eps=wl.eps,
-                         renorm=wl.renorm, out_f32=False)
+                         renorm=wl.renorm, out_f32=False, gate_sequential=args.gate_sequential)
     ws = torch.empty(moe.layer_workspace_size(desc), dtype=torch.uint8, device=dev)
     out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
     status = moe.new_status(dev)
@@ -385,7 +401,7 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
             e["gate_fp32_tflops"] = round(wk["gate_flops"] / (ms / 1e3) / 1e12, 2)
         per_stage[name] = e
 
-    launches_per_step = 7 + (2 if wl.E > 64 else 0)
+    launches = launches_per_step(wl, args.gate_sequential, two_streams)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
@@ -395,7 +411,9 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
                    "I_shared": wl.I_s, "rmsnorm": wl.rmsnorm, "out": "bf16",
                    "shared_expert": ("none" if not wl.I_s else
                                      "second stream" if two_streams else "same launches"),
-                   "gate": "fp32", "l2": "inputs larger than L2 (no flush needed)",
+                   "gate": ("fp32, sequential FMA order" if args.gate_sequential or wl.T <= 512
+                            else "fp32 on the tensor cores (exact 3-part bf16 split of Wg)"),
+                   "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": round(achieved / tc_peak, 4),
@@ -409,7 +427,7 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
             "value": round(e2e_value, 1), "unit": UNIT,
             "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2,
             "timing": "wall clock, copies of neighbouring steps overlap the compute"},
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": launches * K,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -122,10 +122,12 @@ moe_status_t moe_rmsnorm_gate(const moe_bf16_t *x, const moe_bf16_t *gamma,
  *   xs     [T, H] bf16 in: the (already normalised) hidden states
  *   wg     [E, H] fp32 in;  gate_bias [E] fp32 or NULL
  *   logits [T, E] fp32 out
- * H % 128 == 0, E <= 1024.  T may be 0.  Workspace (the split weight and
- * the partial logits): moe_gate_tensor_workspace_size() bytes, 256-byte
- * aligned, caller-owned.  A device-side wait that runs out sets *dev_status
- * (may be NULL).
+ * H % 128 == 0, E <= 1024.  T may be 0.  Workspace:
+ * moe_gate_tensor_workspace_size() bytes, 256-byte aligned, caller-owned;
+ * it starts with the split weight [NW, H] bf16 (NW = 3E rounded up to a
+ * multiple of 128; rows [pE, (p+1)E) hold part p+1, the rest are zero),
+ * followed (256-byte aligned) by the partial logits [T, NW] fp32.  A
+ * device-side wait that runs out sets *dev_status (may be NULL).
  */
 moe_status_t moe_gate_tensor_workspace_size(int32_t T, int32_t H, int32_t E, size_t *bytes);
 moe_status_t moe_gate_tensor(const moe_bf16_t *xs, const float *wg, const float *gate_bias,

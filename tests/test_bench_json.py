@@ -16,7 +16,7 @@ from moe_inputs import WORKLOADS  # noqa: E402
 def _args(**kw):
     a = dict(workload="imagegen-16k", no_cpu_baseline=True, cpu_seconds=0.1, gpus=1, steps=10,
              warmup=3, T=None, E=None, I=None, Is=None, tp=1, shared_stream="off", seed=0,
-             no_e2e=False, impl="ours")
+             no_e2e=False, impl="ours", gate_sequential=False)
     a.update(kw)
     return argparse.Namespace(**a)
 
@@ -56,3 +56,21 @@ def test_traffic_not_reported_for_a_resized_workload():
     res = bench.finish_ours(args, wl, 1, 0, 10, 3, 10.0, _stages(0.5), CLK, None, {})
     assert res["roofline"]["traffic"] is None
     assert res["e2e"] is None
+
+
+def test_launch_count_follows_the_gate_path():
+    """gpu_launches is the library's kernels per step times the steps: the
+    tensor-core gate adds RMSNorm, split, GEMM and combine launches above 512
+    tokens; the small-batch router and the sequential gate are fewer."""
+    img = WORKLOADS["imagegen-16k"]
+    assert bench.launches_per_step(img) == 10
+    assert bench.launches_per_step(img, gate_sequential=True) == 7
+    assert bench.launches_per_step(img, two_streams=True) == 11
+    assert bench.launches_per_step(WORKLOADS["skewed-32k"]) == 9          # no RMSNorm
+    assert bench.launches_per_step(WORKLOADS["smallbatch-8"]) == 8
+    res = bench.finish_ours(_args(), img, 1, 0, 10, 3, 80.0, _stages(1.0), CLK, None, {})
+    assert res["gpu_launches"] == 100
+    assert "tensor cores" in res["config"]["gate"]
+    res = bench.finish_ours(_args(gate_sequential=True), img, 1, 0, 10, 3, 80.0, _stages(1.0),
+                            CLK, None, {})
+    assert res["gpu_launches"] == 70 and "sequential" in res["config"]["gate"]
