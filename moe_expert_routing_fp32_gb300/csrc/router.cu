@@ -4,7 +4,15 @@
 // the MoE block), "消除gate计算冗余cast算子" (the gate runs in fp32 on the
 // hidden states cast to float, autocast off) and "MoE EP优化" (GatingTopK).
 //
-// One CTA owns 32 tokens and 64 experts:
+// Two gates.  The sequential one (router_kernel, router_small_kernel below)
+// reproduces the plain fp32 loop bit for bit; the layer uses it for batches
+// of at most 512 tokens and on request.  For larger batches the layer runs
+// the tensor-core gate (end of this file): RMSNorm alone (rmsnorm_kernel),
+// the exact three-way bf16 split of the gate weight, the grouped GEMM kernel
+// for the partial logits, and gate_combine_kernel (the fp32 sum of the
+// parts, top-k, weights and the routing histogram).
+//
+// The sequential router: one CTA owns 32 tokens and 64 experts:
 //   phase 1 (RMSNorm only): the 32 rows stream through shared memory in
 //     512-byte pieces (TMA bulk copies, 2-stage ring); warp 0 keeps one fp32
 //     sum of squares per token, accumulated in ascending h;
@@ -18,8 +26,9 @@
 //     histogram of the 32-token chunk, and the logits row write-out.
 // Batches of at most 512 tokens use router_small_kernel instead (one CTA per
 // token, one thread per expert), which keeps every SM busy.
-// The gate is plain fp32 FMA work (2*T*H*E flops); it does not use tensor
-// cores, whose fp32-input mode (tf32) would round the inputs.
+// This gate is plain fp32 FMA work (2*T*H*E flops); the tensor cores' fp32
+// input mode (tf32) would round the inputs, hence the exact bf16 split of the
+// other gate.
 #include <math.h>
 
 #include <algorithm>
