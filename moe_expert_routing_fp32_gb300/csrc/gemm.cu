@@ -357,9 +357,9 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float a0 = __fdiv_rn(g[2 * i], 1.0f + expf(-g[2 * i])) * u[2 * i];
+                        const float a0 = __fdividef(g[2 * i], 1.0f + __expf(-g[2 * i])) * u[2 * i];
                         const float a1 =
-                            __fdiv_rn(g[2 * i + 1], 1.0f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+                            __fdividef(g[2 * i + 1], 1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
                         pk[i] = pack_bf16x2(a0, a1);
                     }
                     if (ok) {
@@ -857,9 +857,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float a0 = __fdiv_rn(g[2 * i], 1.0f + expf(-g[2 * i])) * u[2 * i];
+                        const float a0 = __fdividef(g[2 * i], 1.0f + __expf(-g[2 * i])) * u[2 * i];
                         const float a1 =
-                            __fdiv_rn(g[2 * i + 1], 1.0f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+                            __fdividef(g[2 * i + 1], 1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
                         pk[i] = pack_bf16x2(a0, a1);
                     }
                     if (boxed) {
