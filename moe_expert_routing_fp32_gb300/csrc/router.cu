@@ -897,12 +897,19 @@ gate_split_kernel(const float *__restrict__ wg, int E, int H, uint16_t *__restri
 // Combine: one CTA per 32-token chunk.  All threads form the chunk's logits,
 // logit = (p1 + p2) + p3 (+ bias), coalesced over (token, expert); without
 // fuse_topk they go to `logits`.  With it (E <= 64) they stay in shared
-// memory and lane t of warp 0 takes token t's top-k by k argmax passes over
-// its row (ascending expert index, a later value wins only if strictly
-// larger, so equal logits go to the lower index), then its softmax weights
-// and the chunk's routing histogram.  (A warp-wide argmax per token spent
-// the kernel's time on shuffles.)
+// memory and a group of 8 lanes takes each token's top-k: per slot every
+// lane finds the best untaken expert among its eighth of the row, three
+// shuffles pick the group's best (larger logit, equal logits to the lower
+// index), then the softmax weights and the chunk's routing histogram.  (One
+// lane per token left 7 of 8 warps waiting at the barrier; a warp-wide
+// argmax per token spent the time on shuffles.)
 constexpr int GC_THREADS = 256;
+
+__device__ __forceinline__ bool better_sel(float va, int ia, float vb, int ib) {
+    if (ia < 0) return false;
+    if (ib < 0) return true;
+    return va > vb || (va == vb && ia < ib);
+}
 
 __global__ void __launch_bounds__(GC_THREADS)
 gate_combine_kernel(const float *__restrict__ parts, int NW, int T, int E,
@@ -910,7 +917,6 @@ gate_combine_kernel(const float *__restrict__ parts, int NW, int T, int E,
                     int fuse_topk, int k, int renorm, int32_t *__restrict__ topk_idx,
                     float *__restrict__ topk_w, int32_t *__restrict__ hist) {
     __shared__ float s_lg[RT_TOK][RT_EXP + 1];
-    __shared__ int s_sel[RT_TOK][33];
     __shared__ int s_cnt[RT_EXP];
     const int tok0 = blockIdx.x * RT_TOK;
     const int ntok = min(RT_TOK, T - tok0);
@@ -927,36 +933,59 @@ gate_combine_kernel(const float *__restrict__ parts, int NW, int T, int E,
     }
     if (!fuse_topk) return;
     __syncthreads();
-    if (threadIdx.x < RT_TOK && static_cast<int>(threadIdx.x) < ntok) {
-        const int t = threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int t = (threadIdx.x >> 5) * 4 + (lane >> 3);    // 8 warps x 4 tokens
+    const int sl = lane & 7;                                // this lane's experts: sl + 8i
+    if (t < ntok) {                                         // whole 8-lane groups agree
         const float *row = s_lg[t];
-        uint64_t taken = 0;
+        const unsigned gmask = 0xFFu << (lane & 24);
+        uint32_t taken = 0;                                 // bit i: expert sl + 8i
+        int sel = -1, sel0 = -1;
         for (int j = 0; j < k; ++j) {
             int bi = -1;
             float bv = -INFINITY;
-            for (int e = 0; e < E; ++e) {
+            for (int i = 0, e = sl; e < E; ++i, e += 8) {
                 const float v = row[e];
-                if (!((taken >> e) & 1ull) && (bi < 0 || v > bv)) {
+                if (!((taken >> i) & 1u) && (bi < 0 || v > bv)) {
                     bv = v;
                     bi = e;
                 }
             }
-            taken |= 1ull << bi;
-            s_sel[t][j] = bi;
+#pragma unroll
+            for (int off = 4; off > 0; off >>= 1) {
+                const float ov = __shfl_xor_sync(gmask, bv, off);
+                const int oi = __shfl_xor_sync(gmask, bi, off);
+                if (better_sel(ov, oi, bv, bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if ((bi & 7) == sl) taken |= 1u << (bi >> 3);
+            if (j == 0) sel0 = bi;
+            if ((j & 7) == sl) sel = bi;                    // lane sl keeps slots sl, sl+8, ...
+            if ((j & 7) == 7 || j == k - 1) {
+                // flush the (up to) 8 slots gathered so far
+                const int j0 = j & ~7;
+                if (j0 + sl <= j) {
+                    topk_idx[static_cast<size_t>(tok0 + t) * k + j0 + sl] = sel;
+                    atomicAdd(&s_cnt[sel], 1);
+                }
+            }
         }
-        const float m = row[s_sel[t][0]];
+        // softmax weights over the chosen slots (renorm) or over all experts
+        const float m = row[sel0];
         float den = 0.0f;
         if (renorm) {
-            for (int j = 0; j < k; ++j) den += expf(row[s_sel[t][j]] - m);
+            for (int j = sl; j < k; j += 8)
+                den += expf(row[topk_idx[static_cast<size_t>(tok0 + t) * k + j]] - m);
         } else {
-            for (int e = 0; e < E; ++e) den += expf(row[e] - m);
+            for (int e = sl; e < E; e += 8) den += expf(row[e] - m);
         }
-        const size_t a0 = static_cast<size_t>(tok0 + t) * k;
-        for (int j = 0; j < k; ++j) {
-            const int e = s_sel[t][j];
-            topk_idx[a0 + j] = e;
-            topk_w[a0 + j] = expf(row[e] - m) / den;
-            atomicAdd(&s_cnt[e], 1);
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1) den += __shfl_xor_sync(gmask, den, off);
+        for (int j = sl; j < k; j += 8) {
+            const int e = topk_idx[static_cast<size_t>(tok0 + t) * k + j];
+            topk_w[static_cast<size_t>(tok0 + t) * k + j] = expf(row[e] - m) / den;
         }
     }
     if (hist) {

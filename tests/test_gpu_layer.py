@@ -90,6 +90,10 @@ SMALL = [
              gamma_std=0.1),
     # E > 64: separate top-k and histogram launches
     Workload("mid-wideE", T=640, H=128, E=80, k=5, I=128),
+    # the fused top-k of the tensor-core gate with more than 8 slots, softmax
+    # over all experts (no renorm), and gate offsets
+    Workload("mid-k12", T=600, H=256, E=48, k=12, I=128, renorm=False, skew_s=1.2,
+             skew_beta=0.5),
     # the limits: 1024 experts (most of them empty), 32 slots per token
     Workload("max-Ek", T=200, H=128, E=1024, k=32, I=128, I_s=128, rmsnorm=True),
 ]
