@@ -69,6 +69,25 @@ def test_invalid_arguments_rejected_on_host(L):
                               fake, n.value - 1, None, None) == 3
     # finalize: H % 8
     assert L.moe_finalize_routing(fake, fake, fake, None, 4, 12, 2, 0, fake, None) == 2
+    # tensor-core gate: H % 128, E <= 1024, workspace size, alignment
+    assert L.moe_gate_tensor_workspace_size(4, 192, 8, ctypes.byref(n)) == 2
+    assert L.moe_gate_tensor_workspace_size(4, 128, 2000, ctypes.byref(n)) == 2
+    assert L.moe_gate_tensor_workspace_size(600, 256, 16, ctypes.byref(n)) == 0
+    # the split weight [128, 256] bf16, then the partial logits [600, 128] fp32
+    assert n.value == 128 * 256 * 2 + 600 * 128 * 4
+    assert L.moe_gate_tensor(fake, fake, None, 600, 256, 16, fake, fake, n.value - 1, None,
+                             None) == 3
+    assert L.moe_gate_tensor(P(0x1002), fake, None, 600, 256, 16, fake, fake, n.value, None,
+                             None) == 1
+    assert L.moe_gate_tensor(fake, fake, None, 600, 256, 16, None, fake, n.value, None,
+                             None) == 1
+    # the RMSNorm-only form of moe_rmsnorm_gate: H % 128, xn and the flag required
+    assert L.moe_rmsnorm_gate(fake, None, None, None, 4, 192, 1, 1e-6, moe.RMSNORM, fake, None,
+                              None) == 2
+    assert L.moe_rmsnorm_gate(fake, None, None, None, 4, 256, 1, 1e-6, moe.RMSNORM, None, None,
+                              None) == 1
+    assert L.moe_rmsnorm_gate(fake, None, None, None, 4, 256, 1, 1e-6, 0, fake, None,
+                              None) == 1
 
 
 def test_layer_desc_checks(L):
@@ -79,8 +98,8 @@ def test_layer_desc_checks(L):
     assert L.moe_layer_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 2
     d = moe.make_desc(T=16, H=128, E=8, k=2, I=128, I_shared=128, rmsnorm=True)
     assert L.moe_layer_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
-    # xn + idx + w + row_idx + act + y + act_s + y_s (+ hist, counts, offsets, and
-    # either the token map of the gathering GEMM or expanded_x)
+    # xn + idx + w + row_idx + act + y + act_s + y_s (+ hist, counts, offsets and
+    # expanded_x)
     assert n.value >= 16 * 128 * 2 + 3 * 32 * 4 + 32 * 128 * 2 * 2 + 16 * 128 * 6
     P = ctypes.c_void_p
     fake = P(0x1000)
