@@ -112,7 +112,8 @@ moe_status_t moe_rmsnorm_gate(const moe_bf16_t *x, const moe_bf16_t *gamma,
 /*
  * The same fp32 gate on the tensor cores ("消除gate计算冗余cast算子": an fp32
  * linear layer).  Every fp32 weight is split exactly into three bf16 parts,
- * wg = w1 + w2 + w3; each product of a bf16 xs value with a part is exact,
+ * wg = w1 + w2 + w3 (exact for |wg| >= 2^-110, within 2^-134 below); each
+ * product of a bf16 xs value with a part is exact,
  * the grouped GEMM accumulates the three partial dot products in fp32 and a
  * combine kernel adds them, (p1 + p2) + p3, plus gate_bias[e].  The logits
  * are fp32-accurate but summed in another order than moe_rmsnorm_gate's, so

@@ -861,8 +861,9 @@ rmsnorm_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamm
 // The gate on the tensor cores at fp32 accuracy: each fp32 weight splits
 // exactly into three bf16 parts, w = w1 + w2 + w3 (w1 = bf16(w), w2 =
 // bf16(w - w1), w3 = bf16(w - w1 - w2); the two differences are exact in
-// fp32 and the last part holds the remaining bits), and every product of a
-// bf16 xn value with a part is exact.  The grouped GEMM computes the three
+// fp32 and the last part holds the remaining bits -- for |w| >= 2^-110;
+// closer to fp32's underflow the parts are within 2^-134 of w), and every
+// product of a bf16 xn value with a part is exact.  The grouped GEMM computes the three
 // partial dot products as separate output columns (fp32 accumulation in the
 // tensor core) and the combine kernel adds them: logit = (p1 + p2) + p3.
 // The sum is fp32-accurate but not in the sequential order of the plain
