@@ -10,6 +10,11 @@ The layer follows "NPU HunyuanImage-3.0模型推理优化实践" (HunyuanImage-3
 block: RMSNorm, fp32 gate, GatingTopK, init_routing, compute_expert_tokens,
 grouped matmul with SwiGLU on the merged w13 weight, down projection,
 finalize_routing, shared expert).  See include/moe.h for the contracts.
+
+Two fp32 gates: ``rmsnorm_gate`` sums each logit sequentially (the oracle's
+order, bit for bit); ``gate_tensor`` sums the same exact products on the
+tensor cores (the weight split exactly into three bf16 parts), which the
+layer uses above 512 tokens unless ``make_desc(..., gate_sequential=True)``.
 """
 from __future__ import annotations
 
