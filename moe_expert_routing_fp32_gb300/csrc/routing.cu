@@ -202,7 +202,7 @@ permute_kernel(const uint16_t *__restrict__ xs, const int32_t *__restrict__ row_
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int v = v0 + u * blockDim.x + threadIdx.x;
-                    if (v < nvec) dst[v] = q[u];
+                    if (v < nvec) __stcs(dst + v, q[u]);   // streamed: read once, later
                 }
             }
         }
