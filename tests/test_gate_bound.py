@@ -18,7 +18,9 @@ of the CUDA code:
 import numpy as np
 
 import oracle
-from tests._helpers import bf16_to_f64, gate_tc_bound
+import pytest
+
+from tests._helpers import bf16_to_f64, gate_tc_bound, routing_flips
 
 
 def _bf16_rne(a):
@@ -104,3 +106,22 @@ def test_bound_covers_a_blocked_fp32_sum_and_catches_a_dropped_part():
     lg_bad = ((acc[0] + acc[2]).astype(np.float32) + bias).astype(np.float32)
     d_bad = np.abs(lg_bad.astype(np.float64) - lg_ref.astype(np.float64))
     assert float(np.sqrt(np.mean(d_bad * d_bad))) > rms_b
+
+
+def test_routing_check_accepts_near_ties_and_rejects_wrong_choices():
+    """routing_flips, the GPU tests' routing check, planted on CPU: a swap
+    within the bound of a tie passes (reported as a flip), a clearly worse
+    expert or a wrong slot order does not."""
+    lg = np.array([[3.0, 2.0, 1.0000001, 1.0, -1.0],
+                   [5.0, 4.0, 3.0, 2.0, 1.0]], dtype=np.float32)
+    per = np.full(lg.shape, 1e-6)
+    ref = np.array([[0, 1, 2], [0, 1, 2]], dtype=np.int32)
+    assert len(routing_flips(ref, ref, lg, per)) == 0
+    near = np.array([[0, 1, 3], [0, 1, 2]], dtype=np.int32)     # 1.0 vs 1.0000001: a near-tie
+    assert list(routing_flips(near, ref, lg, per)) == [0]
+    with pytest.raises(AssertionError):
+        routing_flips(np.array([[0, 1, 4], [0, 1, 2]], dtype=np.int32), ref, lg, per)
+    with pytest.raises(AssertionError):                            # slot order not descending
+        routing_flips(np.array([[0, 1, 2], [1, 0, 2]], dtype=np.int32), ref, lg, per)
+    with pytest.raises(AssertionError):                            # an expert twice
+        routing_flips(np.array([[0, 1, 1], [0, 1, 2]], dtype=np.int32), ref, lg, per)
