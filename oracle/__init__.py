@@ -60,7 +60,7 @@ def _bind(lib):
         "oracle_grouped_mlp": [P, P, I64, P, P, I64, I64, P, P],
         "oracle_finalize": [P, P, P, P, I64, I64, I64, P],
         "oracle_layer_tokens": [P, I64, I64, I64, I64, I64, I64, INT, F, INT,
-                                P, P, P, P, P, P, P, P, I64, P, P, P],
+                                P, P, P, P, P, P, P, P, I64, P, P, P, P],
         "oracle_local_rerouting": [P, P, I64, I64, I64, I64, P, P, P, P],
         "oracle_local_finalize_rerouting": [P, P, I64, I64, P],
     }
@@ -267,10 +267,11 @@ def finalize(y_exp, row_idx, topk_w, shared=None):
     return out
 
 
-def layer_tokens(inputs: dict, wl, tokens=None):
+def layer_tokens(inputs: dict, wl, tokens=None, routed_rows=False):
     """Whole layer for ``tokens`` (default: all).  ``inputs`` is the dict made
     by moe_inputs.make_inputs; ``wl`` the Workload.  Returns (out f64 [n,H],
-    topk_idx [n,k], topk_w [n,k])."""
+    topk_idx [n,k], topk_w [n,k]), and with ``routed_rows`` also each slot's
+    routed expert output as bf16 bits [n,k,H]."""
     x = _u16(inputs["x"])
     T, H = x.shape
     E, k, I, I_s = wl.E, wl.k, wl.I, wl.I_s
@@ -279,6 +280,7 @@ def layer_tokens(inputs: dict, wl, tokens=None):
     out = np.empty((n, H), dtype=np.float64)
     idx = np.empty((n, k), dtype=np.int32)
     w = np.empty((n, k), dtype=np.float32)
+    y = np.empty((n, k, H), dtype=np.uint16) if routed_rows else None
     gamma = _u16(inputs.get("gamma"))
     wg = _arr(inputs["wg"], np.float32)
     bias = _arr(inputs.get("gate_bias"), np.float32)
@@ -289,9 +291,9 @@ def layer_tokens(inputs: dict, wl, tokens=None):
     rc = _load().oracle_layer_tokens(
         _p(x), T, H, E, k, I, I_s, int(wl.rmsnorm), ctypes.c_float(wl.eps),
         int(wl.renorm), _p(gamma), _p(wg), _p(bias), _p(w13), _p(w2), _p(w13_s),
-        _p(w2_s), _p(tok), 0 if tok is None else tok.size, _p(out), _p(idx), _p(w))
+        _p(w2_s), _p(tok), 0 if tok is None else tok.size, _p(out), _p(idx), _p(w), _p(y))
     _check(rc, "oracle_layer_tokens")
-    return out, idx, w
+    return (out, idx, w, y) if routed_rows else (out, idx, w)
 
 
 # ------------------------------------------------------------ EP local steps

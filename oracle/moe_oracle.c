@@ -372,13 +372,15 @@ int oracle_finalize(const bf16_t *y_exp, const int32_t *row_idx, const float *to
 /*   wg [E,H] fp32; bias [E] or NULL; w13 [E,2I,H]; w2 [E,H,I];             */
 /*   w13_s [2I_s,H], w2_s [H,I_s] or NULL (no shared expert);               */
 /*   tokens [n_tok] (NULL = 0..T-1, n_tok = T).                             */
-/* Outputs: out [n_tok,H] double; idx/w [n_tok,k] (may be NULL).             */
+/* Outputs: out [n_tok,H] double; idx/w [n_tok,k] (may be NULL);            */
+/*   y_out [n_tok,k,H] bf16 (may be NULL): each slot's routed expert output,  */
+/*   as it enters the weighted sum.                                           */
 int oracle_layer_tokens(const bf16_t *x, int64_t T, int64_t H, int64_t E, int64_t k,
                         int64_t I, int64_t I_s, int rmsnorm, float eps, int renorm,
                         const bf16_t *gamma, const float *wg, const float *bias,
                         const bf16_t *w13, const bf16_t *w2, const bf16_t *w13_s,
                         const bf16_t *w2_s, const int32_t *tokens, int64_t n_tok,
-                        double *out, int32_t *idx_out, float *w_out)
+                        double *out, int32_t *idx_out, float *w_out, bf16_t *y_out)
 {
     if (!x || !wg || !w13 || !w2 || !out || H <= 0 || E <= 0 || k < 1 || k > E ||
         I <= 0 || I_s < 0 || (I_s > 0 && (!w13_s || !w2_s)))
@@ -420,6 +422,8 @@ int oracle_layer_tokens(const bf16_t *x, int64_t T, int64_t H, int64_t E, int64_
             if ((rc = oracle_expert_mlp(xrow, 1, w13 + e * 2 * I * H, w2 + e * H * I,
                                         H, I, NULL, yb, NULL)))
                 goto done;
+            if (y_out)
+                memcpy(y_out + (n * k + j) * H, yb, (size_t)H * sizeof(bf16_t));
             for (int64_t c = 0; c < H; ++c)
                 o[c] += (double)w[j] * (double)bf16_to_float(yb[c]);
         }

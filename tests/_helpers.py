@@ -3,7 +3,8 @@
 Tolerances (layer outputs): the fp32 output mode must be within max-abs 2e-2
 and relative-L2 5e-3 of the oracle's double result; the bf16 output mode may
 in addition be off by half a bf16 ulp of the oracle value (its own final
-rounding).  act / y_exp (bf16 intermediates) may differ from the oracle by
+rounding).  Where the test has the oracle's routed rows, a rare element may
+also be off by one bf16 ulp of each routed term (routed_flip_allowance).  act / y_exp (bf16 intermediates) may differ from the oracle by
 one bf16 ulp where the fp32 tensor-core sum and the oracle's exact sum round
 to neighbouring bf16 values; such flips must stay rare.  Near zero (after
 cancellation in the sum) the fp32 accumulation error is absolute, not
@@ -42,17 +43,38 @@ def bf16_ulp(v: np.ndarray) -> np.ndarray:
     return 2.0 ** (np.floor(np.log2(a)) - 7)
 
 
-def check_out(gpu: np.ndarray, ref: np.ndarray, bf16_out: bool, what=""):
-    """Assert the layer-output tolerance; returns (max_abs, rel_l2)."""
+def routed_flip_allowance(y_bits, w):
+    """Per output element, sum_j |w_j| * ulp_bf16(y_j): what one-ulp flips of
+    the routed bf16 expert outputs y_j (the oracle's, [n, k, H] bits) can move
+    the weighted sum by.  The GPU rounds its fp32 sum of each y to bf16 as the
+    oracle rounds its exact sum; where the two straddle a rounding boundary
+    they land one bf16 ulp apart (0.031 for |y| in [4, 8))."""
+    y = bf16_to_f64(y_bits)
+    return np.einsum("nk,nkh->nh", np.abs(np.asarray(w, dtype=np.float64)), bf16_ulp(y))
+
+
+# elements allowed past MAX_ABS by routed one-ulp flips: must stay this rare
+FLIP_FRAC = 1e-4
+
+
+def check_out(gpu: np.ndarray, ref: np.ndarray, bf16_out: bool, what="", flip_allowance=None):
+    """Assert the layer-output tolerance; returns (max_abs, rel_l2).  With
+    ``flip_allowance`` (routed_flip_allowance of the oracle's rows) an element
+    may exceed max-abs by at most that much, on at most FLIP_FRAC of the
+    elements: a one-ulp flip of a bf16 routed output with a weight near 1 at
+    |y| >= 4 moves the output by more than 2e-2 on its own."""
     d = np.abs(gpu - ref)
     rel = float(np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-30))
     mx = float(d.max()) if d.size else 0.0
-    if bf16_out:
-        bound = MAX_ABS + 0.5 * bf16_ulp(ref)
-        bad = d > bound
-        assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond 2e-2 + ulp/2, max {mx}"
+    bound = MAX_ABS + (0.5 * bf16_ulp(ref) if bf16_out else 0.0)
+    over = d > bound
+    if flip_allowance is not None and over.any():
+        assert not (d > bound + flip_allowance).any(), (
+            f"{what}: elements beyond 2e-2 plus one bf16 ulp of every routed term, max {mx}")
+        assert over.mean() <= FLIP_FRAC, f"{what}: {int(over.sum())} elements past 2e-2"
     else:
-        assert mx <= MAX_ABS, f"{what}: max-abs {mx} > {MAX_ABS}"
+        assert not over.any(), (f"{what}: {int(over.sum())} elements beyond 2e-2"
+                                f"{' + ulp/2' if bf16_out else ''}, max {mx}")
     assert rel <= REL_L2, f"{what}: rel-L2 {rel} > {REL_L2}"
     return mx, rel
 
