@@ -96,6 +96,10 @@ SMALL = [
              skew_beta=0.5),
     # the limits: 1024 experts (most of them empty), 32 slots per token
     Workload("max-Ek", T=200, H=128, E=1024, k=32, I=128, I_s=128, rmsnorm=True),
+    # either side of the gate switch (512 tokens: sequential; 513: tensor cores, with
+    # 65 experts the combine writes logits for the separate top-k)
+    Workload("edge-512", T=512, H=128, E=65, k=3, I=128, rmsnorm=True, gamma_std=0.1),
+    Workload("edge-513", T=513, H=128, E=65, k=3, I=128, rmsnorm=True, gamma_std=0.1),
 ]
 
 
