@@ -420,21 +420,21 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
 // Few tokens (T <= 512): one CTA per token and one thread per expert, so
 // that every logit's sequential FMA chain runs at the same time.  The row is
 // kept in shared memory as fp32; thread 0 takes the sum of squares in
-// ascending h; the gate weight streams through a SLOTS-deep cp.async ring
-// in 64-column chunks (rows padded to 68 floats: conflict-free 16-byte
-// reads), filled while the sum of squares runs.  Every CTA streams the whole
-// gate weight from L2: a chunk arrives as two TMA tensor boxes (E rows x 32
-// fp32 columns, 128-byte swizzle: 16-byte piece q of row e sits at piece
-// q ^ (e & 7)) completed on the slot's mbarrier, which keeps far more bytes
-// in flight per SM than per-thread 16-byte copies.  With at most one CTA per
-// SM the ring is as deep as shared memory allows (11 chunks in flight); with
-// more tokens it is sized for two CTAs per SM.
+// ascending h; the gate weight streams through a SLOTS-deep ring of chunks
+// of NB*32 columns, filled while the sum of squares runs.  Every CTA streams
+// the whole gate weight from L2: a chunk arrives as NB TMA tensor boxes
+// (E rows x 32 fp32 columns, 128-byte swizzle: 16-byte piece q of row e sits
+// at piece q ^ (e & 7), so the 32 lanes' reads of one piece are
+// conflict-free) completed on the slot's mbarrier.  With at most one CTA per
+// SM the ring is as deep as shared memory allows, in 128-column chunks when
+// H allows (one barrier test and one release per 128 FMAs of each chain);
+// with more tokens it is sized for two CTAs per SM.
 // Same arithmetic, in the same order, as the tiled kernel above.
-constexpr int SM_HC = 64;
+constexpr int SM_BOX = 32;    // columns of one tensor box
 constexpr int SM_SMEM_CAP = 220 * 1024;
-// bytes of one 32-column half of a ring slot: E rows of 128 bytes, rounded to
-// whole 1 KB swizzle atoms
-__host__ __device__ inline int sm_half_bytes(int E) { return ((E + 7) / 8) * 1024; }
+// bytes of one box of a ring slot: E rows of 128 bytes, rounded to whole
+// 1 KB swizzle atoms
+__host__ __device__ inline int sm_box_bytes(int E) { return ((E + 7) / 8) * 1024; }
 constexpr int SMALL_MAX_T = kGateSmallMaxT;
 constexpr int SMALL_MAX_E = 128;
 constexpr int SMALL_MAX_H = 8192;
@@ -447,7 +447,7 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // up to 32)); the warp after them only streams the gate weight: it refills a
 // slot once every consumer warp has arrived on the slot's empty barrier, so
 // the consumers' FMA chains never stop at a block-wide barrier.
-template <int SLOTS>
+template <int SLOTS, int NB>
 __global__ void __launch_bounds__(160)
 router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
                     const float *__restrict__ wg, const float *__restrict__ gate_bias, int H,
@@ -456,10 +456,13 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
                     int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
                     int32_t *dev_status, const __grid_constant__ CUtensorMap tmw) {
     extern __shared__ uint8_t sm_raw[];
-    uint8_t *ring = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int hb = sm_half_bytes(E);   // ring: [SLOTS][2 halves][hb]
-    float *xf = reinterpret_cast<float *>(ring + SLOTS * 2 * hb);   // [H]
+    // 1 KB aligned for the swizzled boxes; offsetting the shared pointer (not
+    // an integer copy of it) keeps the loads below in the shared window
+    uint8_t *ring = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
+    static_assert(NB >= 2 && NB % 2 == 0, "boxes are consumed in pairs");
+    constexpr int HC = NB * SM_BOX;    // columns of one chunk
+    const int hb = sm_box_bytes(E);   // ring: [SLOTS][NB boxes][hb]
+    float *xf = reinterpret_cast<float *>(ring + SLOTS * NB * hb);   // [H]
     __shared__ float s_r;
     __shared__ float s_lg[SMALL_MAX_E];
     __shared__ __align__(8) uint64_t s_full[SLOTS];
@@ -470,7 +473,7 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
     const int tid = threadIdx.x;
     const int nc = blockDim.x - 32;      // consumer threads
     const int nvec = H / 8;
-    const int nch = H / SM_HC;
+    const int nch = H / HC;
 
     if (tid == 0) {
         *s_abort = 0;
@@ -492,10 +495,11 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
                     !mbar_wait_bounded(&s_empty[st], static_cast<uint32_t>((c / SLOTS - 1) & 1),
                                        s_abort, dev_status))
                     break;
-                mbar_arrive_expect_tx(&s_full[st], static_cast<uint32_t>(E) * SM_HC * 4);
-                uint8_t *slot = ring + st * 2 * hb;
-                tma_load_2d(slot, &tmw, &s_full[st], c * SM_HC, 0);
-                tma_load_2d(slot + hb, &tmw, &s_full[st], c * SM_HC + SM_HC / 2, 0);
+                mbar_arrive_expect_tx(&s_full[st], static_cast<uint32_t>(E) * HC * 4);
+                uint8_t *slot = ring + st * NB * hb;
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+                    tma_load_2d(slot + b * hb, &tmw, &s_full[st], c * HC + b * SM_BOX, 0);
                 issued = c + 1;
             }
             if (*s_abort) {
@@ -525,27 +529,60 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
     consumer_sync(nc);
 
     if (rmsnorm) {
+        // the other consumers fetch their gamma groups while thread 0 runs
+        // the chain (nvec <= SMALL_MAX_H / 8, nc >= 64: at most 16 each)
+        constexpr int GQ = SMALL_MAX_H / 8 / 64;
+        uint4 gqs[GQ];
+#pragma unroll
+        for (int j = 0; j < GQ; ++j) {
+            const int v = tid + j * nc;
+            gqs[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (gamma && tid != 0 && v < nvec)
+                gqs[j] = __ldg(reinterpret_cast<const uint4 *>(gamma) + v);
+        }
         if (tid == 0) {
-            // one sequential chain, fed by 16-byte shared loads
+            // one sequential chain; its operands are read into registers 32
+            // values ahead (H is a multiple of 64)
             float ss = 0.0f;
             const float4 *xv = reinterpret_cast<const float4 *>(xf);
-#pragma unroll 8
-            for (int b = 0; b < H / 4; ++b) {
-                const float4 q = xv[b];
-                ss = __fmaf_rn(q.x, q.x, ss);
-                ss = __fmaf_rn(q.y, q.y, ss);
-                ss = __fmaf_rn(q.z, q.z, ss);
-                ss = __fmaf_rn(q.w, q.w, ss);
+            float4 qa[8], qb[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) qa[i] = xv[i];
+            for (int b = 0; b < H / 4; b += 16) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) qb[i] = xv[b + 8 + i];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    ss = __fmaf_rn(qa[i].x, qa[i].x, ss);
+                    ss = __fmaf_rn(qa[i].y, qa[i].y, ss);
+                    ss = __fmaf_rn(qa[i].z, qa[i].z, ss);
+                    ss = __fmaf_rn(qa[i].w, qa[i].w, ss);
+                }
+                if (b + 16 < H / 4) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) qa[i] = xv[b + 16 + i];
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    ss = __fmaf_rn(qb[i].x, qb[i].x, ss);
+                    ss = __fmaf_rn(qb[i].y, qb[i].y, ss);
+                    ss = __fmaf_rn(qb[i].z, qb[i].z, ss);
+                    ss = __fmaf_rn(qb[i].w, qb[i].w, ss);
+                }
             }
             const float mean = __fdiv_rn(ss, static_cast<float>(H));
             s_r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
         }
         consumer_sync(nc);
         const float r = s_r;
-        for (int v = tid; v < nvec; v += nc) {
+#pragma unroll
+        for (int j = 0; j < GQ; ++j) {
+            const int v = tid + j * nc;
+            if (v >= nvec) break;
             float gm[8];
             if (gamma) {
-                const uint4 gq = reinterpret_cast<const uint4 *>(gamma)[v];
+                const uint4 gq =
+                    tid != 0 ? gqs[j] : __ldg(reinterpret_cast<const uint4 *>(gamma) + v);
                 const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -573,25 +610,26 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
     }
 
     // The logit's FMA chain is the critical path: its operands are read into
-    // registers half a chunk (32 columns) ahead, so the chain never waits on
-    // shared memory.  A warp releases a slot (empty barrier) once its loads
-    // of the slot's second half are issued.
+    // registers one box (32 columns) ahead, so the chain never waits on
+    // shared memory, and neither on the full barriers while the ring is ahead
+    // (their test overlaps the FMAs).  A warp releases a slot (empty barrier)
+    // once its loads of the slot's last box have landed.
     const int e = tid;
     const int lane = tid & 31;
     const int er = e < E ? e : 0;             // threads past E follow along on row 0
-    constexpr int HQ = SM_HC / 8;             // float4s per half chunk
+    constexpr int HQ = SM_BOX / 4;            // float4s per box row
     float acc = 0.0f;
     float4 wa[HQ], xa[HQ], wb[HQ], xb[HQ];
-    auto load_half = [&](int c, int half, float4 (&w)[HQ], float4 (&xv)[HQ]) {
-        const uint8_t *wr = ring + ((c % SLOTS) * 2 + half) * hb + er * 128;
-        const float *xc = xf + c * SM_HC + half * (SM_HC / 2);
+    auto load_box = [&](int c, int b, float4 (&w)[HQ], float4 (&xv)[HQ]) {
+        const uint8_t *wr = ring + ((c % SLOTS) * NB + b) * hb + er * 128;
+        const float *xc = xf + c * HC + b * SM_BOX;
 #pragma unroll
         for (int q = 0; q < HQ; ++q) {
             w[q] = *reinterpret_cast<const float4 *>(wr + ((q ^ (er & 7)) << 4));
             xv[q] = *reinterpret_cast<const float4 *>(xc + 4 * q);
         }
     };
-    auto fma_half = [&](const float4 (&w)[HQ], const float4 (&xv)[HQ]) {
+    auto fma_box = [&](const float4 (&w)[HQ], const float4 (&xv)[HQ]) {
 #pragma unroll
         for (int q = 0; q < HQ; ++q) {
             acc = __fmaf_rn(xv[q].x, w[q].x, acc);
@@ -605,17 +643,33 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
                           dev_status);
     };
     wait_chunk(0);
-    load_half(0, 0, wa, xa);
+    load_box(0, 0, wa, xa);
     for (int c = 0; c < nch; ++c) {
-        load_half(c, 1, wb, xb);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[c % SLOTS]);
-        fma_half(wa, xa);
-        if (c + 1 < nch) {
-            wait_chunk(c + 1);
-            load_half(c + 1, 0, wa, xa);
+        const bool more = c + 1 < nch;
+#pragma unroll
+        for (int j = 0; j < NB; j += 2) {
+            // box j is in (wa, xa); box j + 1 goes to (wb, xb)
+            load_box(c, j + 1, wb, xb);
+            if (j + 2 < NB) {
+                fma_box(wa, xa);
+                load_box(c, j + 2, wa, xa);
+                fma_box(wb, xb);
+                continue;
+            }
+            // the test of the next chunk's barrier is in flight while box j's
+            // FMAs issue; the release of slot c follows them, when the loads
+            // of its last box have landed
+            const bool ready = !more || mbar_try_wait(&s_full[(c + 1) % SLOTS],
+                                                      static_cast<uint32_t>(((c + 1) / SLOTS) & 1));
+            fma_box(wa, xa);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[c % SLOTS]);
+            if (more) {
+                if (!ready) wait_chunk(c + 1);
+                load_box(c + 1, 0, wa, xa);
+            }
+            fma_box(wb, xb);
         }
-        fma_half(wb, xb);
     }
     if (e < E) {
         if (gate_bias) acc = __fadd_rn(acc, gate_bias[e]);
@@ -1016,7 +1070,7 @@ bool make_wg_map(CUtensorMap *m, const float *wg, int H, int E) {
     if (!fn) return false;
     cuuint64_t gdim[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(E)};
     cuuint64_t gstride[1] = {static_cast<cuuint64_t>(H) * 4};
-    cuuint32_t box[2] = {SM_HC / 2, static_cast<cuuint32_t>(E)};
+    cuuint32_t box[2] = {SM_BOX, static_cast<cuuint32_t>(E)};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(wg), gdim, gstride, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1035,12 +1089,12 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
         const int threads = std::max(64, static_cast<int>(ceil_div(E, 32)) * 32) + 32;
         CUtensorMap tmw;
         if (!make_wg_map(&tmw, wg, H, E)) return cudaErrorInvalidValue;
-        auto smem_for = [&](int slots) {
-            return 1024 + static_cast<size_t>(slots) * 2 * sm_half_bytes(E) +
+        auto smem_for = [&](int slots, int nb) {
+            return 1024 + static_cast<size_t>(slots) * nb * sm_box_bytes(E) +
                    static_cast<size_t>(H) * sizeof(float);
         };
-        auto run = [&](auto kernel, int slots) -> cudaError_t {
-            const size_t smem = smem_for(slots);
+        auto run = [&](auto kernel, int slots, int nb) -> cudaError_t {
+            const size_t smem = smem_for(slots, nb);
             if (smem > 48 * 1024) {
                 cudaError_t e = cudaFuncSetAttribute(
                     kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -1055,12 +1109,14 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
         // up to one CTA per SM: the deepest ring that fits; more tokens than
         // SMs: a ring that lets two CTAs share an SM
         cudaError_t le;
-        if (T <= num_sms() && smem_for(12) <= SM_SMEM_CAP)
-            le = run(router_small_kernel<12>, 12);
-        else if (smem_for(5) <= SM_SMEM_CAP / 2)
-            le = run(router_small_kernel<5>, 5);
+        if (T <= num_sms() && H % (4 * SM_BOX) == 0 && smem_for(6, 4) <= SM_SMEM_CAP)
+            le = run(router_small_kernel<6, 4>, 6, 4);
+        else if (T <= num_sms() && smem_for(12, 2) <= SM_SMEM_CAP)
+            le = run(router_small_kernel<12, 2>, 12, 2);
+        else if (smem_for(5, 2) <= SM_SMEM_CAP / 2)
+            le = run(router_small_kernel<5, 2>, 5, 2);
         else
-            le = run(router_small_kernel<3>, 3);
+            le = run(router_small_kernel<3, 2>, 3, 2);
         if (le != cudaSuccess) return le;
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess || !fuse_topk || hist == nullptr) return e;

@@ -28,9 +28,11 @@ def _cuda(d):
     Workload("g-rms", T=77, H=320, E=13, k=3, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-bias", T=100, H=256, E=64, k=8, I=128, rmsnorm=True, skew_s=1.2, skew_beta=1.0),
     Workload("g-wideE", T=40, H=192, E=160, k=6, I=128, rmsnorm=True),
-    # the small-batch router's ring depths: 12 slots with refills (T <= SMs),
-    # 5 slots (T > SMs), 3 slots (E=128 at the largest H), one chunk (H=64)
+    # the small-batch router's rings: 6 slots of 128 columns with refills
+    # (T <= SMs), 12 slots of 64 columns with refills (H not a multiple of
+    # 128), 5 slots (T > SMs), 3 slots (E=128 at the largest H), one chunk
     Workload("g-small-deep", T=100, H=1024, E=64, k=8, I=128, rmsnorm=True, gamma_std=0.1),
+    Workload("g-small-h64", T=50, H=1088, E=40, k=4, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-small-2cta", T=300, H=512, E=32, k=4, I=128, rmsnorm=True),
     Workload("g-small-maxH", T=24, H=8192, E=128, k=8, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-small-1chunk", T=5, H=64, E=6, k=2, I=128),
