@@ -446,12 +446,15 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // Threads [0, nc) are the consumers (one per expert, nc = max(64, E rounded
 // up to 32)); the warp after them only streams the gate weight: it refills a
 // slot once every consumer warp has arrived on the slot's empty barrier, so
-// the consumers' FMA chains never stop at a block-wide barrier.
-template <int SLOTS, int NB>
-__global__ void __launch_bounds__(160)
+// the consumers' FMA chains never stop at a block-wide barrier.  A CTA takes
+// TPC consecutive tokens: every consumer runs one chain per token on the
+// same weight operands, so the weight streams through the SM once per TPC
+// tokens.  MIN_CTAS = 2 caps the registers so that two CTAs share an SM.
+template <int SLOTS, int NB, int TPC, int MIN_CTAS = 1>
+__global__ void __launch_bounds__(160, MIN_CTAS)
 router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
-                    const float *__restrict__ wg, const float *__restrict__ gate_bias, int H,
-                    int E, float eps, int rmsnorm, uint16_t *__restrict__ xn,
+                    const float *__restrict__ wg, const float *__restrict__ gate_bias, int T,
+                    int H, int E, float eps, int rmsnorm, uint16_t *__restrict__ xn,
                     float *__restrict__ logits, int fuse_topk, int k, int renorm,
                     int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
                     int32_t *dev_status, const __grid_constant__ CUtensorMap tmw) {
@@ -460,16 +463,18 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
     // an integer copy of it) keeps the loads below in the shared window
     uint8_t *ring = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
     static_assert(NB >= 2 && NB % 2 == 0, "boxes are consumed in pairs");
+    static_assert(TPC >= 1 && TPC <= 2, "one chain-running warp per token among the first two");
     constexpr int HC = NB * SM_BOX;    // columns of one chunk
     const int hb = sm_box_bytes(E);   // ring: [SLOTS][NB boxes][hb]
-    float *xf = reinterpret_cast<float *>(ring + SLOTS * NB * hb);   // [H]
-    __shared__ float s_r;
-    __shared__ float s_lg[SMALL_MAX_E];
+    float *xf = reinterpret_cast<float *>(ring + SLOTS * NB * hb);   // [TPC][H]
+    __shared__ float s_r[TPC];
+    __shared__ float s_lg[TPC][SMALL_MAX_E];
     __shared__ __align__(8) uint64_t s_full[SLOTS];
     __shared__ __align__(8) uint64_t s_empty[SLOTS];
     __shared__ int s_abort_v;
     volatile int *s_abort = &s_abort_v;
-    const int t = blockIdx.x;
+    const int t0 = blockIdx.x * TPC;
+    const int ntok = min(TPC, T - t0);
     const int tid = threadIdx.x;
     const int nc = blockDim.x - 32;      // consumer threads
     const int nvec = H / 8;
@@ -512,39 +517,48 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
         return;
     }
 
-    // ---- consumers
-    const uint4 *xq = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
-    for (int v = tid; v < nvec; v += nc) {
-        const uint4 q = xq[v];
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-        float f[8];
+    // ---- consumers: the tokens' rows as fp32 (a missing last token repeats
+    // the CTA's first row; nothing of it is written)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    for (int tk = 0; tk < TPC; ++tk) {
+        const int t = tk < ntok ? t0 + tk : t0;
+        const uint4 *xq = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
+        float *xr = xf + tk * H;
+        for (int v = tid; v < nvec; v += nc) {
+            const uint4 q = xq[v];
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                f[2 * i] = __uint_as_float(w[i] << 16);
+                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+            *reinterpret_cast<float4 *>(xr + 8 * v) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4 *>(xr + 8 * v + 4) = make_float4(f[4], f[5], f[6], f[7]);
         }
-        *reinterpret_cast<float4 *>(xf + 8 * v) = make_float4(f[0], f[1], f[2], f[3]);
-        *reinterpret_cast<float4 *>(xf + 8 * v + 4) = make_float4(f[4], f[5], f[6], f[7]);
     }
     consumer_sync(nc);
 
     if (rmsnorm) {
-        // the other consumers fetch their gamma groups while thread 0 runs
-        // the chain (nvec <= SMALL_MAX_H / 8, nc >= 64: at most 16 each)
+        // lane 0 of warp tk runs token tk's chain; the other consumers fetch
+        // their gamma groups meanwhile (nvec <= SMALL_MAX_H / 8, nc >= 64: at
+        // most 16 each)
+        const bool chain = (tid & 31) == 0 && (tid >> 5) < TPC;
         constexpr int GQ = SMALL_MAX_H / 8 / 64;
         uint4 gqs[GQ];
 #pragma unroll
         for (int j = 0; j < GQ; ++j) {
             const int v = tid + j * nc;
             gqs[j] = make_uint4(0u, 0u, 0u, 0u);
-            if (gamma && tid != 0 && v < nvec)
+            if (gamma && !chain && v < nvec)
                 gqs[j] = __ldg(reinterpret_cast<const uint4 *>(gamma) + v);
         }
-        if (tid == 0) {
+        if (chain) {
             // one sequential chain; its operands are read into registers 32
             // values ahead (H is a multiple of 64)
+            const int tk = tid >> 5;
             float ss = 0.0f;
-            const float4 *xv = reinterpret_cast<const float4 *>(xf);
+            const float4 *xv = reinterpret_cast<const float4 *>(xf + tk * H);
             float4 qa[8], qb[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) qa[i] = xv[i];
@@ -571,10 +585,9 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
                 }
             }
             const float mean = __fdiv_rn(ss, static_cast<float>(H));
-            s_r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+            s_r[tk] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
         }
         consumer_sync(nc);
-        const float r = s_r;
 #pragma unroll
         for (int j = 0; j < GQ; ++j) {
             const int v = tid + j * nc;
@@ -582,7 +595,7 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
             float gm[8];
             if (gamma) {
                 const uint4 gq =
-                    tid != 0 ? gqs[j] : __ldg(reinterpret_cast<const uint4 *>(gamma) + v);
+                    !chain ? gqs[j] : __ldg(reinterpret_cast<const uint4 *>(gamma) + v);
                 const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -590,21 +603,26 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
                     gm[2 * i + 1] = __uint_as_float(gw[i] & 0xFFFF0000u);
                 }
             }
-            uint32_t packed[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float val = __fmul_rn(xf[8 * v + i], r);
-                if (gamma) val = __fmul_rn(val, gm[i]);
-                const uint16_t b = float_to_bf16_bits(val);
-                xf[8 * v + i] = bf16_bits_to_float(b);
-                if (i & 1)
-                    packed[i >> 1] |= static_cast<uint32_t>(b) << 16;
-                else
-                    packed[i >> 1] = b;
+            for (int tk = 0; tk < TPC; ++tk) {
+                const float r = s_r[tk];
+                float *xr = xf + tk * H;
+                uint32_t packed[4];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float val = __fmul_rn(xr[8 * v + i], r);
+                    if (gamma) val = __fmul_rn(val, gm[i]);
+                    const uint16_t b = float_to_bf16_bits(val);
+                    xr[8 * v + i] = bf16_bits_to_float(b);
+                    if (i & 1)
+                        packed[i >> 1] |= static_cast<uint32_t>(b) << 16;
+                    else
+                        packed[i >> 1] = b;
+                }
+                if (xn && tk < ntok)
+                    reinterpret_cast<uint4 *>(xn + static_cast<size_t>(t0 + tk) * H)[v] =
+                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }
-            if (xn)
-                reinterpret_cast<uint4 *>(xn + static_cast<size_t>(t) * H)[v] =
-                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
         consumer_sync(nc);
     }
@@ -618,24 +636,31 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
     const int lane = tid & 31;
     const int er = e < E ? e : 0;             // threads past E follow along on row 0
     constexpr int HQ = SM_BOX / 4;            // float4s per box row
-    float acc = 0.0f;
-    float4 wa[HQ], xa[HQ], wb[HQ], xb[HQ];
-    auto load_box = [&](int c, int b, float4 (&w)[HQ], float4 (&xv)[HQ]) {
+    float acc[TPC];
+#pragma unroll
+    for (int tk = 0; tk < TPC; ++tk) acc[tk] = 0.0f;
+    float4 wa[HQ], xa[TPC][HQ], wb[HQ], xb[TPC][HQ];
+    auto load_box = [&](int c, int b, float4 (&w)[HQ], float4 (&xv)[TPC][HQ]) {
         const uint8_t *wr = ring + ((c % SLOTS) * NB + b) * hb + er * 128;
         const float *xc = xf + c * HC + b * SM_BOX;
 #pragma unroll
         for (int q = 0; q < HQ; ++q) {
             w[q] = *reinterpret_cast<const float4 *>(wr + ((q ^ (er & 7)) << 4));
-            xv[q] = *reinterpret_cast<const float4 *>(xc + 4 * q);
+#pragma unroll
+            for (int tk = 0; tk < TPC; ++tk)
+                xv[tk][q] = *reinterpret_cast<const float4 *>(xc + tk * H + 4 * q);
         }
     };
-    auto fma_box = [&](const float4 (&w)[HQ], const float4 (&xv)[HQ]) {
+    auto fma_box = [&](const float4 (&w)[HQ], const float4 (&xv)[TPC][HQ]) {
 #pragma unroll
         for (int q = 0; q < HQ; ++q) {
-            acc = __fmaf_rn(xv[q].x, w[q].x, acc);
-            acc = __fmaf_rn(xv[q].y, w[q].y, acc);
-            acc = __fmaf_rn(xv[q].z, w[q].z, acc);
-            acc = __fmaf_rn(xv[q].w, w[q].w, acc);
+#pragma unroll
+            for (int tk = 0; tk < TPC; ++tk) {
+                acc[tk] = __fmaf_rn(xv[tk][q].x, w[q].x, acc[tk]);
+                acc[tk] = __fmaf_rn(xv[tk][q].y, w[q].y, acc[tk]);
+                acc[tk] = __fmaf_rn(xv[tk][q].z, w[q].z, acc[tk]);
+                acc[tk] = __fmaf_rn(xv[tk][q].w, w[q].w, acc[tk]);
+            }
         }
     };
     auto wait_chunk = [&](int c) {
@@ -672,25 +697,31 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
         }
     }
     if (e < E) {
-        if (gate_bias) acc = __fadd_rn(acc, gate_bias[e]);
-        s_lg[e] = acc;
-        if (logits) logits[static_cast<size_t>(t) * E + e] = acc;
+#pragma unroll
+        for (int tk = 0; tk < TPC; ++tk) {
+            float a = acc[tk];
+            if (gate_bias) a = __fadd_rn(a, gate_bias[e]);
+            s_lg[tk][e] = a;
+            if (logits && tk < ntok) logits[static_cast<size_t>(t0 + tk) * E + e] = a;
+        }
     }
     consumer_sync(nc);
-    if (fuse_topk && tid < 32) {
+    // warp tk: token tk's top-k
+    const int tk = tid >> 5;
+    if (fuse_topk && tk < ntok) {
         float v[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int ee = tid + 32 * i;
-            v[i] = ee < E ? s_lg[ee] : -INFINITY;
+            const int ee = lane + 32 * i;
+            v[i] = ee < E ? s_lg[tk][ee] : -INFINITY;
         }
         int sel_e;
         float sel_v;
         warp_topk<4>(v, k, &sel_e, &sel_v);
         const float w = slot_weight<4>(v, k, renorm != 0, sel_v);
-        if (tid < k) {
-            topk_idx[static_cast<size_t>(t) * k + tid] = sel_e;
-            topk_w[static_cast<size_t>(t) * k + tid] = w;
+        if (lane < k) {
+            topk_idx[static_cast<size_t>(t0 + tk) * k + lane] = sel_e;
+            topk_w[static_cast<size_t>(t0 + tk) * k + lane] = w;
         }
     }
 }
@@ -1089,34 +1120,45 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
         const int threads = std::max(64, static_cast<int>(ceil_div(E, 32)) * 32) + 32;
         CUtensorMap tmw;
         if (!make_wg_map(&tmw, wg, H, E)) return cudaErrorInvalidValue;
-        auto smem_for = [&](int slots, int nb) {
+        auto smem_for = [&](int slots, int nb, int tpc) {
             return 1024 + static_cast<size_t>(slots) * nb * sm_box_bytes(E) +
-                   static_cast<size_t>(H) * sizeof(float);
+                   static_cast<size_t>(tpc) * H * sizeof(float);
         };
-        auto run = [&](auto kernel, int slots, int nb) -> cudaError_t {
-            const size_t smem = smem_for(slots, nb);
+        auto run = [&](auto kernel, int slots, int nb, int tpc) -> cudaError_t {
+            const size_t smem = smem_for(slots, nb, tpc);
             if (smem > 48 * 1024) {
                 cudaError_t e = cudaFuncSetAttribute(
                     kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
                 if (e != cudaSuccess) return e;
             }
-            kernel<<<T, threads, smem, stream>>>(x, gamma, wg, gate_bias, H, E, eps,
-                                                 rmsnorm ? 1 : 0, xn, logits, fuse_topk ? 1 : 0,
-                                                 k, renorm ? 1 : 0, topk_idx, topk_w, dev_status,
-                                                 tmw);
+            kernel<<<static_cast<unsigned>(ceil_div(T, tpc)), threads, smem, stream>>>(
+                x, gamma, wg, gate_bias, T, H, E, eps, rmsnorm ? 1 : 0, xn, logits,
+                fuse_topk ? 1 : 0, k, renorm ? 1 : 0, topk_idx, topk_w, dev_status, tmw);
             return cudaSuccess;
         };
-        // up to one CTA per SM: the deepest ring that fits; more tokens than
-        // SMs: a ring that lets two CTAs share an SM
+        // One CTA per SM while the tokens allow: one token per CTA up to a
+        // CTA per SM, two up to two tokens per SM (the weight then streams
+        // through each SM once per two tokens), the deepest ring that fits,
+        // in 128-column chunks when H allows.  Beyond that two CTAs of two
+        // tokens share an SM.
+        const int64_t sms = num_sms();
+        const bool h128 = H % (4 * SM_BOX) == 0;
+        const size_t full = SM_SMEM_CAP, half = SM_SMEM_CAP / 2;
         cudaError_t le;
-        if (T <= num_sms() && H % (4 * SM_BOX) == 0 && smem_for(6, 4) <= SM_SMEM_CAP)
-            le = run(router_small_kernel<6, 4>, 6, 4);
-        else if (T <= num_sms() && smem_for(12, 2) <= SM_SMEM_CAP)
-            le = run(router_small_kernel<12, 2>, 12, 2);
-        else if (smem_for(5, 2) <= SM_SMEM_CAP / 2)
-            le = run(router_small_kernel<5, 2>, 5, 2);
+        if (T <= sms && h128 && smem_for(6, 4, 1) <= full)
+            le = run(router_small_kernel<6, 4, 1>, 6, 4, 1);
+        else if (T <= sms && smem_for(12, 2, 1) <= full)
+            le = run(router_small_kernel<12, 2, 1>, 12, 2, 1);
+        else if (T > sms && T <= 2 * sms && h128 && smem_for(5, 4, 2) <= full)
+            le = run(router_small_kernel<5, 4, 2>, 5, 4, 2);
+        else if (T > sms && T <= 2 * sms && smem_for(10, 2, 2) <= full)
+            le = run(router_small_kernel<10, 2, 2>, 10, 2, 2);
+        else if (T > 2 * sms && smem_for(4, 2, 2) <= half)
+            le = run(router_small_kernel<4, 2, 2, 2>, 4, 2, 2);
+        else if (smem_for(5, 2, 1) <= half)
+            le = run(router_small_kernel<5, 2, 1>, 5, 2, 1);
         else
-            le = run(router_small_kernel<3, 2>, 3, 2);
+            le = run(router_small_kernel<3, 2, 1>, 3, 2, 1);
         if (le != cudaSuccess) return le;
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess || !fuse_topk || hist == nullptr) return e;
