@@ -14,6 +14,11 @@ with CUDA events on the launching stream, max over ranks.  Per-stage times
 come from events the library records between its launches in the same
 timed steps (moe_layer_forward_timed).
 
+``roofline`` is the w13 matmul's: flops against the measured sustained bf16
+rate when its flops per byte exceed the balance of the two measured peaks
+(many rows per expert), else bytes (the weights of the experts that get
+rows, once, plus the rows in and out) against the measured HBM copy rate.
+
 ``e2e`` is the same metric through moe_layer_forward_host on pinned host
 buffers: every step copies its tokens in and its output out (both inside
 the wall-clock timed region, which ends when the last output is on the
@@ -238,15 +243,18 @@ def cpu_oracle_rate(inputs_cpu, wl, seconds, first_token=0):
 
 
 # --------------------------------------------------------------- our arm
-def stage_bytes_flops(wl, two_streams=False):
+def stage_bytes_flops(wl, two_streams=False, active=None):
     """Algorithmic work of each timed stage.  With two streams the row copies
     run on the second stream beside the shared expert's w13, so the permute
     stage of the main stream is empty and gets no bytes; both matmul stages
-    still run every matmul on the main stream."""
+    still run every matmul on the main stream.  Given the number of experts
+    that receive rows, the matmul stages also get their bytes: the weights of
+    those experts (and the shared expert's) once, their input rows and their
+    outputs."""
     T, H, E, k, I, Is = wl.T, wl.H, wl.E, wl.k, wl.I, wl.I_s
     N = T * k
     # algorithmic work of each stage (what the step must touch or compute once)
-    return {
+    work = {
         "router": {"bytes": T * H * 2 + (T * H * 2 if wl.rmsnorm else 0) + E * H * 4 + N * 8,
                    "gate_flops": 2.0 * T * H * E},
         "permute": {"bytes": 0 if two_streams else T * H * 2 + N * H * 2 + N * 4},
@@ -254,19 +262,50 @@ def stage_bytes_flops(wl, two_streams=False):
         "gemm_down": {"flops": 2.0 * N * H * I + 2.0 * T * H * Is},
         "finalize": {"bytes": N * H * 2 + (T * H * 4 if wl.I_s else 0) + T * H * 2 + N * 8},
     }
+    if active is not None:
+        # w13: weights [2I, H] bf16, rows in bf16, SwiGLU rows out bf16; down:
+        # weights [H, I], act rows in, y rows out bf16 (the shared expert's fp32)
+        work["gemm_w13_swiglu"]["bytes"] = (active * 2 * I * H * 2 + 2 * Is * H * 2 +
+                                            (N + (T if Is else 0)) * H * 2 + (N * I + T * Is) * 2)
+        work["gemm_down"]["bytes"] = (active * H * I * 2 + H * Is * 2 + (N * I + T * Is) * 2 +
+                                      N * H * 2 + (T * H * 4 if Is else 0))
+    return work
+
+
+def active_experts(g, wl) -> int:
+    """Experts that receive at least one row, from the library's own routing
+    of the step's tokens (sequential fp32 gate), for the byte count of the
+    matmul stages."""
+    import torch
+    import moe_expert_routing_fp32_gb300 as moe
+    _, logits = moe.rmsnorm_gate(g["x"], g["wg"], g["gamma"], g["gate_bias"], wl.eps,
+                                 rmsnorm=wl.rmsnorm)
+    idx, _ = moe.gate_topk(logits, wl.k, wl.renorm)
+    return int((torch.bincount(idx.flatten().long(), minlength=wl.E) > 0).sum().item())
+
+
+def gemm_bound(flops, nbytes, tc_peak_tflops, hbm_peak_gbs):
+    """'tensor' when the matmul's flops per byte exceed the machine balance of
+    the two measured peaks, else 'hbm' (few rows per expert: the step streams
+    the weights)."""
+    return "tensor" if flops / nbytes > tc_peak_tflops * 1e3 / hbm_peak_gbs else "hbm"
 
 
 def launches_per_step(wl, gate_sequential=False, two_streams=False):
     """Library kernel launches of one layer pass (the tile-counter memsets
     before the CTA-pair matmuls are not kernels)."""
     E, T = wl.E, wl.T
+    # up to 512 tokens the scan counts the routing histogram itself
+    scan_hist = T <= 512 and -(-T // 32) * E <= 8 * 1024
+    topk_hist = (1 if E > 64 else 0) + (0 if scan_hist else 1)
     if T <= 512 and E <= 128 and wl.H <= 8192:
-        router = 2 if E <= 64 else 3            # small-batch router + histogram (+ top-k)
+        router = 1 + (1 if E > 64 else 0)       # small-batch router (+ top-k)
     elif T > 512 and not gate_sequential:
         # RMSNorm, split, gate GEMM, combine (+ top-k and histogram for E > 64)
         router = (1 if wl.rmsnorm else 0) + 3 + (2 if E > 64 else 0)
     else:
-        router = 1 + (2 if E > 64 else 0)       # sequential router (+ top-k, histogram)
+        # sequential router (+ top-k for E > 64, + histogram unless fused)
+        router = 1 + (topk_hist if E > 64 else 0)
     # scan, scatter, permute, w13 (two launches on two streams), down, finalize
     return router + 6 + (1 if two_streams else 0)
 
@@ -331,11 +370,12 @@ def run_ours(args, rank, world, local):
     stage_ms = {}
     for j, name in enumerate(moe.STAGE_NAMES):
         stage_ms[name] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+    active = active_experts(g, wl)
 
     # end to end on host buffers (pinned), through the same public call
     if args.no_e2e:
         return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, None, g,
-                           two_streams)
+                           two_streams, active)
     # two host batches (this rank's tokens and a second draw) used in turn,
     # two host output buffers; every step copies its tokens in and its output
     # out, overlapped with the neighbouring steps' compute
@@ -362,11 +402,11 @@ def run_ours(args, rank, world, local):
         raise RuntimeError(f"device status {int(status.item())} in the end-to-end steps")
     e2e_value = job_throughput(world, wl.T, Ke, e2e_ms)
     return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g,
-                       two_streams)
+                       two_streams, active)
 
 
 def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g,
-                two_streams=False):
+                two_streams=False, active=None):
     import moe_expert_routing_fp32_gb300 as moe  # noqa: F401
     step_ms = elapsed_ms / K
     value = job_throughput(world, wl.T, K, elapsed_ms)
@@ -375,12 +415,18 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
     # the shared expert inside the w13 launch
     from moe_inputs import WORKLOADS
     traffic_applies = wl == WORKLOADS[args.workload] and not two_streams
-    work = stage_bytes_flops(wl, two_streams)
+    work = stage_bytes_flops(wl, two_streams, wl.E if active is None else active)
     dom = "gemm_w13_swiglu"
     dom_s = stage_ms[dom] / 1e3
     tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    achieved = work[dom]["flops"] / dom_s / 1e12
+    bound = gemm_bound(work[dom]["flops"], work[dom]["bytes"], tc_peak, hbm_peak)
+    if bound == "tensor":
+        achieved, peak, punit = work[dom]["flops"] / dom_s / 1e12, tc_peak, "TFLOP/s"
+        psrc = f"bf16_tflops_sustained ({peak_src})"
+    else:
+        achieved, peak, punit = work[dom]["bytes"] / dom_s / 1e9, hbm_peak, "GB/s"
+        psrc = f"hbm_gbs ({peak_src})"
     gemm_s = (stage_ms["gemm_w13_swiglu"] + stage_ms["gemm_down"]) / 1e3
     gemm_tflops = (work["gemm_w13_swiglu"]["flops"] + work["gemm_down"]["flops"]) / gemm_s / 1e12
     # whole-layer GEMM rate: every GEMM flop of the step (routed + shared) over the step
@@ -394,7 +440,7 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
         if "flops" in wk and name.startswith("gemm"):
             e["tflops"] = round(wk["flops"] / (ms / 1e3) / 1e12, 1)
             e["frac_bf16_peak"] = round(e["tflops"] / tc_peak, 4)
-        if "bytes" in wk and not name.startswith("gemm"):
+        if "bytes" in wk:
             e["gbs"] = round(wk["bytes"] / (ms / 1e3) / 1e9, 1)
             e["frac_hbm"] = round(e["gbs"] / hbm_peak, 4)
         if "gate_flops" in wk:
@@ -415,9 +461,9 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
                             else "fp32 on the tensor cores (exact 3-part bf16 split of Wg)"),
                    "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
-                     "peak": tc_peak, "unit": "TFLOP/s", "frac": round(achieved / tc_peak, 4),
-                     "peak_source": f"bf16_tflops_sustained ({peak_src})",
+        "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": peak, "unit": punit, "frac": round(achieved / peak, 4),
+                     "peak_source": psrc,
                      "traffic": recorded_traffic(wl.name) if traffic_applies else None},
         "gemm_tflops": round(gemm_tflops, 1),
         "gemm_frac_bf16_peak": round(gemm_tflops / tc_peak, 4),

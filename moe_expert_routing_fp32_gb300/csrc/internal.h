@@ -55,9 +55,17 @@ cudaError_t launch_topk(const float *logits, int T, int E, int k, bool renorm,
 // ---- routing.cu
 cudaError_t launch_route_hist(const int32_t *topk_idx, int T, int k, int E, int32_t *hist,
                               int32_t *dev_status, cudaStream_t stream);
-// hist [B][E] -> in place per-chunk row bases; counts [E]; offsets [E+1]
+// hist [B][E] -> in place per-chunk row bases; counts [E]; offsets [E+1].
+// Given topk_idx ([T, k], B = ceil(T/32)), the scan's CTA first counts the
+// histogram itself (scan_builds_hist(T, E) must hold); else hist holds it.
 cudaError_t launch_route_scan(int32_t *hist, int B, int E, int32_t *counts, int32_t *offsets,
+                              const int32_t *topk_idx, int T, int k, int32_t *dev_status,
                               cudaStream_t stream);
+// few tokens: one CTA counts the histogram faster than a launch of its own
+// (at most 32 KB of it, within the default 48 KB of shared memory)
+inline bool scan_builds_hist(int T, int E) {
+    return T <= kGateSmallMaxT && ceil_div(T, kChunkTokens) * E <= 8 * 1024;
+}
 cudaError_t launch_route_scatter(const int32_t *topk_idx, const int32_t *base, int T, int k,
                                  int E, int32_t *row_idx, int32_t *src_token,
                                  int32_t *sorted_ids, int32_t *dev_status, cudaStream_t stream);

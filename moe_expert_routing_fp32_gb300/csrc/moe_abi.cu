@@ -278,8 +278,12 @@ moe_status_t moe_init_routing(const int32_t *topk_idx, const moe_bf16_t *x, int3
         MOE_TRY(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s));
         return MOE_OK;
     }
-    MOE_TRY(launch_route_hist(topk_idx, T, k, E, hist, dev_status, s));
-    MOE_TRY(launch_route_scan(hist, B, E, counts, offsets, s));
+    if (scan_builds_hist(T, E)) {
+        MOE_TRY(launch_route_scan(hist, B, E, counts, offsets, topk_idx, T, k, dev_status, s));
+    } else {
+        MOE_TRY(launch_route_hist(topk_idx, T, k, E, hist, dev_status, s));
+        MOE_TRY(launch_route_scan(hist, B, E, counts, offsets, nullptr, T, k, dev_status, s));
+    }
     MOE_TRY(launch_route_scatter(topk_idx, hist, T, k, E, expanded_row_idx, src_token,
                                  sorted_expert_ids, dev_status, s));
     if (expanded_x) MOE_TRY(launch_permute(x, expanded_row_idx, T, H, k, expanded_x, s));
@@ -418,27 +422,30 @@ moe_status_t layer_forward_impl(const moe_desc_t *desc, const moe_bf16_t *x,
         return cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s);
     };
 
-    // 1. RMSNorm + gate (+ top-k + routing histogram when E <= 64)
+    // 1. RMSNorm + gate (+ top-k, and the routing histogram when E <= 64 and
+    // the scan does not count it itself)
     MOE_TRY(mark(0));
     const bool fuse = E <= kRouterExperts;
+    const bool scan_hist = scan_builds_hist(T, E);
+    int32_t *hist_out = fuse && !scan_hist ? hist : nullptr;
     if (layer_gate_tc(d)) {
         // RMSNorm alone, then the gate as a tensor-core GEMM on the normalised rows
         if (rms) MOE_TRY(launch_rmsnorm(x, gamma, T, H, d.rms_eps, xn, dev_status, s));
         MOE_TRY(launch_gate_tc(xs, wg, gate_bias, T, H, E, static_cast<uint16_t *>(at(L.wsplit)),
                                static_cast<float *>(at(L.parts)), logits, fuse, k, renorm, idx, w,
-                               fuse ? hist : nullptr, dev_status, s));
+                               hist_out, dev_status, s));
     } else {
         MOE_TRY(launch_router(x, rms ? gamma : nullptr, wg, gate_bias, T, H, E, d.rms_eps, rms,
-                              xn, logits, fuse, k, renorm, idx, w, fuse ? hist : nullptr,
-                              dev_status, s));
+                              xn, logits, fuse, k, renorm, idx, w, hist_out, dev_status, s));
     }
     if (!fuse) {
         MOE_TRY(launch_topk(logits, T, E, k, renorm, idx, w, s));
-        MOE_TRY(launch_route_hist(idx, T, k, E, hist, dev_status, s));
+        if (!scan_hist) MOE_TRY(launch_route_hist(idx, T, k, E, hist, dev_status, s));
     }
     // 2. init_routing: scan + stable scatter, then the row copies
     MOE_TRY(mark(1));
-    MOE_TRY(launch_route_scan(hist, B, E, counts, offsets, s));
+    MOE_TRY(launch_route_scan(hist, B, E, counts, offsets, scan_hist ? idx : nullptr, T, k,
+                              dev_status, s));
     MOE_TRY(launch_route_scatter(idx, hist, T, k, E, row_idx, nullptr, nullptr, dev_status, s));
     MOE_TRY(mark(2));
     const bool two_streams = shared && shared_stream != nullptr;

@@ -97,10 +97,13 @@ extern "C" moe_status_t moe_init_routing_noalloc(
             return MOE_ERR_CUDA;
         return MOE_OK;
     }
-    // Every histogram entry that is read below is written first by the
-    // histogram kernel, so the array needs no clearing between calls.
-    if (launch_route_hist(topk_idx, T, k, E, hist, dev_status, s) != cudaSuccess ||
-        launch_route_scan(hist, B, E, counts, offsets, s) != cudaSuccess ||
+    // Every histogram entry that is read below is written first (by the
+    // histogram kernel, or by the scan when it counts few tokens itself), so
+    // the array needs no clearing between calls.
+    const bool scan_hist = scan_builds_hist(T, E);
+    if ((!scan_hist && launch_route_hist(topk_idx, T, k, E, hist, dev_status, s) != cudaSuccess) ||
+        launch_route_scan(hist, B, E, counts, offsets, scan_hist ? topk_idx : nullptr, T, k,
+                          dev_status, s) != cudaSuccess ||
         launch_route_scatter(topk_idx, hist, T, k, E, expanded_row_idx, src_token,
                              sorted_expert_ids, dev_status, s) != cudaSuccess)
         return MOE_ERR_CUDA;

@@ -50,14 +50,32 @@ route_hist_kernel(const int32_t *__restrict__ topk_idx, int T, int k, int E,
 }
 
 // One CTA of 1024 threads (E <= 1024).  Thread (s, e) owns expert e's column
-// of the [B][E] histogram over the chunk segment s.
+// of the [B][E] histogram over the chunk segment s.  Given topk_idx (few
+// tokens), the CTA first counts the histogram in shared memory and stores it.
 __global__ void __launch_bounds__(1024)
 route_scan_kernel(int32_t *__restrict__ hist, int B, int E, int32_t *__restrict__ counts,
-                  int32_t *__restrict__ offsets) {
+                  int32_t *__restrict__ offsets, const int32_t *__restrict__ topk_idx, int T,
+                  int k, int32_t *dev_status) {
     __shared__ int s_seg[1024];
     __shared__ int s_cnt[1024];
     __shared__ int s_warp[32];
+    extern __shared__ int s_hist[];   // [B][E], with topk_idx
     const int tid = threadIdx.x;
+    if (topk_idx) {
+        for (int i = tid; i < B * E; i += blockDim.x) s_hist[i] = 0;
+        __syncthreads();
+        const int n = T * k;
+        for (int a = tid; a < n; a += blockDim.x) {
+            const int e = topk_idx[a];
+            if (e >= 0 && e < E)
+                atomicAdd(&s_hist[(a / k) / kChunkTokens * E + e], 1);
+            else
+                report(dev_status, MOE_DEV_BAD_EXPERT_ID);
+        }
+        __syncthreads();
+        for (int i = tid; i < B * E; i += blockDim.x) hist[i] = s_hist[i];
+        __syncthreads();
+    }
     const int S = 1024 / E;                  // segments per expert
     const int L = (B + S - 1) / S;           // chunks per segment
     const int e = tid % E;
@@ -339,8 +357,12 @@ cudaError_t launch_route_hist(const int32_t *topk_idx, int T, int k, int E, int3
 }
 
 cudaError_t launch_route_scan(int32_t *hist, int B, int E, int32_t *counts, int32_t *offsets,
+                              const int32_t *topk_idx, int T, int k, int32_t *dev_status,
                               cudaStream_t stream) {
-    route_scan_kernel<<<1, 1024, 0, stream>>>(hist, B, E, counts, offsets);
+    if (topk_idx && !scan_builds_hist(T, E)) return cudaErrorInvalidValue;
+    const size_t smem = topk_idx ? static_cast<size_t>(B) * E * sizeof(int) : 0;
+    route_scan_kernel<<<1, 1024, smem, stream>>>(hist, B, E, counts, offsets, topk_idx, T, k,
+                                                 dev_status);
     return cudaGetLastError();
 }
 

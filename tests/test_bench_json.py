@@ -67,10 +67,36 @@ def test_launch_count_follows_the_gate_path():
     assert bench.launches_per_step(img, gate_sequential=True) == 7
     assert bench.launches_per_step(img, two_streams=True) == 11
     assert bench.launches_per_step(WORKLOADS["skewed-32k"]) == 9          # no RMSNorm
-    assert bench.launches_per_step(WORKLOADS["smallbatch-8"]) == 8
+    assert bench.launches_per_step(WORKLOADS["smallbatch-8"]) == 7   # histogram in the scan
     res = bench.finish_ours(_args(), img, 1, 0, 10, 3, 80.0, _stages(1.0), CLK, None, {})
     assert res["gpu_launches"] == 100
     assert "tensor cores" in res["config"]["gate"]
     res = bench.finish_ours(_args(gate_sequential=True), img, 1, 0, 10, 3, 80.0, _stages(1.0),
                             CLK, None, {})
     assert res["gpu_launches"] == 70 and "sequential" in res["config"]["gate"]
+
+
+def test_roofline_bound_follows_the_arithmetic_intensity():
+    """Thousands of rows per expert make the matmul tensor-bound; a few rows
+    per expert make it stream the weights, and the roofline is then HBM
+    bytes (the experts that get rows, each weight once) against the HBM peak."""
+    img, small = WORKLOADS["imagegen-16k"], WORKLOADS["smallbatch-8"]
+    w = bench.stage_bytes_flops(img, active=img.E)["gemm_w13_swiglu"]
+    assert bench.gemm_bound(w["flops"], w["bytes"], 1699.4, 6769.8) == "tensor"
+    w = bench.stage_bytes_flops(small, active=41)["gemm_w13_swiglu"]
+    H, I, Is, N = small.H, small.I, small.I_s, small.T * small.k
+    weights = 41 * 2 * I * H * 2 + 2 * Is * H * 2
+    assert weights < w["bytes"] < weights * 1.01          # the weights are nearly all of it
+    assert bench.gemm_bound(w["flops"], w["bytes"], 1699.4, 6769.8) == "hbm"
+    d = bench.stage_bytes_flops(small, active=41)["gemm_down"]["bytes"]
+    assert 41 * H * I * 2 + H * Is * 2 < d < (41 * H * I * 2 + H * Is * 2) * 1.01
+    stages = _stages(0.01)
+    stages["gemm_w13_swiglu"] = 0.32
+    res = bench.finish_ours(_args(workload="smallbatch-8"), small, 1, 0, 10, 3, 5.7, stages, CLK,
+                            None, {}, active=41)
+    r = res["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(w["bytes"] / 0.32e-3 / 1e9, rel=1e-3)
+    assert res["stages"]["gemm_w13_swiglu"]["frac_hbm"] == pytest.approx(r["frac"], rel=1e-3)
+    assert bench.finish_ours(_args(), img, 1, 0, 10, 3, 80.0, _stages(1.0), CLK, None,
+                             {})["roofline"]["bound"] == "tensor"

@@ -106,8 +106,12 @@ def test_topk(T, E, k, renorm):
 
 
 # ------------------------------------------------------------------ routing
+# up to 512 tokens (and 8K histogram entries) the scan counts the histogram
+# itself: 77, 1, 512 tokens and 256 x 1024 experts (the largest such array);
+# 384 x 1024 is past it
 @pytest.mark.parametrize("T,k,E,H", [(1000, 8, 64, 256), (77, 2, 8, 128), (1, 1, 1, 64),
-                                     (4097, 6, 300, 64), (513, 4, 1024, 64)])
+                                     (4097, 6, 300, 64), (513, 4, 1024, 64), (512, 8, 64, 128),
+                                     (256, 3, 1024, 64), (384, 3, 1024, 64)])
 def test_init_routing_bitexact(T, k, E, H):
     rng = np.random.default_rng(T * 7 + E)
     w = rng.pareto(1.2, E) + 0.01              # skewed expert popularity

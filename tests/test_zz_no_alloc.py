@@ -61,7 +61,8 @@ def test_noalloc_matches_workspace_entry_point_twice():
     moe.build()
     # two calls in a row with different inputs (the second must not see the
     # first call's leftovers in the shared array)
-    for T, k, E, H, seed in [(3000, 8, 64, 256, 1), (777, 4, 200, 128, 2)]:
+    for T, k, E, H, seed in [(3000, 8, 64, 256, 1), (777, 4, 200, 128, 2),
+                             (300, 8, 64, 128, 3)]:
         idx, x = _case(T, k, E, H, seed)
         ref = moe.init_routing(idx, x, E)
         got, st = _noalloc(idx, x, E)
