@@ -24,8 +24,10 @@
 //     taken on them) are bit-identical to it;
 //   phase 3 (E <= 64): warp-per-token top-k / softmax, the routing
 //     histogram of the 32-token chunk, and the logits row write-out.
-// Batches of at most 512 tokens use router_small_kernel instead (one CTA per
-// token, one thread per expert), which keeps every SM busy.
+// Batches of at most 512 tokens use router_small_kernel instead (one thread
+// per expert, one token per CTA up to one CTA per SM, two tokens per CTA
+// beyond), which keeps every SM busy; the routing histogram is then counted
+// by the scan (routing.cu).
 // This gate is plain fp32 FMA work (2*T*H*E flops); the tensor cores' fp32
 // input mode (tf32) would round the inputs, hence the exact bf16 split of the
 // other gate.
