@@ -451,9 +451,9 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // the consumers' FMA chains never stop at a block-wide barrier.  A CTA takes
 // TPC consecutive tokens: every consumer runs one chain per token on the
 // same weight operands, so the weight streams through the SM once per TPC
-// tokens.  MIN_CTAS = 2 caps the registers so that two CTAs share an SM.
-template <int SLOTS, int NB, int TPC, int MIN_CTAS = 1>
-__global__ void __launch_bounds__(160, MIN_CTAS)
+// tokens.
+template <int SLOTS, int NB, int TPC>
+__global__ void __launch_bounds__(160)
 router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
                     const float *__restrict__ wg, const float *__restrict__ gate_bias, int T,
                     int H, int E, float eps, int rmsnorm, uint16_t *__restrict__ xn,
@@ -1138,11 +1138,10 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
                 fuse_topk ? 1 : 0, k, renorm ? 1 : 0, topk_idx, topk_w, dev_status, tmw);
             return cudaSuccess;
         };
-        // One CTA per SM while the tokens allow: one token per CTA up to a
-        // CTA per SM, two up to two tokens per SM (the weight then streams
-        // through each SM once per two tokens), the deepest ring that fits,
-        // in 128-column chunks when H allows.  Beyond that two CTAs of two
-        // tokens share an SM.
+        // One CTA per SM: one token per CTA up to a CTA per SM, else two (the
+        // weight then streams through each SM once per two tokens; beyond two
+        // tokens per SM a second wave), the deepest ring that fits, in
+        // 128-column chunks when H allows.
         const int64_t sms = num_sms();
         const bool h128 = H % (4 * SM_BOX) == 0;
         const size_t full = SM_SMEM_CAP, half = SM_SMEM_CAP / 2;
@@ -1151,12 +1150,10 @@ cudaError_t launch_router(const uint16_t *x, const uint16_t *gamma, const float 
             le = run(router_small_kernel<6, 4, 1>, 6, 4, 1);
         else if (T <= sms && smem_for(12, 2, 1) <= full)
             le = run(router_small_kernel<12, 2, 1>, 12, 2, 1);
-        else if (T > sms && T <= 2 * sms && h128 && smem_for(5, 4, 2) <= full)
+        else if (T > sms && h128 && smem_for(5, 4, 2) <= full)
             le = run(router_small_kernel<5, 4, 2>, 5, 4, 2);
-        else if (T > sms && T <= 2 * sms && smem_for(10, 2, 2) <= full)
+        else if (T > sms && smem_for(10, 2, 2) <= full)
             le = run(router_small_kernel<10, 2, 2>, 10, 2, 2);
-        else if (T > 2 * sms && smem_for(4, 2, 2) <= half)
-            le = run(router_small_kernel<4, 2, 2, 2>, 4, 2, 2);
         else if (smem_for(5, 2, 1) <= half)
             le = run(router_small_kernel<5, 2, 1>, 5, 2, 1);
         else

@@ -30,9 +30,9 @@ def _cuda(d):
     Workload("g-wideE", T=40, H=192, E=160, k=6, I=128, rmsnorm=True),
     # the small-batch router's rings: one token per CTA in 6 slots of 128
     # columns with refills (T <= SMs) or 12 slots of 64 columns (H not a
-    # multiple of 128); two tokens per CTA (T <= 2 SMs: 5 slots of 128
-    # columns; beyond: 4 slots of 64, two CTAs per SM), odd T; 3 slots (E=128
-    # at the largest H); one chunk
+    # multiple of 128); two tokens per CTA in 5 slots of 128 columns (one
+    # wave up to 2 tokens per SM, two beyond), odd T; 3 slots (E=128 at the
+    # largest H); one chunk
     Workload("g-small-deep", T=100, H=1024, E=64, k=8, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-small-h64", T=50, H=1088, E=40, k=4, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-small-2cta", T=300, H=512, E=32, k=4, I=128, rmsnorm=True),
