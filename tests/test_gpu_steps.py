@@ -31,14 +31,15 @@ def _cuda(d):
     # the small-batch router's rings: one token per CTA in 6 slots of 128
     # columns with refills (T <= SMs) or 12 slots of 64 columns (H not a
     # multiple of 128); two tokens per CTA in 5 slots of 128 columns (one
-    # wave up to 2 tokens per SM, two beyond), odd T; 3 slots (E=128 at the
-    # largest H); one chunk
+    # wave up to 2 tokens per SM, two beyond) or 10 of 64, odd T; 3 slots
+    # (E=128 at the largest H); one chunk
     Workload("g-small-deep", T=100, H=1024, E=64, k=8, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-small-h64", T=50, H=1088, E=40, k=4, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-small-2cta", T=300, H=512, E=32, k=4, I=128, rmsnorm=True),
     Workload("g-small-2tok", T=201, H=1536, E=64, k=8, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-small-2tok-2cta", T=333, H=640, E=24, k=4, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-small-2tok-plain", T=157, H=192, E=16, k=2, I=128),
+    Workload("g-small-2tok-h64", T=171, H=1344, E=48, k=4, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-small-maxH", T=24, H=8192, E=128, k=8, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("g-small-1chunk", T=5, H=64, E=6, k=2, I=128),
     # more than 512 tokens: the tiled router (32 tokens x 64 experts per CTA)
