@@ -14,9 +14,10 @@ with CUDA events on the launching stream, max over ranks.  Per-stage times
 come from events the library records between its launches in the same
 timed steps (moe_layer_forward_timed).
 
-``roofline`` is the w13 matmul's: flops against the measured sustained bf16
-rate when its flops per byte exceed the balance of the two measured peaks
-(many rows per expert), else bytes (the weights of the experts that get
+``roofline`` is the w13 matmul's: flops against the measured bf16 rate
+(sustained when the timed steps ran power-capped, else burst) when its flops
+per byte exceed the balance of the two measured peaks (many rows per
+expert), else bytes (the weights of the experts that get
 rows, once, plus the rows in and out) against the measured HBM copy rate.
 
 ``e2e`` is the same metric through moe_layer_forward_host on pinned host
@@ -284,6 +285,14 @@ def active_experts(g, wl) -> int:
     return int((torch.bincount(idx.flatten().long(), minlength=wl.E) > 0).sum().item())
 
 
+def power_capped(clk) -> bool:
+    """Whether the clock record of the timed steps shows the power cap, or an
+    SM clock below 97% of its maximum; without a record, assume it does."""
+    if not clk or "sm_mhz" not in clk or "sm_max_mhz" not in clk:
+        return True
+    return "sw_power_cap" in clk.get("reasons", []) or clk["sm_mhz"] < 0.97 * clk["sm_max_mhz"]
+
+
 def gemm_bound(flops, nbytes, tc_peak_tflops, hbm_peak_gbs):
     """'tensor' when the matmul's flops per byte exceed the machine balance of
     the two measured peaks, else 'hbm' (few rows per expert: the step streams
@@ -418,12 +427,15 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
     work = stage_bytes_flops(wl, two_streams, wl.E if active is None else active)
     dom = "gemm_w13_swiglu"
     dom_s = stage_ms[dom] / 1e3
-    tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    # the sustained matmul rate when the timed steps ran power-capped (or the
+    # clock sat below its maximum), else the burst rate
+    tc_key = "bf16_tflops_sustained" if power_capped(clk) else "bf16_tflops"
+    tc_peak = float(peaks.get(tc_key, FALLBACK_PEAKS[tc_key]))
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     bound = gemm_bound(work[dom]["flops"], work[dom]["bytes"], tc_peak, hbm_peak)
     if bound == "tensor":
         achieved, peak, punit = work[dom]["flops"] / dom_s / 1e12, tc_peak, "TFLOP/s"
-        psrc = f"bf16_tflops_sustained ({peak_src})"
+        psrc = f"{tc_key} ({peak_src})"
     else:
         achieved, peak, punit = work[dom]["bytes"] / dom_s / 1e9, hbm_peak, "GB/s"
         psrc = f"hbm_gbs ({peak_src})"

@@ -100,3 +100,19 @@ def test_roofline_bound_follows_the_arithmetic_intensity():
     assert res["stages"]["gemm_w13_swiglu"]["frac_hbm"] == pytest.approx(r["frac"], rel=1e-3)
     assert bench.finish_ours(_args(), img, 1, 0, 10, 3, 80.0, _stages(1.0), CLK, None,
                              {})["roofline"]["bound"] == "tensor"
+
+
+def test_tensor_peak_follows_the_clock_record():
+    """Power-capped steps are measured against the sustained matmul rate,
+    steps at full clock against the burst rate."""
+    wl = WORKLOADS["balanced-4k"]
+    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert not bench.power_capped(full) and bench.power_capped(CLK) and bench.power_capped({})
+    assert bench.power_capped({"sm_mhz": 1800.0, "sm_max_mhz": 2070.0, "reasons": []})
+    peaks, _ = bench.load_peaks()
+    r = bench.finish_ours(_args(workload="balanced-4k"), wl, 1, 0, 10, 3, 4.5, _stages(0.1), full,
+                          None, {})["roofline"]
+    assert r["peak"] == pytest.approx(peaks["bf16_tflops"]) and r["peak_source"].startswith("bf16_tflops ")
+    r = bench.finish_ours(_args(workload="balanced-4k"), wl, 1, 0, 10, 3, 4.5, _stages(0.1), CLK,
+                          None, {})["roofline"]
+    assert r["peak"] == pytest.approx(peaks["bf16_tflops_sustained"])
