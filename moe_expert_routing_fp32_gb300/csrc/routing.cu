@@ -8,7 +8,8 @@
 // init_routing is a stable counting sort of the T*k assignments
 // (a = t*k + j) by expert, in three steps over chunks of 32 tokens (the same
 // chunks the router uses, so the router can emit the histogram itself):
-//   hist:    per-chunk expert histogram (shared-memory atomics; counts only)
+//   hist:    per-chunk expert histogram (shared-memory atomics; counts only;
+//            up to 512 tokens the scan's CTA counts it itself)
 //   scan:    per expert, an exclusive scan over chunks -> each chunk's first
 //            row per expert; counts and offsets
 //   scatter: each chunk ranks its assignments within an expert in order of a
