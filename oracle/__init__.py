@@ -59,8 +59,9 @@ def _bind(lib):
         "oracle_expert_mlp": [P, I64, P, P, I64, I64, P, P, P],
         "oracle_grouped_mlp": [P, P, I64, P, P, I64, I64, P, P],
         "oracle_finalize": [P, P, P, P, I64, I64, I64, P],
+        "oracle_finalize_f64": [P, P, P, P, I64, I64, I64, P],
         "oracle_layer_tokens": [P, I64, I64, I64, I64, I64, I64, INT, F, INT,
-                                P, P, P, P, P, P, P, P, I64, P, P, P, P],
+                                P, P, P, P, P, P, P, P, I64, P, P, P, P, INT],
         "oracle_local_rerouting": [P, P, I64, I64, I64, I64, P, P, P, P],
         "oracle_local_finalize_rerouting": [P, P, I64, I64, P],
     }
@@ -255,23 +256,33 @@ def grouped_mlp(expanded_x, offsets, w13, w2):
 
 
 def finalize(y_exp, row_idx, topk_w, shared=None):
-    y = _u16(y_exp)
-    H = y.shape[1]
+    """Weighted sum of the routed rows: bf16 rows (uint16 bits or a torch bf16
+    tensor), or unrounded rows as a float64 array (the fp32-y reading)."""
     w = _arr(topk_w, np.float32)
     T, k = w.shape
     ri = _arr(row_idx, np.int32).reshape(-1)
     sh = _arr(shared, np.float64)
+    if isinstance(y_exp, np.ndarray) and y_exp.dtype == np.float64:
+        y = np.ascontiguousarray(y_exp)
+        H = y.shape[1]
+        out = np.empty((T, H), dtype=np.float64)
+        _check(_load().oracle_finalize_f64(_p(y), _p(ri), _p(w), _p(sh), T, H, k, _p(out)),
+               "oracle_finalize_f64")
+        return out
+    y = _u16(y_exp)
+    H = y.shape[1]
     out = np.empty((T, H), dtype=np.float64)
     _check(_load().oracle_finalize(_p(y), _p(ri), _p(w), _p(sh), T, H, k, _p(out)),
            "oracle_finalize")
     return out
 
 
-def layer_tokens(inputs: dict, wl, tokens=None, routed_rows=False):
+def layer_tokens(inputs: dict, wl, tokens=None, routed_rows=False, y_f32=False):
     """Whole layer for ``tokens`` (default: all).  ``inputs`` is the dict made
     by moe_inputs.make_inputs; ``wl`` the Workload.  Returns (out f64 [n,H],
     topk_idx [n,k], topk_w [n,k]), and with ``routed_rows`` also each slot's
-    routed expert output as bf16 bits [n,k,H]."""
+    routed expert output as bf16 bits [n,k,H].  ``y_f32``: the routed expert
+    outputs enter the weighted sum unrounded (the fp32-y reading)."""
     x = _u16(inputs["x"])
     T, H = x.shape
     E, k, I, I_s = wl.E, wl.k, wl.I, wl.I_s
@@ -291,7 +302,8 @@ def layer_tokens(inputs: dict, wl, tokens=None, routed_rows=False):
     rc = _load().oracle_layer_tokens(
         _p(x), T, H, E, k, I, I_s, int(wl.rmsnorm), ctypes.c_float(wl.eps),
         int(wl.renorm), _p(gamma), _p(wg), _p(bias), _p(w13), _p(w2), _p(w13_s),
-        _p(w2_s), _p(tok), 0 if tok is None else tok.size, _p(out), _p(idx), _p(w), _p(y))
+        _p(w2_s), _p(tok), 0 if tok is None else tok.size, _p(out), _p(idx), _p(w), _p(y),
+        int(bool(y_f32)))
     _check(rc, "oracle_layer_tokens")
     return (out, idx, w, y) if routed_rows else (out, idx, w)
 

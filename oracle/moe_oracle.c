@@ -36,7 +36,10 @@
  *     by expert.
  *   - Expert MLP: fp64 sums of the exact bf16 products; act and the routed
  *     expert output are rounded to bf16 (the grouped matmul's output type);
- *     the shared expert output enters the final sum unrounded.
+ *     the shared expert output enters the final sum unrounded.  A second
+ *     reading keeps the routed expert output unrounded too (the library's
+ *     fp32-y mode, where the down matmul's accumulator goes straight into the
+ *     weighted sum); only the SwiGLU output is then rounded to bf16.
  *   - Finalize: out[t] = sum_j w[t,j] * y[row(t,j)] + shared[t], in double.
  *
  * bf16 tensors are passed as uint16 bit patterns.
@@ -365,6 +368,27 @@ int oracle_finalize(const bf16_t *y_exp, const int32_t *row_idx, const float *to
     return ORACLE_OK;
 }
 
+/* The same weighted sum over unrounded routed rows y_exp [T*k, H] double    */
+/* (the fp32-y reading: no bf16 rounding of the expert outputs).            */
+int oracle_finalize_f64(const double *y_exp, const int32_t *row_idx, const float *topk_w,
+                        const double *shared, int64_t T, int64_t H, int64_t k, double *out)
+{
+    if (!y_exp || !row_idx || !topk_w || !out || T < 0 || H <= 0 || k < 1)
+        return ORACLE_BAD_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t c = 0; c < H; ++c) {
+            double s = 0.0;
+            for (int64_t j = 0; j < k; ++j)
+                s += (double)topk_w[t * k + j] * y_exp[(int64_t)row_idx[t * k + j] * H + c];
+            if (shared)
+                s += shared[t * H + c];
+            out[t * H + c] = s;
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* The whole layer for a list of tokens.  A token's output depends only on  */
 /* its own row and the weights, so any subset is exact for those tokens.    */
@@ -374,13 +398,16 @@ int oracle_finalize(const bf16_t *y_exp, const int32_t *row_idx, const float *to
 /*   tokens [n_tok] (NULL = 0..T-1, n_tok = T).                             */
 /* Outputs: out [n_tok,H] double; idx/w [n_tok,k] (may be NULL);            */
 /*   y_out [n_tok,k,H] bf16 (may be NULL): each slot's routed expert output,  */
-/*   as it enters the weighted sum.                                           */
+/*   rounded to bf16.                                                       */
+/* y_f32 != 0: the routed expert outputs enter the weighted sum unrounded    */
+/*   (the fp32-y reading); y_out still receives their bf16 roundings.       */
 int oracle_layer_tokens(const bf16_t *x, int64_t T, int64_t H, int64_t E, int64_t k,
                         int64_t I, int64_t I_s, int rmsnorm, float eps, int renorm,
                         const bf16_t *gamma, const float *wg, const float *bias,
                         const bf16_t *w13, const bf16_t *w2, const bf16_t *w13_s,
                         const bf16_t *w2_s, const int32_t *tokens, int64_t n_tok,
-                        double *out, int32_t *idx_out, float *w_out, bf16_t *y_out)
+                        double *out, int32_t *idx_out, float *w_out, bf16_t *y_out,
+                        int y_f32)
 {
     if (!x || !wg || !w13 || !w2 || !out || H <= 0 || E <= 0 || k < 1 || k > E ||
         I <= 0 || I_s < 0 || (I_s > 0 && (!w13_s || !w2_s)))
@@ -394,7 +421,8 @@ int oracle_layer_tokens(const bf16_t *x, int64_t T, int64_t H, int64_t E, int64_
     float *w = (float *)malloc((size_t)k * sizeof(float));
     bf16_t *yb = (bf16_t *)malloc((size_t)H * sizeof(bf16_t));
     double *ys = (double *)malloc((size_t)H * sizeof(double));
-    if (!xrow || !logits || !idx || !w || !yb || !ys) {
+    double *yr = (double *)malloc((size_t)H * sizeof(double));
+    if (!xrow || !logits || !idx || !w || !yb || !ys || !yr) {
         rc = ORACLE_NOMEM;
         goto done;
     }
@@ -420,12 +448,12 @@ int oracle_layer_tokens(const bf16_t *x, int64_t T, int64_t H, int64_t E, int64_
         for (int64_t j = 0; j < k; ++j) {
             const int64_t e = idx[j];
             if ((rc = oracle_expert_mlp(xrow, 1, w13 + e * 2 * I * H, w2 + e * H * I,
-                                        H, I, NULL, yb, NULL)))
+                                        H, I, NULL, yb, yr)))
                 goto done;
             if (y_out)
                 memcpy(y_out + (n * k + j) * H, yb, (size_t)H * sizeof(bf16_t));
             for (int64_t c = 0; c < H; ++c)
-                o[c] += (double)w[j] * (double)bf16_to_float(yb[c]);
+                o[c] += (double)w[j] * (y_f32 ? yr[c] : (double)bf16_to_float(yb[c]));
         }
         if (I_s > 0) {
             if ((rc = oracle_expert_mlp(xrow, 1, w13_s, w2_s, H, I_s, NULL, NULL, ys)))
@@ -445,6 +473,7 @@ done:
     free(w);
     free(yb);
     free(ys);
+    free(yr);
     return rc;
 }
 

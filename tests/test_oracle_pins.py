@@ -184,6 +184,18 @@ def pin_finalize():
     sh = rng.standard_normal((T, H))
     out2 = oracle.finalize(ex, r["row_idx"], w, sh)
     assert np.allclose(out2, bits_f64(x) + sh, rtol=1e-6, atol=1e-6)
+    # unrounded routed rows (the fp32-y reading): identity experts on float64
+    # rows that no bf16 value represents, and a hand-summed token
+    xf = rng.standard_normal((T, H))
+    exf = np.ascontiguousarray(xf[r["src_token"]])
+    out3 = oracle.finalize(exf, r["row_idx"], w, sh)
+    assert np.allclose(out3, xf + sh, rtol=1e-6, atol=1e-6)
+    # distinct rows per slot: a token's sum taken by hand, slot by slot
+    yr = rng.standard_normal((T * k, H))
+    out4 = oracle.finalize(yr, r["row_idx"], w)
+    for t in (0, 7, T - 1):
+        hand = sum(float(w[t, j]) * yr[r["row_idx"][t * k + j]] for j in range(k))
+        assert np.allclose(out4[t], hand, rtol=1e-14, atol=1e-14)
 
 
 def pin_worked_example():
@@ -221,10 +233,13 @@ def pin_worked_example():
 
 def pin_layer_brute_force():
     """Whole layer vs a per-token loop with no routing, no sort and no
-    permutation, written with numpy matmuls (tiny workload, seed 0)."""
+    permutation, written with numpy matmuls (tiny workload, seed 0), with the
+    routed expert outputs rounded to bf16 and, in the fp32-y reading, not."""
     wl = WORKLOADS["tiny"]
     d = make_inputs(wl, 0)
     out, idx, w = oracle.layer_tokens(d, wl)
+    out_f, idx_f, w_f = oracle.layer_tokens(d, wl, y_f32=True)
+    assert np.array_equal(idx_f, idx) and np.array_equal(w_f, w)
     X = d["x"].to(torch.float64).numpy()
     WG = d["wg"].to(torch.float64).numpy()
     W13 = d["w13"].to(torch.float64).numpy()
@@ -238,13 +253,18 @@ def pin_layer_brute_force():
         assert sorted(sel) == sorted(idx[t])
         p = softmax(logits[t, sel])
         acc = np.zeros(wl.H)
+        acc_f = np.zeros(wl.H)
         for j, e in enumerate(sel):
             g = X[t] @ W13[e, : wl.I].T
             u = X[t] @ W13[e, wl.I:].T
             a = bits_f64(oracle.bf16_bits(g * expit(g) * u))
-            y = bits_f64(oracle.bf16_bits(a @ W2[e].T))
-            acc += p[j] * y
+            yf = a @ W2[e].T
+            acc += p[j] * bits_f64(oracle.bf16_bits(yf))
+            acc_f += p[j] * yf
         assert np.allclose(out[t], acc, rtol=1e-5, atol=1e-7), t
+        assert np.allclose(out_f[t], acc_f, rtol=1e-5, atol=1e-7), t
+    # the two readings differ by the bf16 rounding of y only (<= half an ulp)
+    assert not np.array_equal(out, out_f)
 
 
 def pin_layer_shared_rmsnorm():
@@ -334,6 +354,9 @@ MUTANTS = {
     "finalize_weight_index": ("(double)topk_w[t * k + j] *", "(double)topk_w[j] *"),
     "bf16_truncate": ("nearbyint(ldexp(m, 8))", "floor(ldexp(m, 8))"),
     "layer_shared_dropped": ("o[c] += ys[c];", "o[c] += 0.0;"),
+    "layer_y_f32_ignored": ("(y_f32 ? yr[c] :", "(0 ? yr[c] :"),
+    "finalize_f64_row_ignored": ("y_exp[(int64_t)row_idx[t * k + j] * H + c];",
+                                 "y_exp[(int64_t)row_idx[t * k] * H + c];"),
     "ep_rank_off_by_one": ("for (int64_t rr = 0; rr < r; ++rr)",
                            "for (int64_t rr = 0; rr <= r; ++rr)"),
     "ep_finalize_wrong_side": ("memcpy(recv_y + (int64_t)local_src[d] * H, local_y + d * H,",
