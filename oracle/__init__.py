@@ -61,7 +61,7 @@ def _bind(lib):
         "oracle_finalize": [P, P, P, P, I64, I64, I64, P],
         "oracle_finalize_f64": [P, P, P, P, I64, I64, I64, P],
         "oracle_layer_tokens": [P, I64, I64, I64, I64, I64, I64, INT, F, INT,
-                                P, P, P, P, P, P, P, P, I64, P, P, P, P, INT],
+                                P, P, P, P, P, P, P, P, I64, P, P, P, P, P],
         "oracle_local_rerouting": [P, P, I64, I64, I64, I64, P, P, P, P],
         "oracle_local_finalize_rerouting": [P, P, I64, I64, P],
     }
@@ -281,14 +281,28 @@ def layer_tokens(inputs: dict, wl, tokens=None, routed_rows=False, y_f32=False):
     """Whole layer for ``tokens`` (default: all).  ``inputs`` is the dict made
     by moe_inputs.make_inputs; ``wl`` the Workload.  Returns (out f64 [n,H],
     topk_idx [n,k], topk_w [n,k]), and with ``routed_rows`` also each slot's
-    routed expert output as bf16 bits [n,k,H].  ``y_f32``: the routed expert
-    outputs enter the weighted sum unrounded (the fp32-y reading)."""
+    routed expert output as bf16 bits [n,k,H].  ``y_f32``: ``out`` is the
+    fp32-y reading (routed expert outputs enter the weighted sum unrounded)."""
+    out, out_yf, idx, w, y = _layer(inputs, wl, tokens, routed_rows, y_f32)
+    o = out_yf if y_f32 else out
+    return (o, idx, w, y) if routed_rows else (o, idx, w)
+
+
+def layer_tokens_both(inputs: dict, wl, tokens=None):
+    """One pass of the layer giving both readings: (out with bf16 routed
+    outputs, out with unrounded routed outputs, topk_idx, topk_w, routed
+    rows as bf16 bits [n,k,H])."""
+    return _layer(inputs, wl, tokens, True, True)
+
+
+def _layer(inputs, wl, tokens, routed_rows, want_yf):
     x = _u16(inputs["x"])
     T, H = x.shape
     E, k, I, I_s = wl.E, wl.k, wl.I, wl.I_s
     tok = None if tokens is None else _arr(tokens, np.int32).reshape(-1)
     n = T if tok is None else tok.size
     out = np.empty((n, H), dtype=np.float64)
+    out_yf = np.empty((n, H), dtype=np.float64) if want_yf else None
     idx = np.empty((n, k), dtype=np.int32)
     w = np.empty((n, k), dtype=np.float32)
     y = np.empty((n, k, H), dtype=np.uint16) if routed_rows else None
@@ -303,9 +317,9 @@ def layer_tokens(inputs: dict, wl, tokens=None, routed_rows=False, y_f32=False):
         _p(x), T, H, E, k, I, I_s, int(wl.rmsnorm), ctypes.c_float(wl.eps),
         int(wl.renorm), _p(gamma), _p(wg), _p(bias), _p(w13), _p(w2), _p(w13_s),
         _p(w2_s), _p(tok), 0 if tok is None else tok.size, _p(out), _p(idx), _p(w), _p(y),
-        int(bool(y_f32)))
+        _p(out_yf))
     _check(rc, "oracle_layer_tokens")
-    return (out, idx, w, y) if routed_rows else (out, idx, w)
+    return out, out_yf, idx, w, y
 
 
 # ------------------------------------------------------------ EP local steps

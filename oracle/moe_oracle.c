@@ -399,15 +399,15 @@ int oracle_finalize_f64(const double *y_exp, const int32_t *row_idx, const float
 /* Outputs: out [n_tok,H] double; idx/w [n_tok,k] (may be NULL);            */
 /*   y_out [n_tok,k,H] bf16 (may be NULL): each slot's routed expert output,  */
 /*   rounded to bf16.                                                       */
-/* y_f32 != 0: the routed expert outputs enter the weighted sum unrounded    */
-/*   (the fp32-y reading); y_out still receives their bf16 roundings.       */
+/*   out_yf [n_tok,H] double (may be NULL): the same layer in the fp32-y    */
+/*   reading, the routed expert outputs entering the weighted sum unrounded. */
 int oracle_layer_tokens(const bf16_t *x, int64_t T, int64_t H, int64_t E, int64_t k,
                         int64_t I, int64_t I_s, int rmsnorm, float eps, int renorm,
                         const bf16_t *gamma, const float *wg, const float *bias,
                         const bf16_t *w13, const bf16_t *w2, const bf16_t *w13_s,
                         const bf16_t *w2_s, const int32_t *tokens, int64_t n_tok,
                         double *out, int32_t *idx_out, float *w_out, bf16_t *y_out,
-                        int y_f32)
+                        double *out_yf)
 {
     if (!x || !wg || !w13 || !w2 || !out || H <= 0 || E <= 0 || k < 1 || k > E ||
         I <= 0 || I_s < 0 || (I_s > 0 && (!w13_s || !w2_s)))
@@ -443,8 +443,12 @@ int oracle_layer_tokens(const bf16_t *x, int64_t T, int64_t H, int64_t E, int64_
         if ((rc = oracle_topk_softmax(logits, 1, E, k, renorm, idx, w)))
             goto done;
         double *o = out + n * H;
+        double *of = out_yf ? out_yf + n * H : NULL;
         for (int64_t c = 0; c < H; ++c)
             o[c] = 0.0;
+        if (of)
+            for (int64_t c = 0; c < H; ++c)
+                of[c] = 0.0;
         for (int64_t j = 0; j < k; ++j) {
             const int64_t e = idx[j];
             if ((rc = oracle_expert_mlp(xrow, 1, w13 + e * 2 * I * H, w2 + e * H * I,
@@ -453,13 +457,19 @@ int oracle_layer_tokens(const bf16_t *x, int64_t T, int64_t H, int64_t E, int64_
             if (y_out)
                 memcpy(y_out + (n * k + j) * H, yb, (size_t)H * sizeof(bf16_t));
             for (int64_t c = 0; c < H; ++c)
-                o[c] += (double)w[j] * (y_f32 ? yr[c] : (double)bf16_to_float(yb[c]));
+                o[c] += (double)w[j] * (double)bf16_to_float(yb[c]);
+            if (of)
+                for (int64_t c = 0; c < H; ++c)
+                    of[c] += (double)w[j] * yr[c];
         }
         if (I_s > 0) {
             if ((rc = oracle_expert_mlp(xrow, 1, w13_s, w2_s, H, I_s, NULL, NULL, ys)))
                 goto done;
             for (int64_t c = 0; c < H; ++c)
                 o[c] += ys[c];
+            if (of)
+                for (int64_t c = 0; c < H; ++c)
+                    of[c] += ys[c];
         }
         if (idx_out)
             memcpy(idx_out + n * k, idx, (size_t)k * sizeof(int32_t));

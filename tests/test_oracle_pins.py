@@ -286,10 +286,21 @@ def pin_layer_shared_rmsnorm():
     _, _, ys = oracle.expert_mlp(xn, d["w13_s"], d["w2_s"], want_f64=True)
     ref = oracle.finalize(y, r["row_idx"], w, ys)
     assert np.allclose(out, ref, rtol=1e-12, atol=1e-15)
+    # the fp32-y reading: the same composition over each group's unrounded rows
+    yf = np.zeros((ex.shape[0], wl.H))
+    w13b, w2b = d["w13"], d["w2"]
+    for e in range(wl.E):
+        r0, r1 = int(r["offsets"][e]), int(r["offsets"][e + 1])
+        if r1 > r0:
+            yf[r0:r1] = oracle.expert_mlp(ex[r0:r1], w13b[e], w2b[e], want_f64=True)[2]
+    out_f, _, _ = oracle.layer_tokens(d, wl, y_f32=True)
+    assert np.allclose(out_f, oracle.finalize(yf, r["row_idx"], w, ys), rtol=1e-12, atol=1e-15)
     # with the shared expert's weights zeroed the shared term vanishes
     d0 = dict(d, w2_s=torch.zeros_like(d["w2_s"]))
     out0, _, _ = oracle.layer_tokens(d0, wl)
     assert np.allclose(out - out0, ys, rtol=1e-12, atol=1e-15)
+    out0_f, _, _ = oracle.layer_tokens(d0, wl, y_f32=True)
+    assert np.allclose(out_f - out0_f, ys, rtol=1e-12, atol=1e-15)
 
 
 def pin_ep_local_rerouting():
@@ -354,7 +365,9 @@ MUTANTS = {
     "finalize_weight_index": ("(double)topk_w[t * k + j] *", "(double)topk_w[j] *"),
     "bf16_truncate": ("nearbyint(ldexp(m, 8))", "floor(ldexp(m, 8))"),
     "layer_shared_dropped": ("o[c] += ys[c];", "o[c] += 0.0;"),
-    "layer_y_f32_ignored": ("(y_f32 ? yr[c] :", "(0 ? yr[c] :"),
+    "layer_y_f32_rounded": ("of[c] += (double)w[j] * yr[c];",
+                            "of[c] += (double)w[j] * (double)bf16_to_float(yb[c]);"),
+    "layer_y_f32_no_shared": ("of[c] += ys[c];", "of[c] += 0.0;"),
     "finalize_f64_row_ignored": ("y_exp[(int64_t)row_idx[t * k + j] * H + c];",
                                  "y_exp[(int64_t)row_idx[t * k] * H + c];"),
     "ep_rank_off_by_one": ("for (int64_t rr = 0; rr < r; ++rr)",
