@@ -14,11 +14,22 @@ with CUDA events on the launching stream, max over ranks.  Per-stage times
 come from events the library records between its launches in the same
 timed steps (moe_layer_forward_timed).
 
-``roofline`` is the w13 matmul's: flops against the measured bf16 rate
-(sustained when the timed steps ran power-capped, else burst) when its flops
-per byte exceed the balance of the two measured peaks (many rows per
-expert), else bytes (the weights of the experts that get
-rows, once, plus the rows in and out) against the measured HBM copy rate.
+``roofline`` is the w13 matmul's: flops against the measured burst bf16
+rate (cuBLAS on this GPU) when its flops per byte exceed the balance of the
+two measured peaks (many rows per expert), else bytes (the weights of the
+experts that get rows, once, plus the rows in and out) against the measured
+HBM copy rate.  The burst rate is the peak when the median SM clock of the
+timed steps stayed within 3% of its maximum (an isolated power-cap sample
+does not change that), else the measured sustained (power-capped) rate.
+The same flops are also given against both measured rates and against
+GB300's nominal dense bf16 rate (2.25 PFLOP/s), as is and at the sampled
+clock.
+
+``steady_state`` loops the same layer for a few seconds with its own clock
+record: the power-capped regime a long multi-layer run settles in, next to
+the short timed region of ``value``.  ``y_f32`` times the layer with the
+routed expert outputs kept in fp32 (MOE_Y_F32), the mode whose output meets
+max-abs 2e-2 against the oracle with no per-element allowance.
 
 ``e2e`` is the same metric through moe_layer_forward_host on pinned host
 buffers: every step copies its tokens in and its output out (both inside
@@ -50,6 +61,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer tokens/s; grouped-GEMM TFLOP/s (% bf16 peak); routing GB/s"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_BF16_TFLOPS = 2250.0     # GB300 dense bf16 tensor rate, datasheet
 
 
 def parse_args():
@@ -77,6 +89,11 @@ def parse_args():
                     help="time one MoE tensor-parallel shard: I and I_shared divided by tp")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU work of the oracle baseline sample")
+    ap.add_argument("--y-f32", action="store_true",
+                    help="time the layer with fp32 routed expert outputs (MOE_Y_F32) as the "
+                         "main line")
+    ap.add_argument("--steady-seconds", type=float, default=4.0,
+                    help="length of the steady-state loop (0 skips it)")
     return ap.parse_args()
 
 
@@ -244,7 +261,7 @@ def cpu_oracle_rate(inputs_cpu, wl, seconds, first_token=0):
 
 
 # --------------------------------------------------------------- our arm
-def stage_bytes_flops(wl, two_streams=False, active=None):
+def stage_bytes_flops(wl, two_streams=False, active=None, y_f32=False):
     """Algorithmic work of each timed stage.  With two streams the row copies
     run on the second stream beside the shared expert's w13, so the permute
     stage of the main stream is empty and gets no bytes; both matmul stages
@@ -261,7 +278,8 @@ def stage_bytes_flops(wl, two_streams=False, active=None):
         "permute": {"bytes": 0 if two_streams else T * H * 2 + N * H * 2 + N * 4},
         "gemm_w13_swiglu": {"flops": 4.0 * N * H * I + 4.0 * T * H * Is},
         "gemm_down": {"flops": 2.0 * N * H * I + 2.0 * T * H * Is},
-        "finalize": {"bytes": N * H * 2 + (T * H * 4 if wl.I_s else 0) + T * H * 2 + N * 8},
+        "finalize": {"bytes": N * H * (4 if y_f32 else 2) + (T * H * 4 if wl.I_s else 0) +
+                     T * H * 2 + N * 8},
     }
     if active is not None:
         # w13: weights [2I, H] bf16, rows in bf16, SwiGLU rows out bf16; down:
@@ -269,7 +287,7 @@ def stage_bytes_flops(wl, two_streams=False, active=None):
         work["gemm_w13_swiglu"]["bytes"] = (active * 2 * I * H * 2 + 2 * Is * H * 2 +
                                             (N + (T if Is else 0)) * H * 2 + (N * I + T * Is) * 2)
         work["gemm_down"]["bytes"] = (active * H * I * 2 + H * Is * 2 + (N * I + T * Is) * 2 +
-                                      N * H * 2 + (T * H * 4 if Is else 0))
+                                      N * H * (4 if y_f32 else 2) + (T * H * 4 if Is else 0))
     return work
 
 
@@ -285,12 +303,33 @@ def active_experts(g, wl) -> int:
     return int((torch.bincount(idx.flatten().long(), minlength=wl.E) > 0).sum().item())
 
 
-def power_capped(clk) -> bool:
-    """Whether the clock record of the timed steps shows the power cap, or an
-    SM clock below 97% of its maximum; without a record, assume it does."""
-    if not clk or "sm_mhz" not in clk or "sm_max_mhz" not in clk:
-        return True
-    return "sw_power_cap" in clk.get("reasons", []) or clk["sm_mhz"] < 0.97 * clk["sm_max_mhz"]
+def clock_ratio(clk):
+    """Median SM clock of the timed steps over its maximum, or None without a
+    usable record."""
+    if not clk or not clk.get("sm_mhz") or not clk.get("sm_max_mhz"):
+        return None
+    return float(clk["sm_mhz"]) / float(clk["sm_max_mhz"])
+
+
+def tensor_peak(peaks, clk):
+    """(peak TFLOP/s, how it was chosen) for a matmul timed in the steps whose
+    clock record is `clk`: the measured burst rate when the median SM clock
+    stayed within 3% of its maximum (an isolated power-cap sample does not
+    change that), else the measured sustained rate, which the same matmul
+    reaches in the power-capped regime.  (The burst rate scaled by the
+    sampled clock is not used: under the power cap the matmuls here ran
+    above burst x median/max clock, so the sampled clock does not scale the
+    tensor rate linearly.)  Without a clock record: the sustained rate."""
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    r = clock_ratio(clk)
+    if r is None:
+        return sustained, "bf16_tflops_sustained (no clock record)"
+    if r >= 0.97:
+        return burst, "bf16_tflops (burst; median SM clock %.0f of %.0f MHz)" % (
+            clk["sm_mhz"], clk["sm_max_mhz"])
+    return sustained, "bf16_tflops_sustained (median SM clock %.0f of %.0f MHz)" % (
+        clk["sm_mhz"], clk["sm_max_mhz"])
 
 
 def gemm_bound(flops, nbytes, tc_peak_tflops, hbm_peak_gbs):
@@ -330,9 +369,15 @@ def run_ours(args, rank, world, local):
     g = rank_inputs(wl, args.seed, rank, str(dev))
     weights = moe.LayerWeights(wg=g["wg"], w13=g["w13"], w2=g["w2"], gamma=g["gamma"],
                                gate_bias=g["gate_bias"], w13_s=g["w13_s"], w2_s=g["w2_s"])
-    desc = moe.make_desc(wl.T, wl.H, wl.E, wl.k, wl.I, wl.I_s, rmsnorm=wl.rmsnorm, eps=wl.eps,
-                         renorm=wl.renorm, out_f32=False, gate_sequential=args.gate_sequential)
-    ws = torch.empty(moe.layer_workspace_size(desc), dtype=torch.uint8, device=dev)
+
+    def desc_for(y_f32):
+        return moe.make_desc(wl.T, wl.H, wl.E, wl.k, wl.I, wl.I_s, rmsnorm=wl.rmsnorm,
+                             eps=wl.eps, renorm=wl.renorm, out_f32=False,
+                             gate_sequential=args.gate_sequential, y_f32=y_f32)
+    desc = desc_for(args.y_f32)
+    alt_desc = desc_for(not args.y_f32)
+    ws = torch.empty(max(moe.layer_workspace_size(desc), moe.layer_workspace_size(alt_desc)),
+                     dtype=torch.uint8, device=dev)
     out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
     status = moe.new_status(dev)
     x = g["x"]
@@ -350,41 +395,89 @@ def run_ours(args, rank, world, local):
         for e in fj:
             e.record()
         extra = dict(shared_stream=s2, events=fj)
-    for _ in range(W):
-        moe.layer_forward(desc, x, weights, out=out, workspace=ws, status=status, **extra)
-    torch.cuda.synchronize()
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())} during warm-up")
-
     dist = world > 1
-    if dist:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record()
-    for i in range(K):
-        moe.layer_forward(desc, x, weights, out=out, workspace=ws, status=status,
-                          stage_events=evs[i], **extra)
-    end.record()
-    torch.cuda.synchronize()
-    if dist:
-        torch.distributed.barrier()
-    clk = clocks.stop()
-    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())} in the timed steps")
 
-    stage_ms = {}
-    for j, name in enumerate(moe.STAGE_NAMES):
-        stage_ms[name] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+    def step(d, i=None):
+        moe.layer_forward(d, x, weights, out=out, workspace=ws, status=status,
+                          stage_events=None if i is None else evs[i], **extra)
+
+    def check(where):
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())} {where}")
+
+    def timed(d, n):
+        """n steps between barrier + synchronisation, timed with events on the
+        stream; per-stage times from the library's own events."""
+        if dist:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        clocks = ClockSampler(local)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record()
+        for i in range(n):
+            step(d, i)
+        end.record()
+        torch.cuda.synchronize()
+        if dist:
+            torch.distributed.barrier()
+        clk = clocks.stop()
+        ms = max_over_ranks(start.elapsed_time(end), world, dev)
+        st_ms = {name: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
+                 for j, name in enumerate(moe.STAGE_NAMES)}
+        return ms, st_ms, clk
+
+    for _ in range(W):
+        step(desc)
+    torch.cuda.synchronize()
+    check("during warm-up")
+    elapsed_ms, stage_ms, clk = timed(desc, K)
+    check("in the timed steps")
+
+    # the other reading of the routed expert outputs, same number of steps
+    for _ in range(W):
+        step(alt_desc)
+    alt_ms, alt_stage_ms, alt_clk = timed(alt_desc, K)
+    check("in the timed steps of the other y mode")
+    alt = {"value": round(job_throughput(world, wl.T, K, alt_ms), 1),
+           "ms_per_step": round(alt_ms / K, 4),
+           "stages_ms": {k: round(v, 4) for k, v in alt_stage_ms.items()},
+           "clocks": alt_clk}
+
+    # steady state: the same layer looped for a few seconds (power-capped
+    # regime); stage times from the last K steps of the loop
+    steady = None
+    if args.steady_seconds > 0:
+        n_steady = max(K, int(args.steady_seconds * 1e3 / (elapsed_ms / K)))
+        if dist:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        clocks = ClockSampler(local)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record()
+        for i in range(n_steady):
+            step(desc, i - (n_steady - K) if i >= n_steady - K else None)
+        end.record()
+        torch.cuda.synchronize()
+        sclk = clocks.stop()
+        check("in the steady-state loop")
+        sms = max_over_ranks(start.elapsed_time(end), world, dev)
+        s_stage = {name: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+                   for j, name in enumerate(moe.STAGE_NAMES)}
+        steady = {"seconds": round(sms / 1e3, 3), "steps": n_steady,
+                  "value": round(job_throughput(world, wl.T, n_steady, sms), 1),
+                  "ms_per_step": round(sms / n_steady, 4),
+                  "stages_ms_last_steps": {k: round(v, 4) for k, v in s_stage.items()},
+                  "clocks": sclk}
+
     active = active_experts(g, wl)
+    res_extra = {"alt": alt, "steady": steady}
 
     # end to end on host buffers (pinned), through the same public call
     if args.no_e2e:
         return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, None, g,
-                           two_streams, active)
+                           two_streams, active, res_extra)
     # two host batches (this rank's tokens and a second draw) used in turn,
     # two host output buffers; every step copies its tokens in and its output
     # out, overlapped with the neighbouring steps' compute
@@ -407,35 +500,34 @@ def run_ours(args, rank, world, local):
     moe.layer_forward_host(desc, xs, weights, outs, staging=staging, workspace=ws,
                            status=status)          # returns once the last output is on the host
     e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())} in the end-to-end steps")
+    check("in the end-to-end steps")
     e2e_value = job_throughput(world, wl.T, Ke, e2e_ms)
     return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g,
-                       two_streams, active)
+                       two_streams, active, res_extra)
 
 
 def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g,
-                two_streams=False, active=None):
+                two_streams=False, active=None, res_extra=None):
     import moe_expert_routing_fp32_gb300 as moe  # noqa: F401
+    res_extra = res_extra or {}
     step_ms = elapsed_ms / K
     value = job_throughput(world, wl.T, K, elapsed_ms)
     peaks, peak_src = load_peaks()
     # the recorded DRAM bytes were captured on the named workload as-is, with
-    # the shared expert inside the w13 launch
+    # the shared expert inside the w13 launch and bf16 routed outputs
     from moe_inputs import WORKLOADS
     traffic_applies = wl == WORKLOADS[args.workload] and not two_streams
-    work = stage_bytes_flops(wl, two_streams, wl.E if active is None else active)
+    work = stage_bytes_flops(wl, two_streams, wl.E if active is None else active, args.y_f32)
     dom = "gemm_w13_swiglu"
     dom_s = stage_ms[dom] / 1e3
-    # the sustained matmul rate when the timed steps ran power-capped (or the
-    # clock sat below its maximum), else the burst rate
-    tc_key = "bf16_tflops_sustained" if power_capped(clk) else "bf16_tflops"
-    tc_peak = float(peaks.get(tc_key, FALLBACK_PEAKS[tc_key]))
+    tc_peak, tc_how = tensor_peak(peaks, clk)
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     bound = gemm_bound(work[dom]["flops"], work[dom]["bytes"], tc_peak, hbm_peak)
+    ratio = clock_ratio(clk)
     if bound == "tensor":
         achieved, peak, punit = work[dom]["flops"] / dom_s / 1e12, tc_peak, "TFLOP/s"
-        psrc = f"{tc_key} ({peak_src})"
+        psrc = f"{tc_how} ({peak_src})"
     else:
         achieved, peak, punit = work[dom]["bytes"] / dom_s / 1e9, hbm_peak, "GB/s"
         psrc = f"hbm_gbs ({peak_src})"
@@ -452,6 +544,7 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
         if "flops" in wk and name.startswith("gemm"):
             e["tflops"] = round(wk["flops"] / (ms / 1e3) / 1e12, 1)
             e["frac_bf16_peak"] = round(e["tflops"] / tc_peak, 4)
+            e["frac_nominal_bf16"] = round(e["tflops"] / NOMINAL_BF16_TFLOPS, 4)
         if "bytes" in wk:
             e["gbs"] = round(wk["bytes"] / (ms / 1e3) / 1e9, 1)
             e["frac_hbm"] = round(e["gbs"] / hbm_peak, 4)
@@ -459,7 +552,22 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
             e["gate_fp32_tflops"] = round(wk["gate_flops"] / (ms / 1e3) / 1e12, 2)
         per_stage[name] = e
 
+    roof = {"bound": bound, "kernel": dom, "achieved": round(achieved, 1),
+            "peak": round(peak, 1), "unit": punit, "frac": round(achieved / peak, 4),
+            "peak_source": psrc,
+            "traffic": recorded_traffic(wl.name) if traffic_applies and not args.y_f32
+            else None}
+    if bound == "tensor":
+        w13_tf = work[dom]["flops"] / dom_s / 1e12
+        burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        roof["frac_of_burst"] = round(w13_tf / burst, 4)
+        roof["frac_of_sustained"] = round(w13_tf / sustained, 4)
+        roof["frac_nominal_dense_bf16"] = round(w13_tf / NOMINAL_BF16_TFLOPS, 4)
+        if ratio:
+            roof["frac_nominal_at_sampled_clock"] = round(
+                w13_tf / (NOMINAL_BF16_TFLOPS * min(ratio, 1.0)), 4)
     launches = launches_per_step(wl, args.gate_sequential, two_streams)
+    y_mode = "fp32 (MOE_Y_F32)" if args.y_f32 else "bf16"
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
@@ -467,16 +575,14 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) random-init weights)",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
                    "I_shared": wl.I_s, "rmsnorm": wl.rmsnorm, "out": "bf16",
+                   "routed_expert_outputs": y_mode,
                    "shared_expert": ("none" if not wl.I_s else
                                      "second stream" if two_streams else "same launches"),
                    "gate": ("fp32, sequential FMA order" if args.gate_sequential or wl.T <= 512
                             else "fp32 on the tensor cores (exact 3-part bf16 split of Wg)"),
                    "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 1),
-                     "peak": peak, "unit": punit, "frac": round(achieved / peak, 4),
-                     "peak_source": psrc,
-                     "traffic": recorded_traffic(wl.name) if traffic_applies else None},
+        "roofline": roof,
         "gemm_tflops": round(gemm_tflops, 1),
         "gemm_frac_bf16_peak": round(gemm_tflops / tc_peak, 4),
         "layer_gemm_tflops_over_step": round(layer_gemm_tflops, 1),
@@ -488,6 +594,16 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
         "gpu_launches": launches * K,
         "clocks": clk,
     }
+    alt = res_extra.get("alt")
+    if alt is not None:
+        res["y_bf16" if args.y_f32 else "y_f32"] = alt
+    if res_extra.get("steady") is not None:
+        st = dict(res_extra["steady"])
+        sw13 = st["stages_ms_last_steps"][dom] / 1e3
+        if bound == "tensor":
+            st["w13_tflops"] = round(work[dom]["flops"] / sw13 / 1e12, 1)
+            st["w13_frac_of_sustained"] = round(work[dom]["flops"] / sw13 / 1e12 / sustained, 4)
+        res["steady_state"] = st
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in g.items()}
         rate, n, dt = cpu_oracle_rate(cpu, wl, args.cpu_seconds)

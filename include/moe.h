@@ -66,8 +66,11 @@ enum {
     MOE_SHARED = 1u << 2,      /* add the shared expert */
     MOE_OUT_F32 = 1u << 3,     /* layer / finalize output in fp32 (else bf16) */
     MOE_SHARED_F32 = 1u << 4,  /* finalize: `shared` is fp32 (else bf16) */
-    MOE_GATE_SEQUENTIAL = 1u << 5  /* layer: the sequential fp32 gate for every T
+    MOE_GATE_SEQUENTIAL = 1u << 5, /* layer: the sequential fp32 gate for every T
                                       (see moe_gate_tensor for the default) */
+    MOE_Y_F32 = 1u << 6            /* layer: keep the routed expert outputs y_exp in
+                                      fp32, the down matmul's accumulator, instead of
+                                      rounding them to bf16 (finalize: y_exp is fp32) */
 };
 
 typedef struct {
@@ -79,7 +82,7 @@ typedef struct {
     int32_t I_shared;   /* shared expert intermediate size (MOE_SHARED) */
     float rms_eps;      /* RMSNorm epsilon (MOE_RMSNORM) */
     uint32_t flags;     /* MOE_RENORM | MOE_RMSNORM | MOE_SHARED | MOE_OUT_F32 |
-                           MOE_GATE_SEQUENTIAL */
+                           MOE_GATE_SEQUENTIAL | MOE_Y_F32 */
 } moe_desc_t;
 
 /* Human-readable name of a moe_status_t value. */
@@ -235,11 +238,12 @@ moe_status_t moe_grouped_mlp(const moe_bf16_t *expanded_x, const int32_t *offset
  *               + shared[t, :]
  * summed in fp32 in slot order j = 0..k-1, the shared term last; no atomics,
  * so the result is deterministic.
- *   y_exp [T*k, H] bf16; expanded_row_idx [T*k]; topk_w [T, k] fp32
+ *   y_exp [T*k, H] bf16 (fp32 with MOE_Y_F32); expanded_row_idx [T*k];
+ *   topk_w [T, k] fp32
  *   shared [T, H] bf16 (fp32 with MOE_SHARED_F32) or NULL
  *   out [T, H] bf16 (fp32 with MOE_OUT_F32)
  */
-moe_status_t moe_finalize_routing(const moe_bf16_t *y_exp, const int32_t *expanded_row_idx,
+moe_status_t moe_finalize_routing(const void *y_exp, const int32_t *expanded_row_idx,
                                   const float *topk_w, const void *shared, int32_t T,
                                   int32_t H, int32_t k, uint32_t flags, void *out,
                                   moe_stream_t stream);
@@ -251,7 +255,12 @@ moe_status_t moe_finalize_routing(const moe_bf16_t *y_exp, const int32_t *expand
  *   w13_s [2I_s,H], w2_s [H,I_s] bf16 (MOE_SHARED, else NULL);
  *   out [T,H] bf16 (fp32 with MOE_OUT_F32).
  * The shared expert runs on the normalised rows with weight 1 and its output
- * enters the final sum in fp32.  For T > 512 the gate is moe_gate_tensor's
+ * enters the final sum in fp32.  The routed expert outputs are rounded to
+ * bf16 before the weighted sum (a grouped matmul's output type), or, with
+ * MOE_Y_F32, enter it as the down matmul's fp32 accumulator: then nothing
+ * between the two matmuls' fp32 sums and the weighted sum is rounded except
+ * the SwiGLU output (twice the y_exp bytes: one more write and read of
+ * T*k*H*2 bytes per layer).  For T > 512 the gate is moe_gate_tensor's
  * (fp32-accurate, another summation order) unless MOE_GATE_SEQUENTIAL is set;
  * smaller batches always use the sequential gate of moe_rmsnorm_gate.
  * Workspace: moe_layer_workspace_size() bytes,

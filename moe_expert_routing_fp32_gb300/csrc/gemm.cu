@@ -7,7 +7,7 @@
 //
 // One persistent kernel serves both matmuls of the expert FFN:
 //   SWIGLU: act[r, n] = bf16(SiLU(g) * u), g = A[r] . W[grp, n], u = A[r] . W[grp, half + n]
-//   STORE:  out[r, n] = A[r] . W[grp, n]          (bf16, or fp32 for segment 1)
+//   STORE:  out[r, n] = A[r] . W[grp, n]          (bf16, or fp32 per segment)
 // over ragged groups: group g owns rows [offsets[g], offsets[g+1]) of A and
 // weight slice W[g].  An optional dense "segment 1" (the shared expert, its
 // own A, W and output) is appended to the same tile list.
@@ -72,6 +72,7 @@ struct Params {
     int64_t ldo0;
     void *out1;
     int64_t ldo1;
+    int32_t out0_f32;   // store mode: routed output in fp32 (else bf16)
     int32_t out1_f32;
     int32_t *dev_status;
     unsigned int *tile_counter;   // pair kernel: next tile to hand out (zeroed per launch)
@@ -372,7 +373,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
                     }
                 }
             } else {
-                const bool f32 = t.seg == 1 && p.out1_f32;
+                const bool f32 = (t.seg == 0 ? p.out0_f32 : p.out1_f32) != 0;
                 void *outp = t.seg == 0 ? p.out0 : p.out1;
                 const int64_t ldo = t.seg == 0 ? p.ldo0 : p.ldo1;
 #pragma unroll 1
@@ -874,7 +875,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     }
                 }
             } else {
-                const bool f32 = t.seg == 1 && p.out1_f32;
+                const bool f32 = (t.seg == 0 ? p.out0_f32 : p.out1_f32) != 0;
                 void *outp = t.seg == 0 ? p.out0 : p.out1;
                 const int64_t ldo = t.seg == 0 ? p.ldo0 : p.ldo1;
                 const int ncol = t.half ? BN / 2 : BN;
@@ -1000,7 +1001,8 @@ bool make_out_map(CUtensorMap *m, void *ptr, int rows, int cols, int64_t ld, boo
 // Both output maps of a launch (a missing segment reuses the other's map).
 bool make_out_maps(Params &p, int cols0, int cols1) {
     const bool have0 = p.G > 0, have1 = p.rows1 > 0;
-    if (have0 && !make_out_map(&p.tmO0, p.out0, p.rows0, cols0, p.ldo0, false)) return false;
+    if (have0 && !make_out_map(&p.tmO0, p.out0, p.rows0, cols0, p.ldo0, p.out0_f32 != 0))
+        return false;
     if (have1 && !make_out_map(&p.tmO1, p.out1, p.rows1, cols1, p.ldo1, p.out1_f32 != 0))
         return false;
     if (!have0) p.tmO0 = p.tmO1;
@@ -1191,6 +1193,7 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
     p.ldo0 = N;
     p.out1 = seg1.out;
     p.ldo1 = seg1.N1;
+    p.out0_f32 = 0;
     p.out1_f32 = 0;
     p.dev_status = dev_status;
     if (pair) {
@@ -1223,8 +1226,8 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
 }
 
 cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, int n, int K,
-                              const uint16_t *W, int N, uint16_t *y, const GemmSegment1 &seg1,
-                              int32_t *dev_status, cudaStream_t stream) {
+                              const uint16_t *W, int N, void *y, const GemmSegment1 &seg1,
+                              int32_t *dev_status, cudaStream_t stream, bool y_f32) {
     if (G > MAX_GROUPS) return cudaErrorInvalidValue;
     const int BN = (N % 256 == 0 && (seg1.rows == 0 || seg1.N1 % 256 == 0)) ? 256 : 128;
     const bool pair = BN == 256 && use_pair(n, G, seg1.rows) && K % 128 == 0 &&
@@ -1268,6 +1271,7 @@ cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, 
     p.ldo0 = N;
     p.out1 = seg1.out;
     p.ldo1 = seg1.N1;
+    p.out0_f32 = y_f32 ? 1 : 0;
     p.out1_f32 = seg1.out_f32 ? 1 : 0;
     p.dev_status = dev_status;
     if (pair) {

@@ -22,6 +22,9 @@ constexpr int kGateSmallMaxT = 512;
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int num_sms();  // of the current device (cached)
+// whether the current device is of the sm_100 family (looked up once per
+// device; a failed lookup leaves no CUDA error pending)
+bool current_device_ok();
 
 // ---- router.cu
 // RMSNorm (optional) + fp32 gate.  If fuse_topk (requires E <= 64), also
@@ -73,9 +76,11 @@ cudaError_t launch_permute(const uint16_t *xs, const int32_t *row_idx, int T, in
                            uint16_t *expanded_x, cudaStream_t stream);
 cudaError_t launch_expert_tokens(const int32_t *ids, int n, int E, int32_t *counts,
                                  int32_t *offsets, int32_t *dev_status, cudaStream_t stream);
-cudaError_t launch_finalize(const uint16_t *y_exp, const int32_t *row_idx, const float *topk_w,
-                            const void *shared, bool shared_f32, int T, int H, int k,
-                            void *out, bool out_f32, cudaStream_t stream);
+// y_exp is bf16, or fp32 with y_f32 (the routed rows kept at the matmul's
+// accumulator precision)
+cudaError_t launch_finalize(const void *y_exp, bool y_f32, const int32_t *row_idx,
+                            const float *topk_w, const void *shared, bool shared_f32, int T,
+                            int H, int k, void *out, bool out_f32, cudaStream_t stream);
 
 // ---- gemm.cu
 struct GemmSegment1 {       // an optional dense problem appended to the grouped one
@@ -94,10 +99,10 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
                                const uint16_t *W13, int N, uint16_t *act,
                                const GemmSegment1 &seg1, int32_t *dev_status,
                                cudaStream_t stream);
-// y[r, :] = bf16(A W^T) per group; A [n, K], W [G, N, K]
+// y[r, :] = bf16(A W^T) per group (fp32, unrounded, with y_f32); A [n, K], W [G, N, K]
 cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, int n, int K,
-                              const uint16_t *W, int N, uint16_t *y, const GemmSegment1 &seg1,
-                              int32_t *dev_status, cudaStream_t stream);
+                              const uint16_t *W, int N, void *y, const GemmSegment1 &seg1,
+                              int32_t *dev_status, cudaStream_t stream, bool y_f32 = false);
 bool tensor_maps_available();
 
 }  // namespace moe

@@ -30,18 +30,11 @@ DeviceInfo &device_info(int dev) {
         if (cudaGetDeviceProperties(&prop, dev) == cudaSuccess) {
             info[dev].sms = prop.multiProcessorCount;
             info[dev].ok = prop.major == 10;   // the sm_100 family (sm_103a build)
+        } else {
+            cudaGetLastError();   // leave no error pending for later launches
         }
     });
     return info[dev];
-}
-
-bool current_device_ok() {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        cudaGetLastError();
-        return false;
-    }
-    return device_info(dev).ok;
 }
 
 inline bool a16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -126,7 +119,7 @@ LayerWs layer_layout(const moe_desc_t &d) {
     L.row_idx = take(N * 4);
     L.expanded_x = take(N * H * 2);
     L.act = take(N * I * 2);
-    L.y = take(N * H * 2);
+    L.y = take(N * H * ((d.flags & MOE_Y_F32) ? 4 : 2));
     if (d.flags & MOE_SHARED) {
         L.act_s = take(T * Is * 2);
         L.y_s = take(T * H * 4);
@@ -150,6 +143,15 @@ moe_status_t check_desc(const moe_desc_t *d) {
 }
 
 }  // namespace
+
+bool current_device_ok() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return false;
+    }
+    return device_info(dev).ok;
+}
 
 int num_sms() {
     int dev = 0;
@@ -322,7 +324,7 @@ moe_status_t moe_grouped_mlp(const moe_bf16_t *expanded_x, const int32_t *offset
     return MOE_OK;
 }
 
-moe_status_t moe_finalize_routing(const moe_bf16_t *y_exp, const int32_t *expanded_row_idx,
+moe_status_t moe_finalize_routing(const void *y_exp, const int32_t *expanded_row_idx,
                                   const float *topk_w, const void *shared, int32_t T, int32_t H,
                                   int32_t k, uint32_t flags, void *out, moe_stream_t stream) {
     if (T < 0 || H <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
@@ -331,7 +333,7 @@ moe_status_t moe_finalize_routing(const moe_bf16_t *y_exp, const int32_t *expand
     if (!y_exp || !expanded_row_idx || !topk_w || !out) return MOE_ERR_INVALID_ARG;
     if (!a16(y_exp) || !a16(out) || (shared && !a16(shared))) return MOE_ERR_INVALID_ARG;
     if (!current_device_ok()) return MOE_ERR_NO_DEVICE;
-    MOE_TRY(launch_finalize(y_exp, expanded_row_idx, topk_w, shared,
+    MOE_TRY(launch_finalize(y_exp, (flags & MOE_Y_F32) != 0, expanded_row_idx, topk_w, shared,
                             (flags & MOE_SHARED_F32) != 0, T, H, k, out,
                             (flags & MOE_OUT_F32) != 0, reinterpret_cast<cudaStream_t>(stream)));
     return MOE_OK;
@@ -390,7 +392,8 @@ moe_status_t layer_forward_impl(const moe_desc_t *desc, const moe_bf16_t *x,
     int32_t *row_idx = static_cast<int32_t *>(at(L.row_idx));
     uint16_t *ex = static_cast<uint16_t *>(at(L.expanded_x));
     uint16_t *act = static_cast<uint16_t *>(at(L.act));
-    uint16_t *y = static_cast<uint16_t *>(at(L.y));
+    void *y = at(L.y);   // bf16, or fp32 with MOE_Y_F32
+    const bool y_f32 = (d.flags & MOE_Y_F32) != 0;
     uint16_t *act_s = shared ? static_cast<uint16_t *>(at(L.act_s)) : nullptr;
     float *y_s = shared ? static_cast<float *>(at(L.y_s)) : nullptr;
     const uint16_t *xs = rms ? xn : x;
@@ -493,10 +496,10 @@ moe_status_t layer_forward_impl(const moe_desc_t *desc, const moe_bf16_t *x,
         s2.out_f32 = true;
     }
     MOE_TRY(mark(4));
-    MOE_TRY(launch_gemm_store(act, offsets, E, N, I, w2, H, y, s2, dev_status, s));
+    MOE_TRY(launch_gemm_store(act, offsets, E, N, I, w2, H, y, s2, dev_status, s, y_f32));
     // 5. finalize: weighted sum in slot order + shared row
     MOE_TRY(mark(5));
-    MOE_TRY(launch_finalize(y, row_idx, w, y_s, true, T, H, k, out,
+    MOE_TRY(launch_finalize(y, y_f32, row_idx, w, y_s, true, T, H, k, out,
                             (d.flags & MOE_OUT_F32) != 0, s));
     MOE_TRY(mark(6));
     return MOE_OK;

@@ -42,13 +42,19 @@ ScratchSlot g_slots[kMaxDev];
 cudaError_t scratch_for_current_device(int32_t **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e;
+    }
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     ScratchSlot &s = g_slots[dev];
     std::call_once(s.once, [&s] {
         void *p = nullptr;
         s.err = cudaGetSymbolAddress(&p, g_route_scratch);
-        if (s.err == cudaSuccess) s.ptr = static_cast<int32_t *>(p);
+        if (s.err == cudaSuccess)
+            s.ptr = static_cast<int32_t *>(p);
+        else
+            cudaGetLastError();   // leave no error pending for later launches
     });
     if (s.err != cudaSuccess) return s.err;
     *out = s.ptr;
@@ -79,14 +85,7 @@ extern "C" moe_status_t moe_init_routing_noalloc(
     const int B = static_cast<int>(ceil_div(T, kChunkTokens));
     if (static_cast<size_t>(B) * static_cast<size_t>(E) > kNoAllocScratchInts)
         return MOE_ERR_WORKSPACE_TOO_SMALL;
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return MOE_ERR_NO_DEVICE;
-    }
-    cudaDeviceProp prop;
-    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess || prop.major != 10)
-        return MOE_ERR_NO_DEVICE;
+    if (!current_device_ok()) return MOE_ERR_NO_DEVICE;   // cached per device
     int32_t *hist = nullptr;
     if (scratch_for_current_device(&hist) != cudaSuccess) return MOE_ERR_CUDA;
 

@@ -263,9 +263,10 @@ expert_tokens_kernel(const int32_t *__restrict__ ids, int n, int E, int32_t *__r
 // memory; a lane then issues the loads of 8 slots' 16-byte pieces before it
 // accumulates them (in slot order).  blockIdx.y splits the row's columns
 // when there are few tokens.
-template <bool SHARED_F32, bool OUT_F32>
+// Y_F32: the routed rows are fp32 (the down matmul's unrounded accumulator)
+template <bool Y_F32, bool SHARED_F32, bool OUT_F32>
 __global__ void __launch_bounds__(128)
-finalize_kernel(const uint16_t *__restrict__ y_exp, const int32_t *__restrict__ row_idx,
+finalize_kernel(const void *__restrict__ y_exp, const int32_t *__restrict__ row_idx,
                 const float *__restrict__ topk_w, const void *__restrict__ shared, int T, int H,
                 int k, void *__restrict__ out) {
     __shared__ int s_row[32];
@@ -286,27 +287,61 @@ finalize_kernel(const uint16_t *__restrict__ y_exp, const int32_t *__restrict__ 
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
             for (int j0 = 0; j0 < k; j0 += 8) {
-                uint4 q[8];
+                if (Y_F32) {
+                    // eight slots' loads in flight, then the sums in slot order
+                    float4 qa[8], qb[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int j = j0 + u;
-                    const int row = j < k ? s_row[j] : -1;
-                    q[u] = row >= 0
-                               ? __ldg(reinterpret_cast<const uint4 *>(
-                                           y_exp + static_cast<size_t>(row) * H) + v)
-                               : make_uint4(0u, 0u, 0u, 0u);
-                }
+                    for (int u = 0; u < 8; ++u) {
+                        const int j = j0 + u;
+                        const int row = j < k ? s_row[j] : -1;
+                        if (row >= 0) {
+                            const float4 *src = reinterpret_cast<const float4 *>(
+                                static_cast<const float *>(y_exp) + static_cast<size_t>(row) * H);
+                            qa[u] = __ldg(src + 2 * v);
+                            qb[u] = __ldg(src + 2 * v + 1);
+                        } else {
+                            qa[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            qb[u] = qa[u];
+                        }
+                    }
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int j = j0 + u;
-                    if (j >= k || s_row[j] < 0) continue;
-                    const float w = s_w[j];
-                    const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+                    for (int u = 0; u < 8; ++u) {
+                        const int j = j0 + u;
+                        if (j >= k || s_row[j] < 0) continue;
+                        const float w = s_w[j];
+                        acc[0] = __fmaf_rn(w, qa[u].x, acc[0]);
+                        acc[1] = __fmaf_rn(w, qa[u].y, acc[1]);
+                        acc[2] = __fmaf_rn(w, qa[u].z, acc[2]);
+                        acc[3] = __fmaf_rn(w, qa[u].w, acc[3]);
+                        acc[4] = __fmaf_rn(w, qb[u].x, acc[4]);
+                        acc[5] = __fmaf_rn(w, qb[u].y, acc[5]);
+                        acc[6] = __fmaf_rn(w, qb[u].z, acc[6]);
+                        acc[7] = __fmaf_rn(w, qb[u].w, acc[7]);
+                    }
+                } else {
+                    uint4 q[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        acc[2 * i] = __fmaf_rn(w, __uint_as_float(wd[i] << 16), acc[2 * i]);
-                        acc[2 * i + 1] =
-                            __fmaf_rn(w, __uint_as_float(wd[i] & 0xFFFF0000u), acc[2 * i + 1]);
+                    for (int u = 0; u < 8; ++u) {
+                        const int j = j0 + u;
+                        const int row = j < k ? s_row[j] : -1;
+                        q[u] = row >= 0
+                                   ? __ldg(reinterpret_cast<const uint4 *>(
+                                               static_cast<const uint16_t *>(y_exp) +
+                                               static_cast<size_t>(row) * H) + v)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int j = j0 + u;
+                        if (j >= k || s_row[j] < 0) continue;
+                        const float w = s_w[j];
+                        const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            acc[2 * i] = __fmaf_rn(w, __uint_as_float(wd[i] << 16), acc[2 * i]);
+                            acc[2 * i + 1] =
+                                __fmaf_rn(w, __uint_as_float(wd[i] & 0xFFFF0000u), acc[2 * i + 1]);
+                        }
                     }
                 }
             }
@@ -399,9 +434,27 @@ cudaError_t launch_expert_tokens(const int32_t *ids, int n, int E, int32_t *coun
     return cudaGetLastError();
 }
 
-cudaError_t launch_finalize(const uint16_t *y_exp, const int32_t *row_idx, const float *topk_w,
-                            const void *shared, bool shared_f32, int T, int H, int k,
-                            void *out, bool out_f32, cudaStream_t stream) {
+template <bool Y_F32>
+void launch_finalize_t(const void *y_exp, const int32_t *row_idx, const float *topk_w,
+                       const void *shared, bool shared_f32, int T, int H, int k, void *out,
+                       bool out_f32, dim3 grid, cudaStream_t stream) {
+    if (shared_f32 && out_f32)
+        finalize_kernel<Y_F32, true, true><<<grid, 128, 0, stream>>>(y_exp, row_idx, topk_w,
+                                                                     shared, T, H, k, out);
+    else if (shared_f32)
+        finalize_kernel<Y_F32, true, false><<<grid, 128, 0, stream>>>(y_exp, row_idx, topk_w,
+                                                                      shared, T, H, k, out);
+    else if (out_f32)
+        finalize_kernel<Y_F32, false, true><<<grid, 128, 0, stream>>>(y_exp, row_idx, topk_w,
+                                                                      shared, T, H, k, out);
+    else
+        finalize_kernel<Y_F32, false, false><<<grid, 128, 0, stream>>>(y_exp, row_idx, topk_w,
+                                                                       shared, T, H, k, out);
+}
+
+cudaError_t launch_finalize(const void *y_exp, bool y_f32, const int32_t *row_idx,
+                            const float *topk_w, const void *shared, bool shared_f32, int T,
+                            int H, int k, void *out, bool out_f32, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     // few tokens: split each row's columns over blocks (>= 128 vectors each)
     // so that about two blocks per SM run
@@ -411,18 +464,12 @@ cudaError_t launch_finalize(const uint16_t *y_exp, const int32_t *row_idx, const
                                  : static_cast<int>(std::max<int64_t>(
                                        1, std::min<int64_t>(ceil_div(want, T), nvec / 128)));
     const dim3 grid(static_cast<unsigned>(grid_for_rows(T, 16)), static_cast<unsigned>(ysplit));
-    if (shared_f32 && out_f32)
-        finalize_kernel<true, true><<<grid, 128, 0, stream>>>(y_exp, row_idx, topk_w, shared, T,
-                                                              H, k, out);
-    else if (shared_f32)
-        finalize_kernel<true, false><<<grid, 128, 0, stream>>>(y_exp, row_idx, topk_w, shared, T,
-                                                               H, k, out);
-    else if (out_f32)
-        finalize_kernel<false, true><<<grid, 128, 0, stream>>>(y_exp, row_idx, topk_w, shared, T,
-                                                               H, k, out);
+    if (y_f32)
+        launch_finalize_t<true>(y_exp, row_idx, topk_w, shared, shared_f32, T, H, k, out, out_f32,
+                                grid, stream);
     else
-        finalize_kernel<false, false><<<grid, 128, 0, stream>>>(y_exp, row_idx, topk_w, shared,
-                                                                T, H, k, out);
+        launch_finalize_t<false>(y_exp, row_idx, topk_w, shared, shared_f32, T, H, k, out,
+                                 out_f32, grid, stream);
     return cudaGetLastError();
 }
 

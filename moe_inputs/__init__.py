@@ -59,7 +59,9 @@ class Workload:
 # digits) for which the seed-0 draw on a CUDA device (the draw the GPU tests
 # and the benchmark use) leaves 16 of 64 experts without a token.  Found by
 # tests/golden/calibrate_skew.py --device cuda, which takes the routing
-# decisions from the oracle only (the seed-0 CPU draw gives 2.51).
+# decisions from the oracle only; its output is
+# tests/golden/skew_calibration_cuda.json (the seed-0 CPU draw gives 2.51,
+# tests/golden/skew_calibration.json).
 SKEW_BETA_SEED0 = 2.58
 
 WORKLOADS = {

@@ -4,7 +4,8 @@ seed-0 draw leaves 16 of the 64 experts (25%) without any token.
 
 The routing decisions come from the oracle only (its fp32 gate and its
 top-k); the inputs come from moe_inputs.  The result is written to
-skew_calibration.json beside this script and copied by hand into
+skew_calibration.json beside this script (or --out); the CUDA draw's result,
+skew_calibration_cuda.json, is the value copied by hand into
 moe_inputs.SKEW_BETA_SEED0.
 
     python tests/golden/calibrate_skew.py [--device cpu|cuda]

@@ -16,7 +16,7 @@ from moe_inputs import WORKLOADS  # noqa: E402
 def _args(**kw):
     a = dict(workload="imagegen-16k", no_cpu_baseline=True, cpu_seconds=0.1, gpus=1, steps=10,
              warmup=3, T=None, E=None, I=None, Is=None, tp=1, shared_stream="off", seed=0,
-             no_e2e=False, impl="ours", gate_sequential=False)
+             no_e2e=False, impl="ours", gate_sequential=False, y_f32=False, steady_seconds=0.0)
     a.update(kw)
     return argparse.Namespace(**a)
 
@@ -103,16 +103,50 @@ def test_roofline_bound_follows_the_arithmetic_intensity():
 
 
 def test_tensor_peak_follows_the_clock_record():
-    """Power-capped steps are measured against the sustained matmul rate,
-    steps at full clock against the burst rate."""
+    """The matmul is measured against the burst matmul rate when the median
+    SM clock of its timed steps stayed within 3% of the maximum (whatever an
+    isolated power-cap sample says), else, and with no clock record, against
+    the sustained rate.  Both measured rates and the nominal dense bf16 rate
+    appear beside it."""
     wl = WORKLOADS["balanced-4k"]
-    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
-    assert not bench.power_capped(full) and bench.power_capped(CLK) and bench.power_capped({})
-    assert bench.power_capped({"sm_mhz": 1800.0, "sm_max_mhz": 2070.0, "reasons": []})
     peaks, _ = bench.load_peaks()
-    r = bench.finish_ours(_args(workload="balanced-4k"), wl, 1, 0, 10, 3, 4.5, _stages(0.1), full,
+    burst = peaks["bf16_tflops"]
+    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    capped_sample = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    for clk in (full, capped_sample):
+        p, how = bench.tensor_peak(peaks, clk)
+        assert p == pytest.approx(burst) and how.startswith("bf16_tflops (burst")
+    p, how = bench.tensor_peak(peaks, CLK)
+    assert p == pytest.approx(peaks["bf16_tflops_sustained"]) and "sustained" in how
+    p, how = bench.tensor_peak(peaks, {})
+    assert p == pytest.approx(peaks["bf16_tflops_sustained"])
+    stages = _stages(0.1)
+    stages["gemm_w13_swiglu"] = 0.2
+    r = bench.finish_ours(_args(workload="balanced-4k"), wl, 1, 0, 10, 3, 4.5, stages, full,
                           None, {})["roofline"]
-    assert r["peak"] == pytest.approx(peaks["bf16_tflops"]) and r["peak_source"].startswith("bf16_tflops ")
-    r = bench.finish_ours(_args(workload="balanced-4k"), wl, 1, 0, 10, 3, 4.5, _stages(0.1), CLK,
+    flops = 4.0 * wl.T * wl.k * wl.H * wl.I
+    assert r["peak"] == pytest.approx(burst, rel=1e-3)
+    assert r["frac"] == pytest.approx(flops / 0.2e-3 / 1e12 / burst, rel=1e-3)
+    assert r["frac_nominal_dense_bf16"] == pytest.approx(flops / 0.2e-3 / 1e12 / 2250.0, rel=1e-3)
+    assert r["frac_of_sustained"] == pytest.approx(
+        flops / 0.2e-3 / 1e12 / peaks["bf16_tflops_sustained"], rel=1e-3)
+    r = bench.finish_ours(_args(workload="balanced-4k"), wl, 1, 0, 10, 3, 4.5, stages, CLK,
                           None, {})["roofline"]
-    assert r["peak"] == pytest.approx(peaks["bf16_tflops_sustained"])
+    assert r["peak"] == pytest.approx(peaks["bf16_tflops_sustained"], rel=1e-3)
+    assert r["frac_of_burst"] == pytest.approx(flops / 0.2e-3 / 1e12 / burst, rel=1e-3)
+    assert r["frac_nominal_at_sampled_clock"] == pytest.approx(
+        flops / 0.2e-3 / 1e12 / (2250.0 * 1700.0 / 2070.0), rel=1e-3)
+
+
+def test_y_f32_mode_counts_fp32_routed_rows():
+    """With fp32 routed expert outputs the down matmul writes and finalize
+    reads four bytes per element instead of two."""
+    wl = WORKLOADS["imagegen-16k"]
+    N, H = wl.T * wl.k, wl.H
+    a = bench.stage_bytes_flops(wl, active=wl.E)
+    b = bench.stage_bytes_flops(wl, active=wl.E, y_f32=True)
+    assert b["finalize"]["bytes"] - a["finalize"]["bytes"] == N * H * 2
+    assert b["gemm_down"]["bytes"] - a["gemm_down"]["bytes"] == N * H * 2
+    res = bench.finish_ours(_args(y_f32=True), wl, 1, 0, 10, 3, 80.0, _stages(1.0), CLK, None, {})
+    assert res["config"]["routed_expert_outputs"].startswith("fp32")
+    assert res["roofline"]["traffic"] is None

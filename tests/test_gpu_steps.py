@@ -213,13 +213,16 @@ def test_grouped_mlp_bad_offsets_reports():
 # ---------------------------------------------------------------- finalize
 @pytest.mark.parametrize("shared", [None, "bf16", "f32"])
 @pytest.mark.parametrize("out_f32", [False, True])
-def test_finalize(shared, out_f32):
+@pytest.mark.parametrize("y_f32", [False, True], ids=["ybf16", "yf32"])
+def test_finalize(shared, out_f32, y_f32):
     T, H, E, k = 300, 256, 16, 4
     rng = np.random.default_rng(3)
     lg = rng.standard_normal((T, E)).astype(np.float32)
     idx, w = oracle.topk_softmax(lg, k)
     r = oracle.init_routing(idx, E)
-    y = torch.randn((T * k, H)).to(torch.bfloat16)
+    y = torch.randn((T * k, H))
+    if not y_f32:
+        y = y.to(torch.bfloat16)
     sh = None
     sh_ref = None
     if shared == "bf16":
@@ -231,7 +234,7 @@ def test_finalize(shared, out_f32):
     out = moe.finalize_routing(y.to(DEV), torch.from_numpy(r["row_idx"]).to(DEV),
                                torch.from_numpy(w).to(DEV),
                                None if sh is None else sh.to(DEV), out_f32=out_f32)
-    ref = oracle.finalize(y, r["row_idx"], w, sh_ref)
+    ref = oracle.finalize(y.double().numpy() if y_f32 else y, r["row_idx"], w, sh_ref)
     got = t2f64(out)
     if out_f32:
         np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-5)

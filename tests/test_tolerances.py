@@ -39,3 +39,19 @@ def test_one_routed_ulp_flip_is_admitted_and_no_more():
     many[:, cols] += MAX_ABS + 0.5 * allow[:, cols]
     with pytest.raises(AssertionError):
         check_out(many, ref, bf16_out=False, flip_allowance=allow)
+
+
+def test_skew_beta_is_the_committed_cuda_calibration():
+    """The skewed workload's Zipf scale is the one tests/golden/calibrate_skew.py
+    found on the CUDA draw (committed beside it), which leaves 16 of 64
+    experts idle; the CPU draw's calibration is kept beside it for reference."""
+    import json
+    import os
+    import moe_inputs
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    cuda = json.load(open(os.path.join(here, "skew_calibration_cuda.json")))
+    cpu = json.load(open(os.path.join(here, "skew_calibration.json")))
+    assert cuda["device"] == "cuda" and cpu["device"] == "cpu"
+    assert cuda["beta"] == moe_inputs.SKEW_BETA_SEED0
+    assert moe_inputs.WORKLOADS["skewed-32k"].skew_beta == cuda["beta"]
+    assert cuda["zero_experts"] == 16 and cpu["zero_experts"] == 16

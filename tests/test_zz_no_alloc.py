@@ -6,8 +6,9 @@ allocation, or a cudaMalloc is not allowed where they run).  The no-alloc
 entry point keeps its routing histogram in a fixed array inside the library
 instead of a caller workspace.  This test calls it through the C ABI twice in
 a row, on different inputs, and checks that every output equals the regular
-workspace entry point's (index work: bit-exact), and that a call too large
-for the built-in array is refused.
+workspace entry point's (index work: bit-exact), that the largest call the
+built-in array holds (its last entry in use) still matches, and that a call
+one routing chunk larger is refused.
 
 The file sorts last so that a run stopping at the first failure has already
 run every other test; it passes on its own in a fresh process as well.
@@ -72,6 +73,29 @@ def test_noalloc_matches_workspace_entry_point_twice():
             assert torch.equal(got[key], ref[key]), key
         assert torch.equal(got["expanded_x"].view(torch.int16),
                            ref["expanded_x"].view(torch.int16))
+
+
+def test_noalloc_largest_accepted_size_matches():
+    # ceil(T/32) * E == 262144: every entry of the built-in array is used
+    T, k, E = 131072, 2, 64
+    rng = np.random.default_rng(4)
+    # k distinct experts per token, uniform
+    idx = torch.from_numpy(np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)).to(DEV)
+    ref = moe.init_routing(idx, None, E, with_rows=False)
+    N = T * k
+    got = {key: torch.full((n,), -7, dtype=torch.int32, device=DEV)
+           for key, n in (("row_idx", N), ("src_token", N), ("sorted_ids", N), ("counts", E),
+                          ("offsets", E + 1))}
+    st = moe.new_status(DEV)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = moe.lib().moe_init_routing_noalloc(
+        _p(idx), None, T, 0, E, k, None, _p(got["row_idx"]), _p(got["src_token"]),
+        _p(got["sorted_ids"]), _p(got["counts"]), _p(got["offsets"]), _p(st), stream)
+    assert rc == 0, moe.STATUS_NAMES.get(rc, rc)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for key in ("row_idx", "src_token", "counts", "offsets"):
+        assert torch.equal(got[key], ref[key]), key
 
 
 def test_noalloc_rejects_sizes_beyond_its_array():
