@@ -51,6 +51,7 @@ def _bind(lib):
     F = ctypes.c_float
     sigs = {
         "oracle_rmsnorm": [P, P, I64, I64, F, P],
+        "oracle_sumsq": [P, I64, I64, P],
         "oracle_gate_logits": [P, P, P, I64, I64, I64, P],
         "oracle_topk_softmax": [P, I64, I64, I64, INT, P, P],
         "oracle_init_routing": [P, I64, I64, I64, P, P, P, P, P],
@@ -166,6 +167,16 @@ def rmsnorm(x, gamma, eps):
     out = np.empty_like(x)
     _check(_load().oracle_rmsnorm(_p(x), _p(g), T, H, ctypes.c_float(eps), _p(out)),
            "oracle_rmsnorm")
+    return out
+
+
+def sumsq(x):
+    """The RMSNorm's row sums of squares: the exact sum of the bf16 squares
+    of each row, rounded once to fp32 -> float32 [T]."""
+    x = _u16(x)
+    T, H = x.shape
+    out = np.empty(T, dtype=np.float32)
+    _check(_load().oracle_sumsq(_p(x), T, H, _p(out)), "oracle_sumsq")
     return out
 
 

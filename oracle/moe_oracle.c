@@ -24,8 +24,10 @@
  *     and summed in.
  *
  * Readings where the page is silent (each is listed in the design notes):
- *   - RMSNorm: r = 1/sqrt(mean(x^2) + eps) in fp32, the sum of squares taken
- *     in ascending h; xn = bf16((x * r) * gamma).
+ *   - RMSNorm: r = 1/sqrt(mean(x^2) + eps) in fp32, where the sum of squares
+ *     is the exact sum of the bf16 squares rounded once to fp32 (nearest,
+ *     ties to even), so it does not depend on a summation order;
+ *     xn = bf16((x * r) * gamma).
  *   - Gate: every logit is an fp32 dot product accumulated in ascending h with
  *     one fused multiply-add per term, plus an optional per-expert offset.
  *     Routing decisions are taken on these fp32 logits (the page's precision).
@@ -89,6 +91,91 @@ static bf16_t bf16_from_double(double d)
 }
 
 /* ------------------------------------------------------------------------ */
+/* Sum of squares of a bf16 row, exact, rounded once to fp32 (nearest, ties  */
+/* to even).  A finite bf16 value is m * 2^(E - 134) with m its 8-bit       */
+/* significand (implicit bit included) and E = max(biased exponent, 1), so  */
+/* its square is m^2 * 2^(2E - 268): an integer m^2 < 2^16 shifted left by   */
+/* 2E - 2 bits in a fixed-point number whose unit is 2^-266.  The squares    */
+/* are added into such a number held in 64-bit limbs (2E - 2 <= 506, plus    */
+/* 16 bits of m^2 and 31 bits of carries fit 12 limbs), which is then        */
+/* rounded to 24 significant bits, or to a multiple of 2^-149 (bit 117) in   */
+/* fp32's subnormal range.  A row holding an infinity or a NaN gives the     */
+/* plain fp32 sum (inf or NaN).                                             */
+#define SS_LIMBS 12
+static float sumsq_exact_rn(const bf16_t *x, int64_t H)
+{
+    uint64_t acc[SS_LIMBS];
+    memset(acc, 0, sizeof acc);
+    for (int64_t h = 0; h < H; ++h) {
+        const int e = (x[h] >> 7) & 0xFF;
+        if (e == 0xFF) {
+            float s = 0.0f;
+            for (int64_t i = 0; i < H; ++i)
+                s += bf16_to_float(x[i]) * bf16_to_float(x[i]);
+            return s;
+        }
+        const uint64_t m = (uint64_t)(x[h] & 0x7F) | (e ? 0x80u : 0u);
+        const int sh = 2 * (e ? e : 1) - 2;
+        const int li = sh / 64, bo = sh % 64;
+        const uint64_t sq = m * m;
+        /* sq << bo spans limbs li and li + 1 */
+        uint64_t add[2];
+        add[0] = sq << bo;
+        add[1] = bo ? sq >> (64 - bo) : 0;
+        uint64_t carry = 0;
+        for (int j = li; j < SS_LIMBS; ++j) {
+            const uint64_t a = (j - li < 2) ? add[j - li] : 0;
+            const uint64_t old = acc[j];
+            acc[j] = old + a + carry;
+            carry = (acc[j] < old || (carry && acc[j] == old)) ? 1 : 0;
+            if (j - li >= 1 && !carry)
+                break;
+        }
+    }
+    /* the highest set bit */
+    int top = -1;
+    for (int j = SS_LIMBS - 1; j >= 0 && top < 0; --j)
+        for (int b = 63; b >= 0; --b)
+            if ((acc[j] >> b) & 1) {
+                top = j * 64 + b;
+                break;
+            }
+    if (top < 0)
+        return 0.0f;
+    int lsb = top - 23;            /* keep 24 significant bits */
+    if (lsb < 117)
+        lsb = 117;                 /* fp32 subnormals: multiples of 2^-149 */
+#define SS_BIT(i) ((int)((acc[(i) / 64] >> ((i) % 64)) & 1))
+    uint64_t q = 0;
+    for (int i = top; i >= lsb; --i)
+        q = (q << 1) | (uint64_t)SS_BIT(i);
+    /* the part below lsb against half of one unit of lsb */
+    int round_up = 0;
+    if (lsb > 0 && SS_BIT(lsb - 1)) {
+        int rest = 0;
+        for (int i = lsb - 2; i >= 0 && !rest; --i)
+            rest = SS_BIT(i);
+        round_up = rest || (q & 1);
+    }
+#undef SS_BIT
+    q += (uint64_t)round_up;
+    /* q * 2^(lsb - 266): exact in double; the cast to float is exact too,
+       unless it overflows to infinity */
+    return (float)ldexp((double)q, lsb - 266);
+}
+
+/* The row sums of squares as the RMSNorm takes them (test access). */
+int oracle_sumsq(const bf16_t *x, int64_t T, int64_t H, float *ss)
+{
+    if (!x || !ss || T < 0 || H <= 0)
+        return ORACLE_BAD_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        ss[t] = sumsq_exact_rn(x + t * H, H);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* RMSNorm ("RmsNorm算子优化"): xn = x / sqrt(mean(x^2) + eps) * gamma.       */
 /* gamma may be NULL (all ones).                                            */
 int oracle_rmsnorm(const bf16_t *x, const bf16_t *gamma, int64_t T, int64_t H,
@@ -99,11 +186,7 @@ int oracle_rmsnorm(const bf16_t *x, const bf16_t *gamma, int64_t T, int64_t H,
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) {
         const bf16_t *xr = x + t * H;
-        float ss = 0.0f;
-        for (int64_t h = 0; h < H; ++h) {
-            const float v = bf16_to_float(xr[h]);
-            ss = fmaf(v, v, ss);
-        }
+        const float ss = sumsq_exact_rn(xr, H);
         const float mean = ss / (float)H;
         const float r = 1.0f / sqrtf(mean + eps);
         for (int64_t h = 0; h < H; ++h) {

@@ -74,6 +74,80 @@ def pin_rmsnorm():
     assert np.all(np.abs(got - ref) <= ulp + 1e-30)
 
 
+def _f32_rne(S):
+    """A Fraction rounded to the nearest fp32 (ties to even), as a float;
+    infinity past the largest fp32.  Written from the IEEE definition."""
+    from fractions import Fraction
+    if S == 0:
+        return 0.0
+    e = S.numerator.bit_length() - S.denominator.bit_length()
+    if Fraction(2) ** e > S:
+        e -= 1                               # now 2^e <= S < 2^(e+1)
+    quantum = Fraction(2) ** max(e - 23, -149)
+    q = S / quantum
+    n = q.numerator // q.denominator
+    rem = q - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    v = n * quantum
+    return math.inf if v >= Fraction(2) ** 128 else float(v)
+
+
+def pin_sumsq():
+    """The RMSNorm's sum of squares is the exact sum of the bf16 squares,
+    rounded once to fp32: checked against exact rational arithmetic on random
+    rows of every scale, hand-made ties, fp32's subnormal and overflow ranges,
+    and a row whose squares carry across the oracle's 64-bit limbs."""
+    from fractions import Fraction
+
+    def ref(rows):
+        return np.array([_f32_rne(sum(Fraction(float(v)) ** 2 for v in r)) for r in rows],
+                        dtype=np.float32)
+
+    rng = np.random.default_rng(11)
+    rows = [rng.standard_normal(256) * 2.0 ** rng.integers(-40, 40) for _ in range(12)]
+    wide = rng.standard_normal(256) * 2.0 ** rng.integers(-60, 60, 256)   # 120 binades
+    rows.append(wide)
+    bits = f32_to_bf16_bits(np.array(rows))
+    got = oracle.sumsq(bits)
+    assert np.array_equal(got.view(np.uint32), ref(bits_f64(bits)).view(np.uint32))
+
+    def one(vals):
+        return float(oracle.sumsq(f32_to_bf16_bits(np.array([vals], dtype=np.float64)))[0])
+    big = [2.0 ** 11] * 4                     # squares sum to 2^24
+    assert one(big + [1.0]) == 2.0 ** 24                    # 2^24 + 1: a tie, to even
+    assert one(big + [1.0, 2.0 ** -30]) == 2.0 ** 24 + 2    # just above the tie
+    assert one(big + [1.0] * 3) == 2.0 ** 24 + 4            # 2^24 + 3: tie, to even
+    assert one([2.0 ** -70] * 4) == 2.0 ** -138             # exact subnormal
+    assert one([2.0 ** -75]) == 0.0                         # half of 2^-149: tie to 0
+    assert one([2.0 ** -75] * 3) == 2.0 ** -148             # 1.5 * 2^-149: tie to 2
+    assert one([2.0 ** 64]) == math.inf                     # 2^128 overflows
+    assert one([0.0] * 8) == 0.0
+    # an exact sum just below a tie of fp32's subnormal grid (2^-149 plus
+    # 2^-150 - 2^-173): rounding it to 24 bits first would land on the tie
+    # and then round up; rounded once it goes down to 2^-149
+    terms = [(221, 52), (141, 49), (153, 44), (247, 38), (166, 35), (169, 30), (168, 26),
+             (221, 22), (141, 19), (153, 14)]
+    vals = [m * 2.0 ** (E - 134) for m, E in terms]
+    rest = 2 ** 117 + 2 ** 116 - 2 ** 93 - sum(m * m << (2 * E - 2) for m, E in terms)
+    small = []
+    while rest > 0:        # the remainder as squares of smaller bf16 values
+        E = max(1, (rest.bit_length() - 16 + 2) // 2 + 1)
+        while E > 1 and (128 * 128 << (2 * E - 2)) > rest:
+            E -= 1
+        m = 255 if E > 1 else 127
+        while (m * m << (2 * E - 2)) > rest:
+            m -= 1
+        small.append(m * 2.0 ** (E - 134) if E > 1 or m >= 128 else m * 2.0 ** -133)
+        rest -= m * m << (2 * E - 2)
+    row = vals + small
+    assert sum(Fraction(v) ** 2 for v in row) == Fraction(2 ** 117 + 2 ** 116 - 2 ** 93, 2 ** 266)
+    assert one(row) == 2.0 ** -149
+    # 4096 squares of 1.9921875 * 2^32 straddle limbs 4 and 5: carries
+    carry = [1.9921875 * 2.0 ** 32] * 4096
+    assert one(carry) == _f32_rne(4096 * Fraction(1.9921875 * 2.0 ** 32) ** 2)
+
+
 def pin_gate():
     rng = np.random.default_rng(2)
     T, H, E = 5, 96, 7
@@ -331,7 +405,7 @@ def pin_ep_local_rerouting():
     assert np.array_equal(s1, np.arange(7))
 
 
-PINS = [pin_bf16_rounding, pin_rmsnorm, pin_gate, pin_topk, pin_routing,
+PINS = [pin_bf16_rounding, pin_rmsnorm, pin_sumsq, pin_gate, pin_topk, pin_routing,
         pin_expert_mlp, pin_finalize, pin_worked_example, pin_layer_brute_force,
         pin_layer_shared_rmsnorm, pin_ep_local_rerouting]
 
@@ -345,6 +419,13 @@ def test_pin(pin):
 # (original text, planted mistake) in moe_oracle.c
 MUTANTS = {
     "rms_no_sqrt": ("1.0f / sqrtf(mean + eps)", "1.0f / (mean + eps)"),
+    "sumsq_truncated": ("q += (uint64_t)round_up;", "q += 0;"),
+    "sumsq_ties_up": ("round_up = rest || (q & 1);", "round_up = 1;"),
+    "sumsq_no_subnormal": ("        lsb = 117;", "        lsb = lsb;"),
+    "sumsq_carry_dropped": ("carry = (acc[j] < old || (carry && acc[j] == old)) ? 1 : 0;",
+                            "carry = 0;"),
+    "sumsq_square_shift": ("const int sh = 2 * (e ? e : 1) - 2;",
+                           "const int sh = 2 * (e ? e : 1) - 1;"),
     "rms_no_mean": ("ss / (float)H", "ss"),
     "rms_no_gamma": ("v = v * bf16_to_float(gamma[h]);", "v = v;"),
     "gate_transposed": ("wg[e * H + h], acc)", "wg[h * E + e], acc)"),
