@@ -81,6 +81,8 @@ struct Params {
     // pair kernel, half tiles: the same tensors as 64-row boxes (A of both
     // segments; B of the SwiGLU mode, whose half tiles take 64 gate + 64 up rows)
     CUtensorMap tmA0h, tmA1h, tmB0h, tmB1h;
+    // wide pair kernel: B of both segments as 256-row boxes
+    CUtensorMap tmB0w, tmB1w;
 };
 
 struct Tile {
@@ -450,6 +452,7 @@ constexpr int TMEM2_COLS = 512;
 constexpr int QD = 4;                        // tile-queue depth
 constexpr int Q_CONSUMERS = 10;              // see the queue protocol below
 constexpr int EPI_BYTES = 32 * 64;           // one 32-row x 64-byte output box
+
 struct Cfg2 {
     static constexpr int EPI_OFF = STAGES2 * STAGE2_BYTES;   // 4 warps x 2 boxes, 1 KB aligned
     static constexpr int BAR_OFF = EPI_OFF + 4 * 2 * EPI_BYTES;
@@ -462,7 +465,8 @@ struct Cfg2 {
 };
 
 __device__ __forceinline__ Tile decode_tile_pair(const Params &p, int tile, const int *s_off,
-                                                 const int *s_prefix, int total0) {
+                                                 const int *s_prefix, int total0,
+                                                 int ksub = KSUB2) {
     Tile t;
     if (tile < total0) {
         int lo = 0, hi = p.G - 1;
@@ -484,7 +488,7 @@ __device__ __forceinline__ Tile decode_tile_pair(const Params &p, int tile, cons
         t.row0 = s_off[g] + m_blk * BM2;
         t.row_end = s_off[g + 1];
         t.n_blk = nfast ? local % p.nt0 : local / mt;
-        t.kblocks = p.K0 / (BK * KSUB2);
+        t.kblocks = p.K0 / (BK * ksub);
     } else {
         const int local = tile - total0;
         const int mt = (p.rows1 + BM2 - 1) / BM2;
@@ -494,10 +498,59 @@ __device__ __forceinline__ Tile decode_tile_pair(const Params &p, int tile, cons
         t.row0 = (nfast ? local / p.nt1 : local % mt) * BM2;
         t.row_end = p.rows1;
         t.n_blk = nfast ? local % p.nt1 : local / mt;
-        t.kblocks = p.K1 / (BK * KSUB2);
+        t.kblocks = p.K1 / (BK * ksub);
     }
     t.half = t.row_end - t.row0 <= 128;
     return t;
+}
+
+// One 32-row x 64-byte output box of an epilogue warp (lane i holds row
+// row0 + i as 16 words: 32 bf16 or 16 fp32 values starting at column col).
+// The rows are staged in one of the warp's two 2 KB shared-memory boxes in
+// the 64-byte swizzle of the output tensor map (16-byte chunk c of row r at
+// chunk c ^ ((r >> 1) & 3), conflict-free for the lanes' writes), then leave
+//   TMA:  as one TMA tensor store issued by lane 0 (two boxes per warp, so
+//         that the next box is written while the store reads the last);
+//   else: through the load/store units, the warp reading the box back
+//         row-contiguously (8 rows of 64 bytes per instruction) and writing
+//         coalesced 16-byte chunks (one box per warp suffices: the box is
+//         read back before it is written again).
+template <bool TMA>
+__device__ __forceinline__ void emit_out_box(const Params &p, uint8_t *ebox, int &eb, int lane,
+                                             const uint32_t (&w)[16], const CUtensorMap *map,
+                                             int col, int row0) {
+    uint8_t *box = ebox + eb * EPI_BYTES;
+    if (TMA && lane == 0) bulk_wait_read<1>();   // the store that last used this box has read it
+    __syncwarp();
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch)
+        *reinterpret_cast<uint4 *>(box + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4)) =
+            make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+    if (TMA) {
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(map, box, col, row0);
+            bulk_commit();
+        }
+    } else {
+        __syncwarp();
+        const bool seg1 = map == &p.tmO1;
+        const bool f32 = (seg1 ? p.out1_f32 : p.out0_f32) != 0;
+        const int esz = f32 ? 4 : 2;
+        const int64_t ld = (seg1 ? p.ldo1 : p.ldo0) * esz;
+        uint8_t *g = static_cast<uint8_t *>(seg1 ? p.out1 : p.out0) +
+                     static_cast<int64_t>(row0) * ld + static_cast<int64_t>(col) * esz;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int id = i * 32 + lane;
+            const int r = id >> 2, ch = id & 3;
+            const uint4 v =
+                *reinterpret_cast<const uint4 *>(box + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
+            *reinterpret_cast<uint4 *>(g + r * ld + ch * 16) = v;
+        }
+    }
+    if (TMA) eb ^= 1;
 }
 
 template <int MODE>
@@ -791,20 +844,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         uint8_t *ebox = smem + Cfg2::EPI_OFF + (warp - 2) * 2 * EPI_BYTES;
         int eb = 0;
         auto emit_box = [&](const uint32_t(&w)[16], const CUtensorMap *map, int col, int row0) {
-            uint8_t *box = ebox + eb * EPI_BYTES;
-            if (lane == 0) bulk_wait_read<1>();     // the store that last used this box has read it
-            __syncwarp();
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch)
-                *reinterpret_cast<uint4 *>(box + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4)) =
-                    make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_2d(map, box, col, row0);
-                bulk_commit();
-            }
-            eb ^= 1;
+            emit_out_box<true>(p, ebox, eb, lane, w, map, col, row0);
         };
         for (;;) {
             int tile = 0, got = 1;
@@ -942,6 +982,502 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
 }
 
+// ------------------------------------------------------------------ wide CTA-pair kernel
+// Tiles of 256 rows x 512 accumulator columns per CTA pair: per 64-wide
+// k-slice each CTA stages its 128 A rows (16 KB) and 256 rows of B (32 KB),
+// and the MMA thread issues two M=256, N=256 pair MMAs (accumulator halves
+// 0 and 1, TMEM columns [0, 256) and [256, 512)).  Per flop that is a
+// quarter fewer bytes through the SM's TMA engine than the 256 x 256 pair
+// tiles (48 KB for 2 x 256 x 512 x 64 flops against 32 KB for half that),
+// which is the limit of the operand fill when the clock is not capped.
+//   SWIGLU: the tile covers 256 act columns; the even CTA stages the 256
+//     gate rows, the odd CTA the matching 256 up rows, so half h holds g in
+//     its columns [0, 128) and u in [128, 256) for act columns 128h + j.
+//   STORE: the tile covers 512 output columns; CTA r stages B rows
+//     [256r, 256r + 256), so TMEM column 256h + j holds output column
+//     128h + j (j < 128) or 256 + 128h + (j - 128) (j >= 128).
+// The single 512-column accumulator is not double-buffered.  Instead eight
+// epilogue warps per CTA (two per TMEM lane quarter) drain half 0 first and
+// release it, then half 1; the MMA thread starts the next tile on half 0 as
+// soon as that is free and runs ahead on it over the staged k-slices (their
+// stages are released only once the half-1 MMAs of the slice are issued)
+// until half 1 is free too.  A four-deep ring of 48 KB stages gives that
+// run-ahead room; the output leaves through the load/store units from one
+// staging box per warp (the TMA engine stays with the operand loads; three
+// stages with TMA stores were 1.7% slower on the skewed load).
+// A group's last block of at most 128 rows runs as M=128 pair MMAs (64 rows
+// per CTA): MMA h then occupies TMEM columns [256h, 256h + 128), the CTA's
+// 64 rows in lanes 0-63 for N columns 0-127 and again in lanes 64-127 for
+// N columns 128-255; in SWIGLU mode each CTA then stages, per half, 64 gate
+// rows and the matching 64 up rows.
+// Tile queue, bounded waits and unwinding as in the pair kernel above.
+constexpr int WSTAGES = 4;
+constexpr int W_BOXES = 1;                              // staging box per epilogue warp
+constexpr int W_B_BYTES = 2 * A_BYTES;                  // 256 rows x 64 bf16
+constexpr int W_STAGE_BYTES = A_BYTES + W_B_BYTES;      // 48 KB per CTA
+constexpr int W_EPI_WARPS = 8;
+constexpr int W_THREADS = 64 + 32 * W_EPI_WARPS;
+constexpr int WQ_CONSUMERS = 2 + 2 * W_EPI_WARPS;       // MMA thread, odd producer, epilogue
+struct CfgW {
+    static constexpr int EPI_OFF = WSTAGES * W_STAGE_BYTES;
+    static constexpr int BAR_OFF = EPI_OFF + W_EPI_WARPS * W_BOXES * EPI_BYTES;
+    // full[S], empty[S], tfull, tempty[2], drain, q_full[QD], q_empty[QD]
+    static constexpr int NBARS = 2 * WSTAGES + 4 + 2 * QD;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int QT_OFF = MISC_OFF + 16;
+    static constexpr int OFFS_OFF = QT_OFF + QD * 4;
+    static constexpr int PREFIX_OFF = OFFS_OFF + (MAX_GROUPS + 1) * 4;
+    static constexpr int SMEM = 1024 + PREFIX_OFF + (MAX_GROUPS + 2) * 4;
+};
+static_assert(CfgW::SMEM <= 227 * 1024, "wide pair kernel: shared memory");
+
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
+    grouped_gemm_wide_kernel(const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + CfgW::BAR_OFF);
+    uint64_t *full = bars;                      // used in the even CTA only
+    uint64_t *empty = bars + WSTAGES;
+    uint64_t *tfull = bars + 2 * WSTAGES;
+    uint64_t *tempty = tfull + 1;               // [2], used in the even CTA only
+    uint64_t *drain = tempty + 2;
+    uint64_t *q_full = drain + 1;               // [QD]
+    uint64_t *q_empty = q_full + QD;            // [QD], used in the even CTA only
+    volatile int *q_tile = reinterpret_cast<volatile int *>(smem + CfgW::QT_OFF);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + CfgW::MISC_OFF);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + CfgW::MISC_OFF + 4);
+    volatile int *s_bad = reinterpret_cast<volatile int *>(smem + CfgW::MISC_OFF + 8);
+    int *s_off = reinterpret_cast<int *>(smem + CfgW::OFFS_OFF);
+    int *s_prefix = reinterpret_cast<int *>(smem + CfgW::PREFIX_OFF);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cid = static_cast<int>(cluster_id_x());
+
+    if (tid == 0) {
+        *s_abort = 0;
+        *s_bad = 0;
+    }
+    for (int g = tid; g <= p.G; g += W_THREADS) s_off[g] = p.offsets[g];
+    __syncthreads();
+    if (warp == 0) {
+        int run = 0;
+        bool bad = false;
+        for (int g0 = 0; g0 < p.G; g0 += 32) {
+            const int g = g0 + lane;
+            int tiles = 0;
+            if (g < p.G) {
+                const int a = s_off[g], b = s_off[g + 1];
+                if (a < 0 || b < a || b > p.rows0) bad = true;
+                tiles = b > a ? ((b - a + BM2 - 1) / BM2) * p.nt0 : 0;
+            }
+            int inc = tiles;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, inc, off);
+                if (lane >= off) inc += o;
+            }
+            if (g < p.G) s_prefix[g] = run + inc - tiles;
+            run += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) s_prefix[p.G] = run;
+        if (__any_sync(0xffffffffu, bad) && lane == 0) *s_bad = 1;
+    }
+    if (tid == 32) {
+        for (int s = 0; s < WSTAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(&tempty[0], 2 * W_EPI_WARPS);   // lane 0 of every epilogue warp of both CTAs
+        mbar_init(&tempty[1], 2 * W_EPI_WARPS);
+        mbar_init(drain, 1);
+        for (int q = 0; q < QD; ++q) {
+            mbar_init(&q_full[q], 1);
+            mbar_init(&q_empty[q], WQ_CONSUMERS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (*s_bad) {
+        if (tid == 0 && cid == 0 && leader) report(p.dev_status, MOE_DEV_BAD_OFFSETS);
+        return;
+    }
+    const int total0 = s_prefix[p.G];
+    const int total = total0 + (p.rows1 > 0 ? ((p.rows1 + BM2 - 1) / BM2) * p.nt1 : 0);
+
+    if (warp == 1) {
+        tmem_alloc_pair(s_tmem, TMEM2_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+    const uint32_t lead_full = mapa_shared(smem_u32(full), 0);
+    const uint32_t lead_tempty = mapa_shared(smem_u32(tempty), 0);
+    const uint32_t lead_qempty = mapa_shared(smem_u32(q_empty), 0);
+    const uint32_t peer_qfull = mapa_shared(smem_u32(q_full), 1);
+    const uint32_t peer_qtile = mapa_shared(static_cast<uint32_t>(__cvta_generic_to_shared(
+                                                const_cast<int *>(q_tile))), 1);
+    auto next_tile = [&](int &qi, uint32_t &qph, int &tile) -> bool {
+        if (!mbar_wait_bounded_cluster(&q_full[qi], qph, s_abort, p.dev_status)) return false;
+        tile = q_tile[qi];
+        mbar_arrive_cluster(lead_qempty + 8u * static_cast<uint32_t>(qi));
+        if (++qi == QD) {
+            qi = 0;
+            qph ^= 1;
+        }
+        return true;
+    };
+
+    if (warp == 0) {
+        // ================= TMA producer (both CTAs)
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmA0);
+            tma_prefetch_desc(&p.tmB0w);
+            if (p.rows1 > 0) {
+                tma_prefetch_desc(&p.tmA1);
+                tma_prefetch_desc(&p.tmB1w);
+            }
+            int stage = 0;
+            uint32_t phase = 0;
+            int armed[WSTAGES];
+            for (int s = 0; s < WSTAGES; ++s) armed[s] = -1;
+            int qi = 0;
+            uint32_t qph = 0;
+            while (!*s_abort) {
+                int tile;
+                if (leader) {
+                    if (!mbar_wait_bounded_cluster(&q_empty[qi], qph ^ 1, s_abort, p.dev_status))
+                        break;
+                    tile = static_cast<int>(atomicAdd(p.tile_counter, 1u));
+                    q_tile[qi] = tile;
+                    mbar_arrive(&q_full[qi]);
+                    st_shared_cluster_u32(peer_qtile + 4u * static_cast<uint32_t>(qi),
+                                          static_cast<uint32_t>(tile));
+                    mbar_arrive_cluster(peer_qfull + 8u * static_cast<uint32_t>(qi));
+                    if (++qi == QD) {
+                        qi = 0;
+                        qph ^= 1;
+                    }
+                } else if (!next_tile(qi, qph, tile)) {
+                    break;
+                }
+                if (tile >= total) break;
+                const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0, 1);
+                const int arow = t.row0 + (t.half ? 64 : 128) * static_cast<int>(rank);
+                const uint32_t stage_tx =
+                    t.half ? 2u * (A_BYTES / 2 + W_B_BYTES) : 2u * W_STAGE_BYTES;
+                const int whalf = t.seg == 0 ? p.half0 : p.half1;
+                const CUtensorMap *mA = t.seg == 0 ? (t.half ? &p.tmA0h : &p.tmA0)
+                                                   : (t.half ? &p.tmA1h : &p.tmA1);
+                const CUtensorMap *mBw = t.seg == 0 ? &p.tmB0w : &p.tmB1w;
+                const CUtensorMap *mBh = t.seg == 0 ? &p.tmB0h : &p.tmB1h;
+                bool ok = true;
+                for (int kb = 0; kb < t.kblocks; ++kb) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1, s_abort, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    armed[stage] = static_cast<int>(phase);
+                    uint8_t *a_dst = smem + stage * W_STAGE_BYTES;
+                    uint8_t *b_dst = a_dst + A_BYTES;
+                    if (leader) mbar_arrive_expect_tx(&full[stage], stage_tx);
+                    const uint32_t fb = lead_full + 8u * static_cast<uint32_t>(stage);
+                    const int k0 = kb * BK;
+                    tma_load_2d_pair(a_dst, mA, fb, k0, arow);
+                    if (MODE == MODE_SWIGLU && t.half) {
+                        // per half: 64 gate rows, then the matching 64 up rows
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int grow = t.n_blk * 256 + 128 * h + 64 * static_cast<int>(rank);
+                            uint8_t *bd = b_dst + h * A_BYTES;
+                            if (t.seg == 0) {
+                                tma_load_3d_pair(bd, mBh, fb, k0, grow, t.g);
+                                tma_load_3d_pair(bd + A_BYTES / 2, mBh, fb, k0, whalf + grow, t.g);
+                            } else {
+                                tma_load_2d_pair(bd, mBh, fb, k0, grow);
+                                tma_load_2d_pair(bd + A_BYTES / 2, mBh, fb, k0, whalf + grow);
+                            }
+                        }
+                    } else {
+                        const int brow = MODE == MODE_SWIGLU
+                                             ? (rank == 0 ? 0 : whalf) + t.n_blk * 256
+                                             : t.n_blk * 512 + 256 * static_cast<int>(rank);
+                        if (t.seg == 0)
+                            tma_load_3d_pair(b_dst, mBw, fb, k0, brow, t.g);
+                        else
+                            tma_load_2d_pair(b_dst, mBw, fb, k0, brow);
+                    }
+                    if (++stage == WSTAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+            }
+            if (*s_abort && leader) {
+                for (int s = 0; s < WSTAGES; ++s)
+                    if (armed[s] >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>(armed[s]));
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================= MMA issuer (even CTA only)
+        if (lane == 0 && leader) {
+            constexpr uint32_t IDESC = idesc_bf16_f32(BM2, 256);
+            constexpr uint32_t IDESC_HALF = idesc_bf16_f32(BM2 / 2, 256);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t tph = 0;
+            bool issued = false;
+            int qi = 0;
+            uint32_t qph = 0;
+            while (!*s_abort) {
+                int tile;
+                if (!next_tile(qi, qph, tile) || tile >= total) break;
+                const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0, 1);
+                const uint32_t idesc = t.half ? IDESC_HALF : IDESC;
+                // accumulator half h of stage st, k-block kb
+                auto mma_half = [&](int st, int kb, int h) {
+                    const uint32_t a_addr = smem_u32(smem + st * W_STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + A_BYTES + static_cast<uint32_t>(h) * A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma_bf16_pair(tmem_base + 256u * static_cast<uint32_t>(h),
+                                         sdesc_kmajor_sw128(a_addr + kk * 32),
+                                         sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                                         (kb | kk) != 0 ? 1u : 0u);
+                };
+                if (!mbar_wait_bounded_cluster(&tempty[0], tph ^ 1, s_abort, p.dev_status)) break;
+                tc_fence_after();
+                bool h1 = false;
+                int pend_st[WSTAGES];
+                int npend = 0, pend_kb0 = 0;
+                auto flush = [&]() {
+                    for (int i = 0; i < npend; ++i) {
+                        mma_half(pend_st[i], pend_kb0 + i, 1);
+                        tc_commit_pair_mc(&empty[pend_st[i]], 0x3);
+                    }
+                    npend = 0;
+                };
+                bool ok = true;
+                for (int kb = 0; kb < t.kblocks; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase, s_abort, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_half(stage, kb, 0);
+                    issued = true;
+                    if (!h1 && mbar_test_wait_cluster(&tempty[1], tph ^ 1)) {
+                        tc_fence_after();
+                        h1 = true;
+                    }
+                    if (h1) {
+                        flush();
+                        mma_half(stage, kb, 1);
+                        tc_commit_pair_mc(&empty[stage], 0x3);
+                    } else {
+                        if (npend == 0) pend_kb0 = kb;
+                        pend_st[npend++] = stage;
+                        if (npend == WSTAGES) {
+                            // every stage waits for half 1: the producer cannot go on
+                            if (!mbar_wait_bounded_cluster(&tempty[1], tph ^ 1, s_abort,
+                                                           p.dev_status)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            h1 = true;
+                            flush();
+                        }
+                    }
+                    if (++stage == WSTAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (ok && npend > 0) {
+                    // a tile of fewer k-blocks than stages
+                    if (!mbar_wait_bounded_cluster(&tempty[1], tph ^ 1, s_abort, p.dev_status)) {
+                        ok = false;
+                    } else {
+                        tc_fence_after();
+                        flush();
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair_mc(tfull, 0x3);
+                tph ^= 1;
+            }
+            if (*s_abort && issued) {
+                tc_commit_pair_mc(drain, 0x1);
+                mbar_wait_drain(drain, 0);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================= epilogue (warps 2..9 of both CTAs)
+        const int q = warp & 3;            // TMEM lane quarter this warp may read
+        const int sub = (warp - 2) >> 2;   // which half of the quarter's columns
+        uint32_t tph = 0;
+        int qi = 0;
+        uint32_t qph = 0;
+        uint8_t *ebox = smem + CfgW::EPI_OFF + (warp - 2) * W_BOXES * EPI_BYTES;
+        int eb = 0;
+        auto emit_box = [&](const uint32_t(&w)[16], const CUtensorMap *map, int col, int row0) {
+            emit_out_box<false>(p, ebox, eb, lane, w, map, col, row0);
+        };
+        for (;;) {
+            int tile = 0, got = 1;
+            if (lane == 0) {
+                if (mbar_wait_bounded_cluster(&q_full[qi], qph, s_abort, p.dev_status)) {
+                    tile = q_tile[qi];
+                    mbar_arrive_cluster(lead_qempty + 8u * static_cast<uint32_t>(qi));
+                } else {
+                    got = 0;
+                }
+            }
+            got = __shfl_sync(0xffffffffu, got, 0);
+            tile = __shfl_sync(0xffffffffu, tile, 0);
+            if (++qi == QD) {
+                qi = 0;
+                qph ^= 1;
+            }
+            if (!got || tile >= total) break;
+            const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0, 1);
+            if (!mbar_wait_bounded(tfull, tph, s_abort, p.dev_status)) break;
+            tc_fence_after();
+            const int hq = q >> 1;
+            const int row = t.half ? t.row0 + 64 * static_cast<int>(rank) + 32 * (q & 1) + lane
+                                   : t.row0 + 128 * static_cast<int>(rank) + 32 * q + lane;
+            const bool ok = row < t.row_end;
+            const int row_base = row - lane;
+            const bool boxed = row_base + 32 <= t.row_end;
+            const CUtensorMap *omap = t.seg == 0 ? &p.tmO0 : &p.tmO1;
+            const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+            for (int h = 0; h < 2; ++h) {
+                if (MODE == MODE_SWIGLU) {
+                    uint16_t *out = static_cast<uint16_t *>(t.seg == 0 ? p.out0 : p.out1);
+                    const int64_t ldo = t.seg == 0 ? p.ldo0 : p.ldo1;
+                    // full: g at 256h + [0,128), u at 256h + 128 + [0,128), act 128h + j;
+                    // half: g at 256h + [0,64), u at 256h + 64 + [0,64), act 128h + 64 hq + j
+                    const int uoff = t.half ? 64 : 128;
+                    const int ncol = t.half ? 32 : 64;          // this warp's share
+                    const int j0 = ncol * sub;
+                    const int act0 = t.n_blk * 256 + 128 * h + (t.half ? 64 * hq : 0) + j0;
+                    const uint32_t gbase = tq + 256u * static_cast<uint32_t>(h) + j0;
+#pragma unroll 1
+                    for (int c = 0; c < ncol; c += 32) {
+                        float g[32], u[32];
+                        __syncwarp();
+                        tmem_ld32(gbase + c, g);
+                        tmem_ld32(gbase + uoff + c, u);
+                        tmem_ld_wait();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float a0 =
+                                __fdividef(g[2 * i], 1.0f + __expf(-g[2 * i])) * u[2 * i];
+                            const float a1 = __fdividef(g[2 * i + 1], 1.0f + __expf(-g[2 * i + 1])) *
+                                             u[2 * i + 1];
+                            pk[i] = pack_bf16x2(a0, a1);
+                        }
+                        if (boxed) {
+                            emit_box(pk, omap, act0 + c, row_base);
+                        } else if (ok) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(
+                                out + static_cast<int64_t>(row) * ldo + act0 + c);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                                                    pk[4 * v + 3]);
+                        }
+                    }
+                } else {
+                    const bool f32 = (t.seg == 0 ? p.out0_f32 : p.out1_f32) != 0;
+                    void *outp = t.seg == 0 ? p.out0 : p.out1;
+                    const int64_t ldo = t.seg == 0 ? p.ldo0 : p.ldo1;
+                    // full: TMEM 256h + 128 sub + [0,128) -> out 256 sub + 128h + j;
+                    // half: TMEM 256h + 64 sub + [0,64) -> out 256 hq + 128h + 64 sub + j
+                    const int ncol = t.half ? 64 : 128;
+                    const uint32_t tbase = tq + 256u * static_cast<uint32_t>(h) + ncol * sub;
+                    const int col0 = t.n_blk * 512 + 128 * h +
+                                     (t.half ? 256 * hq + 64 * sub : 256 * sub);
+#pragma unroll 1
+                    for (int c = 0; c < ncol; c += 32) {
+                        float v[32];
+                        __syncwarp();
+                        tmem_ld32(tbase + c, v);
+                        tmem_ld_wait();
+                        const int col = col0 + c;
+                        if (boxed) {
+                            uint32_t w[16];
+                            if (f32) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[i]);
+                                emit_box(w, omap, col, row_base);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[16 + i]);
+                                emit_box(w, omap, col + 16, row_base);
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                                emit_box(w, omap, col, row_base);
+                            }
+                            continue;
+                        }
+                        if (!ok) continue;
+                        const int64_t off = static_cast<int64_t>(row) * ldo + col;
+                        if (f32) {
+                            float4 *dst =
+                                reinterpret_cast<float4 *>(static_cast<float *>(outp) + off);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                dst[i] =
+                                    make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        } else {
+                            uint4 *dst =
+                                reinterpret_cast<uint4 *>(static_cast<uint16_t *>(outp) + off);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]),
+                                                    pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                                    pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                                                    pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+                        }
+                    }
+                }
+                // this warp's columns of half h have left TMEM
+                __syncwarp();
+                tc_fence_before();
+                if (lane == 0) mbar_arrive_cluster(lead_tempty + 8u * static_cast<uint32_t>(h));
+            }
+            tph ^= 1;
+        }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM2_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -1012,15 +1548,35 @@ bool make_out_maps(Params &p, int cols0, int cols1) {
 
 // Which grouped-GEMM kernel runs: MOE_GEMM_KERNEL=pair or =single in the
 // environment (read once) forces one; the default picks per launch.
-enum GemmChoice { GEMM_AUTO, GEMM_PAIR, GEMM_SINGLE };
+enum GemmChoice { GEMM_AUTO, GEMM_PAIR, GEMM_SINGLE, GEMM_WIDE };
 GemmChoice gemm_choice() {
     static const GemmChoice c = [] {
         const char *v = getenv("MOE_GEMM_KERNEL");
         if (v && v[0] == 'p') return GEMM_PAIR;
         if (v && v[0] == 's') return GEMM_SINGLE;
+        if (v && v[0] == 'w') return GEMM_WIDE;
         return GEMM_AUTO;
     }();
     return c;
+}
+
+// The wide pair kernel takes the launches the CTA-pair kernel would (about
+// 1024 rows per group or more) when the shapes give whole 512-column tiles
+// (256 act columns in SwiGLU mode) in both segments: measured on GB300 with
+// the clock power-capped, it runs the image-gen block's matmuls 1-1.5% and
+// the skewed load's 1.7% faster than the 256 x 256 pair tiles (fewer bytes
+// staged per flop, so a higher clock under the same power).  With a few
+// hundred rows per group the one-CTA kernel stays faster.
+bool use_wide(bool swiglu, int N, int K, const GemmSegment1 &seg1, int n, int G) {
+    const GemmChoice c = gemm_choice();
+    if (c == GEMM_PAIR || c == GEMM_SINGLE) return false;
+    const int unit = swiglu ? 256 : 512;
+    const bool fits = N % unit == 0 && K % BK == 0 &&
+                      (seg1.rows == 0 || (seg1.N1 % unit == 0 && seg1.K1 % BK == 0));
+    if (!fits) return false;
+    if (c == GEMM_WIDE) return true;
+    const int64_t avg = G > 0 ? n / G : seg1.rows;
+    return avg >= 1024;
 }
 
 // 256-row pair tiles pay off when groups are large.  Each group's last
@@ -1143,6 +1699,50 @@ cudaError_t launch_pair(Params &p, int max_rows0, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <int MODE>
+cudaError_t launch_wide(Params &p, int max_rows0, cudaStream_t stream) {
+    static std::mutex mu;
+    static bool attr_done[64] = {};
+    static int max_clusters[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !attr_done[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(grouped_gemm_wide_kernel<MODE>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 CfgW::SMEM);
+            if (e != cudaSuccess) return e;
+            attr_done[dev] = true;
+        }
+        if (dev < 64 && max_clusters[dev] == 0) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(num_sms()), 1, 1);
+            cfg.blockDim = dim3(W_THREADS, 1, 1);
+            cfg.dynamicSmemBytes = CfgW::SMEM;
+            cfg.stream = stream;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_wide_kernel<MODE>, &cfg) !=
+                    cudaSuccess ||
+                n <= 0) {
+                cudaGetLastError();
+                n = num_sms() / 2;
+            }
+            max_clusters[dev] = std::min(n, num_sms() / 2);
+        }
+    }
+    const int64_t mblocks0 = ceil_div(max_rows0, BM2) + p.G;
+    const int64_t tiles = mblocks0 * p.nt0 + (p.rows1 > 0 ? ceil_div(p.rows1, BM2) * p.nt1 : 0);
+    const int limit = dev < 64 ? max_clusters[dev] : num_sms() / 2;
+    const int clusters = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(limit, tiles)));
+    cudaError_t e = next_tile_counter(&p.tile_counter);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(p.tile_counter, 0, sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return e;
+    grouped_gemm_wide_kernel<MODE><<<2 * clusters, W_THREADS, CfgW::SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool tensor_maps_available() { return encode_fn() != nullptr; }
@@ -1196,6 +1796,39 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
     p.out0_f32 = 0;
     p.out1_f32 = 0;
     p.dev_status = dev_status;
+    if (use_wide(true, N, K, seg1, n, G)) {
+        // 256 act columns per tile; A as 128- and 64-row boxes, B as 256-row
+        // boxes (and 64-row boxes for the gate/up quarters of half tiles)
+        p.nt0 = N / 256;
+        p.nt1 = seg1.N1 / 256;
+        if (!make_out_maps(p, N, seg1.N1)) return cudaErrorInvalidValue;
+        if (G > 0) {
+            const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
+            const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(2 * N),
+                                    static_cast<uint64_t>(G)};
+            if (!make_map(&p.tmA0h, A, 2, a0, 64) || !make_map(&p.tmB0h, W13, 3, b0, 64) ||
+                !make_map(&p.tmB0w, W13, 3, b0, 256))
+                return cudaErrorInvalidValue;
+        }
+        if (seg1.rows > 0) {
+            const uint64_t a1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.rows)};
+            const uint64_t b1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(2 * seg1.N1)};
+            if (!make_map(&p.tmA1h, seg1.A, 2, a1, 64) || !make_map(&p.tmB1h, seg1.B, 2, b1, 64) ||
+                !make_map(&p.tmB1w, seg1.B, 2, b1, 256))
+                return cudaErrorInvalidValue;
+        }
+        if (G == 0) {
+            p.tmA0h = p.tmA1h;
+            p.tmB0h = p.tmB1h;
+            p.tmB0w = p.tmB1w;
+        }
+        if (seg1.rows == 0) {
+            p.tmA1h = p.tmA0h;
+            p.tmB1h = p.tmB0h;
+            p.tmB1w = p.tmB0w;
+        }
+        return launch_wide<MODE_SWIGLU>(p, n, stream);
+    }
     if (pair) {
         if (!make_out_maps(p, N, seg1.N1)) return cudaErrorInvalidValue;
         // 64-row boxes for half tiles: A, and B as 64 gate + 64 up rows
@@ -1274,6 +1907,37 @@ cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, 
     p.out0_f32 = y_f32 ? 1 : 0;
     p.out1_f32 = seg1.out_f32 ? 1 : 0;
     p.dev_status = dev_status;
+    if (use_wide(false, N, K, seg1, n, G)) {
+        // 512 output columns per tile; A as 128- and 64-row boxes, B as
+        // 256-row boxes
+        p.nt0 = N / 512;
+        p.nt1 = seg1.N1 / 512;
+        if (!make_out_maps(p, N, seg1.N1)) return cudaErrorInvalidValue;
+        if (G > 0) {
+            const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
+            const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                                    static_cast<uint64_t>(G)};
+            if (!make_map(&p.tmA0h, A, 2, a0, 64) || !make_map(&p.tmB0w, W, 3, b0, 256))
+                return cudaErrorInvalidValue;
+        }
+        if (seg1.rows > 0) {
+            const uint64_t a1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.rows)};
+            const uint64_t b1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.N1)};
+            if (!make_map(&p.tmA1h, seg1.A, 2, a1, 64) || !make_map(&p.tmB1w, seg1.B, 2, b1, 256))
+                return cudaErrorInvalidValue;
+        }
+        if (G == 0) {
+            p.tmA0h = p.tmA1h;
+            p.tmB0w = p.tmB1w;
+        }
+        if (seg1.rows == 0) {
+            p.tmA1h = p.tmA0h;
+            p.tmB1w = p.tmB0w;
+        }
+        p.tmB0h = p.tmB0w;
+        p.tmB1h = p.tmB1w;
+        return launch_wide<MODE_STORE>(p, n, stream);
+    }
     if (pair) {
         if (!make_out_maps(p, N, seg1.N1)) return cudaErrorInvalidValue;
         // 64-row A boxes for half tiles (B keeps its 128-row boxes)

@@ -40,12 +40,13 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert torch.allclose(w.cpu(), torch.tensor([[0.5, 0.5]]))
 
 
-@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("kernel", ["single", "pair", "wide"])
 def test_each_gemm_kernel_subprocess(kernel):
-    """Both grouped-GEMM kernels (one CTA per 128-row tile, and CTA pairs on
-    256-row tiles) pass the grouped-GEMM and layer parity tests when forced
-    with MOE_GEMM_KERNEL (the default picks per launch; the choice is read
-    once per process, hence the child process)."""
+    """Every grouped-GEMM kernel (one CTA per 128-row tile, CTA pairs on
+    256 x 256 tiles, CTA pairs on 256 x 512 tiles where the shapes allow)
+    passes the grouped-GEMM and layer parity tests when forced with
+    MOE_GEMM_KERNEL (the default picks per launch; the choice is read once
+    per process, hence the child process)."""
     env = dict(os.environ, MOE_GEMM_KERNEL=kernel)
     cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
            os.path.join(ROOT, "tests", "test_gpu_steps.py"),

@@ -109,6 +109,9 @@ SMALL = [
     # 65 experts the combine writes logits for the separate top-k)
     Workload("edge-512", T=512, H=128, E=65, k=3, I=128, rmsnorm=True, gamma_std=0.1),
     Workload("edge-513", T=513, H=128, E=65, k=3, I=128, rmsnorm=True, gamma_std=0.1),
+    # shapes the wide pair kernel takes (I, I_s % 256 == 0, H % 512 == 0)
+    Workload("mid-wide", T=900, H=512, E=8, k=2, I=256, I_s=256, rmsnorm=True,
+             gamma_std=0.1, x_std=1.0),
 ]
 
 
