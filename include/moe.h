@@ -95,9 +95,9 @@ const char *moe_status_string(int status);
  *   gamma  [H] bf16, or NULL for all ones (used with MOE_RMSNORM only)
  *   wg     [E, H] fp32 gate weight
  *   gate_bias [E] fp32 per-expert logit offset, or NULL
- *   xn     [T, H] bf16 out: bf16((x * r) * gamma), r = 1/sqrt(mean(x^2)+eps)
- *          with the sum of squares taken in fp32 in ascending h.  Required
- *          with MOE_RMSNORM, ignored (may be NULL) without it.
+ *   xn     [T, H] bf16 out: bf16((x * r) * gamma), r = 1/sqrt(ss/H + eps)
+ *          in fp32, ss the row's sum of squares as moe_rmsnorm_sumsq gives
+ *          it.  Required with MOE_RMSNORM, ignored (may be NULL) without it.
  *   logits [T, E] fp32 out: fp32 dot product of the (normalised) row with
  *          wg[e], one fused multiply-add per term in ascending h, plus
  *          gate_bias[e].  These are bit-identical to the same steps done
@@ -111,6 +111,17 @@ moe_status_t moe_rmsnorm_gate(const moe_bf16_t *x, const moe_bf16_t *gamma,
                               const float *wg, const float *gate_bias, int32_t T,
                               int32_t H, int32_t E, float eps, uint32_t flags,
                               moe_bf16_t *xn, float *logits, moe_stream_t stream);
+
+/*
+ * The RMSNorm's reduction ("RmsNorm算子优化"): per row, the exact sum of the
+ * squares of its bf16 values rounded once to fp32 (nearest, ties to even;
+ * fp32 subnormals and overflow to infinity included).  The value does not
+ * depend on a summation order; every RMSNorm of this library uses it.
+ *   x  [T, H] bf16 (16-byte aligned, H % 8 == 0);  ss [T] fp32 out
+ * T may be 0.  A row holding an infinity or a NaN gives inf or NaN.
+ */
+moe_status_t moe_rmsnorm_sumsq(const moe_bf16_t *x, int32_t T, int32_t H, float *ss,
+                               moe_stream_t stream);
 
 /*
  * The same fp32 gate on the tensor cores ("消除gate计算冗余cast算子": an fp32

@@ -36,7 +36,8 @@ DEV_BAD_EXPERT_ID, DEV_TIMEOUT, DEV_BAD_OFFSETS, DEV_UNSORTED = 1, 2, 4, 8
 RENORM, RMSNORM, SHARED, OUT_F32, SHARED_F32, GATE_SEQUENTIAL, Y_F32 = 1, 2, 4, 8, 16, 32, 64
 
 # every symbol include/moe.h declares
-EXPORTS = ("moe_status_string", "moe_rmsnorm_gate", "moe_gate_tensor_workspace_size",
+EXPORTS = ("moe_status_string", "moe_rmsnorm_gate", "moe_rmsnorm_sumsq",
+           "moe_gate_tensor_workspace_size",
            "moe_gate_tensor", "moe_gate_topk",
            "moe_init_routing_workspace_size", "moe_init_routing", "moe_init_routing_noalloc",
            "moe_expert_tokens",
@@ -85,6 +86,7 @@ def lib() -> ctypes.CDLL:
             PSZ = ctypes.POINTER(ctypes.c_size_t)
             sigs = {
                 "moe_rmsnorm_gate": [P, P, P, P, I32, I32, I32, F, U32, P, P, P],
+                "moe_rmsnorm_sumsq": [P, I32, I32, P, P],
                 "moe_gate_tensor_workspace_size": [I32, I32, I32, PSZ],
                 "moe_gate_tensor": [P, P, P, I32, I32, I32, P, P, SZ, P, P],
                 "moe_gate_topk": [P, I32, I32, I32, U32, P, P, P],
@@ -202,6 +204,16 @@ def rmsnorm_gate(x, wg, gamma=None, gate_bias=None, eps=1e-6, rmsnorm=True):
     _call("moe_rmsnorm_gate", _ptr(x), _ptr(gamma), _ptr(wg), _ptr(gate_bias), T, H, E,
           float(eps), RMSNORM if rmsnorm else 0, _ptr(xn), _ptr(logits), _stream(x.device))
     return xn, logits
+
+
+def rmsnorm_sumsq(x):
+    """-> float32 [T]: each row's sum of squares as the RMSNorm takes it (the
+    exact sum of the bf16 squares rounded once to fp32)."""
+    _check(x, torch.bfloat16, "x")
+    T, H = x.shape
+    ss = torch.empty(T, dtype=torch.float32, device=x.device)
+    _call("moe_rmsnorm_sumsq", _ptr(x), T, H, _ptr(ss), _stream(x.device))
+    return ss
 
 
 def gate_tensor_workspace_size(T, H, E) -> int:

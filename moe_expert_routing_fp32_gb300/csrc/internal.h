@@ -48,6 +48,8 @@ cudaError_t launch_rmsnorm(const uint16_t *x, const uint16_t *gamma, int T, int 
                            uint16_t *xn, int32_t *dev_status, cudaStream_t stream);
 cudaError_t launch_gate_split(const float *wg, int E, int H, uint16_t *wsplit, int NW,
                               cudaStream_t stream);
+// RMSNorm's sum of squares of each row: the exact sum rounded once to fp32
+cudaError_t launch_sumsq(const uint16_t *x, int T, int H, float *ss, cudaStream_t stream);
 cudaError_t launch_gate_combine(const float *parts, int NW, int T, int E, const float *gate_bias,
                                 float *logits, bool fuse_topk, int k, bool renorm,
                                 int32_t *topk_idx, float *topk_w, int32_t *hist,

@@ -206,6 +206,17 @@ moe_status_t moe_rmsnorm_gate(const moe_bf16_t *x, const moe_bf16_t *gamma, cons
     return MOE_OK;
 }
 
+moe_status_t moe_rmsnorm_sumsq(const moe_bf16_t *x, int32_t T, int32_t H, float *ss,
+                               moe_stream_t stream) {
+    if (T < 0 || H <= 0) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!x || !ss || !a16(x)) return MOE_ERR_INVALID_ARG;
+    if (!current_device_ok()) return MOE_ERR_NO_DEVICE;
+    MOE_TRY(launch_sumsq(x, T, H, ss, reinterpret_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
 moe_status_t moe_gate_tensor_workspace_size(int32_t T, int32_t H, int32_t E, size_t *bytes) {
     if (!bytes || T < 0 || H <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
     if (H % 128 != 0 || E > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;

@@ -12,10 +12,13 @@
 // for the partial logits, and gate_combine_kernel (the fp32 sum of the
 // parts, top-k, weights and the routing histogram).
 //
+// RMSNorm's sum of squares is the exact sum of the bf16 squares rounded once
+// to fp32 (see "sum of squares" below): every kernel here takes it with one
+// warp per row, in parallel, and they all give the same bits.
+//
 // The sequential router: one CTA owns 32 tokens and 64 experts:
-//   phase 1 (RMSNorm only): the 32 rows stream through shared memory in
-//     512-byte pieces (TMA bulk copies, 2-stage ring); warp 0 keeps one fp32
-//     sum of squares per token, accumulated in ascending h;
+//   phase 1 (RMSNorm only): each of the 4 warps takes the sum of squares of
+//     every 4th row, reading it from memory;
 //   phase 2: 32-wide slices of the normalised rows (bf16-rounded, then fp32)
 //     and of the gate weight are staged in shared memory; every thread owns
 //     4 tokens x 4 experts and accumulates each logit with one FMA per term
@@ -45,21 +48,17 @@ namespace {
 constexpr int RT_THREADS = 128;
 constexpr int RT_TOK = kChunkTokens;     // 32
 constexpr int RT_EXP = kRouterExperts;   // 64
-constexpr int SS_HC = 256;               // h per sum-of-squares piece
-constexpr int SS_ROW = SS_HC * 2 + 16;   // padded smem row (bytes)
-constexpr int SS_STAGES = 2;
 constexpr int G_HC = 32;                 // h per gate slice
 constexpr int G_LD = 36;                 // padded fp32 row stride
 constexpr int G_STAGES = 3;              // cp.async ring depth of the gate slices
 
-constexpr int SMEM_SS = SS_STAGES * RT_TOK * SS_ROW;                       // 33792
 constexpr int WG_STAGE = RT_EXP * G_LD * 4;                                // 9216
 constexpr int XR_STAGE = RT_TOK * G_HC * 2;                                // 2048
 constexpr int SMEM_XS = 2 * RT_TOK * G_LD * 4;                             // 9216
 constexpr int SMEM_G = G_STAGES * (WG_STAGE + XR_STAGE) + SMEM_XS;         // 43008
 constexpr int SMEM_LG = RT_TOK * (RT_EXP + 1) * 4;                         // 8320
-constexpr int SMEM_MAIN = SMEM_SS > SMEM_G ? SMEM_SS : SMEM_G;
-constexpr int SMEM_TOTAL = SMEM_MAIN + SMEM_LG + 64 * 8 /*bars*/ + RT_TOK * 4 + RT_EXP * 4 + 16;
+constexpr int SMEM_MAIN = SMEM_G;
+constexpr int SMEM_TOTAL = SMEM_MAIN + SMEM_LG + RT_TOK * 4 + RT_EXP * 4;
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)),
@@ -143,6 +142,279 @@ __device__ __forceinline__ float slot_weight(const float (&v)[NV], int k, bool r
     return ej / den;
 }
 
+// ---------------------------------------------------------------- sum of squares
+// The RMSNorm's sum of squares is the exact sum of the squares of a bf16 row
+// rounded once to fp32 (nearest, ties to even), a value that does not depend
+// on a summation order, so one warp sums a row in parallel.
+//
+// Fast path (finite rows whose largest |x| lies in [2^-20, 2^40] and whose
+// smallest nonzero |x| is at least 2^-60; then every square is exact in
+// fp32).  With ex the exponent of the largest |x|, every square is below
+// 2^(2ex+2).  Each square v is split exactly into
+//   q1 = v truncated to a multiple of u1 = 2^(2ex-14) (s1 + v rounded toward
+//        zero, minus s1, with s1 = 2^(2ex+9)),
+//   q2 = the rest truncated to a multiple of u2 = 2^(2ex-30) (s2 = 2^(2ex-7)),
+//   r2 = the rest, 0 <= r2 < u2.
+// The q1 of at most 128 squares (16 vectors of a lane) add up exactly in fp32
+// (multiples of u1 below 2^24 u1), likewise the q2; those group sums become
+// exact integers (units u1, u2) summed across lanes in 64 bits, giving
+// T = sum(q1 + q2) / u2 exactly.  The r2 are summed in fp32 (A, in units of
+// u2 after scaling) with a relative error below (n + 8) 2^-23 for n squares
+// per lane, so the exact sum is T + R, R in [A (1 - d), A (1 + d)] (R = 0
+// exactly when A = 0).  Rounded to 24 bits, both ends of that interval giving
+// the same fp32 value decides the result; otherwise (the interval holds a
+// rounding tie) the slow path decides.
+// Slow path: every square m^2 * 2^(2E-268) (m the 8-bit significand, E the
+// biased exponent, at least 1) is added exactly into a fixed-point number of
+// 20 32-bit limbs per lane (unit 2^-266), the lanes' numbers are added
+// exactly across the warp, and the total is rounded (to 24 significant bits,
+// or to a multiple of 2^-149 in fp32's subnormal range; infinity past the
+// largest fp32).
+constexpr int SQ_LIMBS = 20;
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// Slow path: exact fixed-point sum of the squares of the row (nvec vectors of
+// 8 bf16, lanes take vectors lane, lane + 32, ...), rounded; every lane
+// returns the result.
+__device__ __noinline__ float sumsq_row_exact(const uint4 *row, int nvec) {
+    const int lane = threadIdx.x & 31;
+    uint32_t acc[SQ_LIMBS];
+#pragma unroll
+    for (int j = 0; j < SQ_LIMBS; ++j) acc[j] = 0u;
+    for (int v = lane; v < nvec; v += 32) {
+        const uint4 q = row[v];
+        const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t b = (i & 1) ? (wd[i >> 1] >> 16) : (wd[i >> 1] & 0xFFFFu);
+            const uint32_t e = (b >> 7) & 0xFFu;
+            const uint32_t m = (b & 0x7Fu) | (e ? 0x80u : 0u);
+            if (m == 0u) continue;
+            const uint32_t sh = 2u * (e ? e : 1u) - 2u;     // bit of the square's unit
+            const uint64_t val = static_cast<uint64_t>(m * m) << (sh & 31u);   // < 2^47
+            uint32_t j = sh >> 5;
+            uint64_t carry = (val & 0xFFFFFFFFull);
+            carry += acc[j];
+            acc[j] = static_cast<uint32_t>(carry);
+            carry = (carry >> 32) + (val >> 32);
+            for (++j; carry != 0u && j < SQ_LIMBS; ++j) {
+                carry += acc[j];
+                acc[j] = static_cast<uint32_t>(carry);
+                carry >>= 32;
+            }
+        }
+    }
+    // add the lanes' numbers: lane 0 ends with the total
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        uint64_t carry = 0;
+#pragma unroll
+        for (int j = 0; j < SQ_LIMBS; ++j) {
+            const uint32_t o = __shfl_down_sync(0xffffffffu, acc[j], off);
+            carry += static_cast<uint64_t>(acc[j]) + o;
+            acc[j] = static_cast<uint32_t>(carry);
+            carry >>= 32;
+        }
+    }
+    float res = 0.0f;
+    if (lane == 0) {
+        int top = -1;
+        for (int j = SQ_LIMBS - 1; j >= 0 && top < 0; --j)
+            if (acc[j]) top = 32 * j + 31 - __clz(acc[j]);
+        if (top >= 0) {
+            auto bit = [&](int i) { return (acc[i >> 5] >> (i & 31)) & 1u; };
+            const int lsb = max(top - 23, 117);             // bit 117 = 2^-149
+            uint32_t q = 0;
+            for (int i = top; i >= lsb; --i) q = (q << 1) | bit(i);
+            if (bit(lsb - 1)) {
+                bool rest = false;
+                for (int i = lsb - 2; i >= 0 && !rest; --i) rest = bit(i) != 0u;
+                if (rest || (q & 1u)) ++q;
+            }
+            // q * 2^(lsb - 266), q <= 2^24: exact in double, and either an exact
+            // fp32 value or at least 2^128, which the conversion turns into inf
+            res = static_cast<float>(ldexp(static_cast<double>(q), lsb - 266));
+        }
+    }
+    return __shfl_sync(0xffffffffu, res, 0);
+}
+
+// x^2 split into its q1 + q2 and the rest, accumulated (see above)
+__device__ __forceinline__ void sumsq_split(float x, float s1, float s2, float &a1, float &a2,
+                                            float &a3) {
+    const float v = __fmul_rn(x, x);
+    const float q1 = __fsub_rn(__fadd_rz(s1, v), s1);
+    a1 = __fadd_rn(a1, q1);
+    const float r1 = __fsub_rn(v, q1);
+    const float q2 = __fsub_rn(__fadd_rz(s2, r1), s2);
+    a2 = __fadd_rn(a2, q2);
+    a3 = __fadd_rn(a3, __fsub_rn(r1, q2));
+}
+
+// n + f (an integer n >= 2^30 and a real f >= 0, in units u2) rounded to 24
+// significant bits, nearest-even: the rounded value, an integer of at most 24
+// significant bits.  (n >= 2^30: the largest square alone is at least 2^30 u2.)
+__device__ __forceinline__ long long round24(long long n0, double f) {
+    const double fl = floor(f);
+    const long long n = n0 + static_cast<long long>(fl);
+    const double fr = f - fl;
+    const int top = 63 - __clzll(n);
+    const int L = top - 23;
+    const long long q = n >> L;
+    const long long rem = n & ((1ll << L) - 1);
+    const long long half = 1ll << (L - 1);
+    const double d = static_cast<double>(rem - half) + fr;
+    const bool up = d > 0.0 || (d == 0.0 && (q & 1));
+    return (q + (up ? 1 : 0)) << L;
+}
+
+// Largest and smallest nonzero |x| of 8 bf16 values, as fp32 bit patterns
+// (for non-negative floats the integer order is the value order).
+__device__ __forceinline__ void sumsq_extent(const uint4 &q, uint32_t &amax, uint32_t &amin) {
+    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = (wd[j] << 16) & 0x7FFF0000u, hi = wd[j] & 0x7FFF0000u;
+        amax = max(amax, max(lo, hi));
+        amin = min(amin, min(lo ? lo : 0x7F800000u, hi ? hi : 0x7F800000u));
+    }
+}
+__device__ __forceinline__ void sumsq_split8(const uint4 &q, float s1, float s2, float &a1,
+                                             float &a2, float &a3) {
+    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        sumsq_split(__uint_as_float(wd[j] << 16), s1, s2, a1, a2, a3);
+        sumsq_split(__uint_as_float(wd[j] & 0xFFFF0000u), s1, s2, a1, a2, a3);
+    }
+}
+
+// Scales of the fast path for the row's largest exponent ex: s1, s2 and the
+// factors that turn multiples of u1 and u2 into integers.
+struct SumsqScales {
+    float s1, s2, k1, k2;
+};
+__device__ __forceinline__ float pow2f(int e) {   // 2^e, e in fp32's normal range
+    return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+__device__ __forceinline__ SumsqScales sumsq_scales(int ex) {
+    return SumsqScales{pow2f(2 * ex + 9), pow2f(2 * ex - 7), pow2f(14 - 2 * ex), pow2f(30 - 2 * ex)};
+}
+
+// Pass 1 across the warp: 0 = the fast path applies (ex set), else the
+// result to return now: +0 for an all-zero row, inf/NaN for a non-finite
+// one, or a request for the slow path (flagged in *slow).
+__device__ __forceinline__ bool sumsq_plan(uint32_t amax, uint32_t amin, int *ex, float *early,
+                                           bool *slow) {
+    amax = warp_max_u32(amax);
+    amin = warp_min_u32(amin);
+    *slow = false;
+    if (amax == 0u) {
+        *early = 0.0f;
+        return false;
+    }
+    if (amax >= 0x7F800000u) {
+        *early = __uint_as_float(amax);   // inf, or NaN
+        return false;
+    }
+    *ex = static_cast<int>(amax >> 23) - 127;
+    if (*ex < -20 || *ex > 40 || amin < (67u << 23)) {   // 67 << 23 = 2^-60
+        *slow = true;
+        return false;
+    }
+    return true;
+}
+
+// Lanes' exact integer sums and fp32 residual sums -> the rounded result, or
+// the slow path when the residual's error interval holds a rounding tie.
+// nsq: squares per lane at most.
+__device__ __forceinline__ float sumsq_finish(long long n1, long long n2, float a3, int ex,
+                                              int nsq, const SumsqScales &sc, const uint4 *row,
+                                              int nvec) {
+    n1 = warp_sum_ll(n1);
+    n2 = warp_sum_ll(n2);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) a3 = __fadd_rn(a3, __shfl_xor_sync(0xffffffffu, a3, off));
+    const long long T = (n1 << 16) + n2;          // units u2 = 2^(2ex - 30)
+    long long res;
+    if (a3 == 0.0f) {
+        res = round24(T, 0.0);
+    } else {
+        const double A = static_cast<double>(a3) * static_cast<double>(sc.k2);
+        const double d = (nsq + 8.0) * 0x1p-23;
+        res = round24(T, A * (1.0 - d));
+        if (round24(T, A * (1.0 + d)) != res) return sumsq_row_exact(row, nvec);
+    }
+    // res has at most 24 significant bits: exact in fp32, and so is the
+    // power-of-two scaling (the result is normal)
+    return __fmul_rn(__ll2float_rn(res), pow2f(2 * ex - 30));
+}
+
+// The row's exact sum of squares rounded to fp32, by one warp, from the
+// lane's VPL vectors held in registers (vector lane + 32 i of the row; the
+// caller passes zeros past the row's nvec vectors).  `row` is the row in
+// memory, for the slow path.
+template <int VPL>
+__device__ __forceinline__ float warp_sumsq_rn(const uint4 (&vec)[VPL], const uint4 *row, int nvec) {
+    uint32_t amax = 0u, amin = 0x7F800000u;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) sumsq_extent(vec[i], amax, amin);
+    int ex = 0;
+    float early = 0.0f;
+    bool slow;
+    if (!sumsq_plan(amax, amin, &ex, &early, &slow)) return slow ? sumsq_row_exact(row, nvec) : early;
+    const SumsqScales sc = sumsq_scales(ex);
+    long long n1 = 0, n2 = 0;
+    float a3 = 0.0f;
+#pragma unroll
+    for (int g = 0; g < VPL; g += 16) {
+        float a1 = 0.0f, a2 = 0.0f;       // at most 128 squares: exact
+#pragma unroll
+        for (int i = g; i < g + 16 && i < VPL; ++i) sumsq_split8(vec[i], sc.s1, sc.s2, a1, a2, a3);
+        n1 += __float2ll_rn(__fmul_rn(a1, sc.k1));
+        n2 += __float2ll_rn(__fmul_rn(a2, sc.k2));
+    }
+    return sumsq_finish(n1, n2, a3, ex, 8 * VPL, sc, row, nvec);
+}
+
+// The same, reading the row (global or shared memory) twice instead of
+// holding it in registers.
+__device__ float warp_sumsq_rn_mem(const uint4 *row, int nvec) {
+    const int lane = threadIdx.x & 31;
+    uint32_t amax = 0u, amin = 0x7F800000u;
+    for (int v = lane; v < nvec; v += 32) sumsq_extent(row[v], amax, amin);
+    int ex = 0;
+    float early = 0.0f;
+    bool slow;
+    if (!sumsq_plan(amax, amin, &ex, &early, &slow)) return slow ? sumsq_row_exact(row, nvec) : early;
+    const SumsqScales sc = sumsq_scales(ex);
+    long long n1 = 0, n2 = 0;
+    float a3 = 0.0f;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * 16) {
+        float a1 = 0.0f, a2 = 0.0f;       // at most 128 squares: exact
+#pragma unroll 4
+        for (int v = v0; v < v0 + 32 * 16 && v < nvec; v += 32)
+            sumsq_split8(row[v], sc.s1, sc.s2, a1, a2, a3);
+        n1 += __float2ll_rn(__fmul_rn(a1, sc.k1));
+        n2 += __float2ll_rn(__fmul_rn(a2, sc.k2));
+    }
+    return sumsq_finish(n1, n2, a3, ex, 8 * ((nvec + 31) / 32), sc, row, nvec);
+}
+
 __global__ void __launch_bounds__(RT_THREADS)
 router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
               const float *__restrict__ wg, const float *__restrict__ gate_bias, int T, int H,
@@ -151,14 +423,10 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
               int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
               int32_t *__restrict__ hist, int32_t *dev_status) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *ss_buf = smem;                                        // phase 1 (phase 2 reuses it)
     float *lg = reinterpret_cast<float *>(smem + SMEM_MAIN);       // phase 3
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SMEM_MAIN + SMEM_LG);
-    uint64_t *full = bars;                 // [SS_STAGES]
-    uint64_t *empty = bars + SS_STAGES;    // [SS_STAGES]
-    float *s_r = reinterpret_cast<float *>(bars + 64);
+    float *s_r = reinterpret_cast<float *>(smem + SMEM_MAIN + SMEM_LG);
     int *s_cnt = reinterpret_cast<int *>(s_r + RT_TOK);
-    volatile int *s_abort = s_cnt + RT_EXP;
+    (void)dev_status;   // no waits that could time out
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -167,100 +435,28 @@ router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma
     const int e0 = blockIdx.y * RT_EXP;
     const int ntok = min(RT_TOK, T - tok0);
 
-    if (tid == 0) {
-        *s_abort = 0;
-        for (int s = 0; s < SS_STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        fence_barrier_init();
-    }
     if (tid < RT_EXP) s_cnt[tid] = 0;
     if (tid < RT_TOK) s_r[tid] = 1.0f;
     __syncthreads();
 
-    // ---------------- phase 1: r = 1/sqrt(mean(x^2) + eps) per token
+    // ---------------- phase 1: r = 1/sqrt(mean(x^2) + eps) per token, the
+    // sum of squares of each row by one warp (rows w, w + 4, ...)
     if (rmsnorm) {
-        const int npieces = (H + SS_HC - 1) / SS_HC;
-        if (warp == 1) {
-            // producer: lane t copies token t's piece of every stage
-            uint32_t phase = 0;
-            int armed[SS_STAGES];
-            for (int s = 0; s < SS_STAGES; ++s) armed[s] = -1;
-            for (int c = 0, s = 0; c < npieces; ++c) {
-                if (!mbar_wait_bounded(&empty[s], phase ^ 1, s_abort, dev_status)) break;
-                armed[s] = static_cast<int>(phase);
-                const int h0 = c * SS_HC;
-                const int bytes = min(SS_HC, H - h0) * 2;
-                if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes * ntok);
-                __syncwarp();
-                if (lane < ntok) {
-                    const uint16_t *src = x + static_cast<size_t>(tok0 + lane) * H + h0;
-                    uint8_t *dst = ss_buf + (s * RT_TOK + lane) * SS_ROW;
-                    asm volatile(
-                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
-                        " [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
-                        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
-                        "r"(smem_u32(&full[s]))
-                        : "memory");
-                }
-                if (++s == SS_STAGES) {
-                    s = 0;
-                    phase ^= 1;
-                }
-            }
-            if (*s_abort) {
-                // unwinding: let every copy this warp started land first
-                for (int s = 0; s < SS_STAGES; ++s)
-                    if (armed[s] >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>(armed[s]));
-            }
-        } else if (warp == 0) {
-            // consumer: lane t sums token t's squares in ascending h
-            float ss = 0.0f;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int c = 0, s = 0; c < npieces; ++c) {
-                if (!mbar_wait_bounded(&full[s], phase, s_abort, dev_status)) {
-                    ok = false;
-                    break;
-                }
-                const int nv = min(SS_HC, H - c * SS_HC) / 8;
-                const uint4 *row =
-                    reinterpret_cast<const uint4 *>(ss_buf + (s * RT_TOK + lane) * SS_ROW);
-                uint4 q = row[0];
-                for (int v = 0; v < nv; ++v) {
-                    const uint4 qn = row[v + 1 < nv ? v + 1 : v];   // load ahead of the chain
-                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float a = __uint_as_float(w[i] << 16);
-                        const float b = __uint_as_float(w[i] & 0xFFFF0000u);
-                        ss = __fmaf_rn(a, a, ss);
-                        ss = __fmaf_rn(b, b, ss);
-                    }
-                    q = qn;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-                if (++s == SS_STAGES) {
-                    s = 0;
-                    phase ^= 1;
-                }
-            }
-            if (ok) {
+        for (int t = warp; t < ntok; t += RT_THREADS / 32) {
+            const float ss = warp_sumsq_rn_mem(
+                reinterpret_cast<const uint4 *>(x + static_cast<size_t>(tok0 + t) * H), H / 8);
+            if (lane == 0) {
                 const float mean = __fdiv_rn(ss, static_cast<float>(H));
-                s_r[lane] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+                s_r[t] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
             }
         }
         __syncthreads();
-        if (*s_abort) return;
     }
 
     // ---------------- phase 2: logits
     // Slices of G_HC columns: the raw x slice (bf16) and the gate-weight slice
     // (fp32, padded rows) arrive through a G_STAGES-deep cp.async ring; each x
     // slice is then normalised once into an fp32 buffer (double-buffered).
-    fence_proxy_async();      // phase 1 wrote this memory through the async proxy
     __syncthreads();
     uint8_t *wg_ring = smem;
     uint8_t *xr_ring = smem + G_STAGES * WG_STAGE;
@@ -542,52 +738,26 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
     consumer_sync(nc);
 
     if (rmsnorm) {
-        // lane 0 of warp tk runs token tk's chain; the other consumers fetch
-        // their gamma groups meanwhile (nvec <= SMALL_MAX_H / 8, nc >= 64: at
-        // most 16 each)
-        const bool chain = (tid & 31) == 0 && (tid >> 5) < TPC;
+        // warp tk takes token tk's sum of squares (reading the row from
+        // memory); every consumer fetches its gamma groups meanwhile
+        // (nvec <= SMALL_MAX_H / 8, nc >= 64: at most 16 each)
         constexpr int GQ = SMALL_MAX_H / 8 / 64;
         uint4 gqs[GQ];
 #pragma unroll
         for (int j = 0; j < GQ; ++j) {
             const int v = tid + j * nc;
             gqs[j] = make_uint4(0u, 0u, 0u, 0u);
-            if (gamma && !chain && v < nvec)
-                gqs[j] = __ldg(reinterpret_cast<const uint4 *>(gamma) + v);
+            if (gamma && v < nvec) gqs[j] = __ldg(reinterpret_cast<const uint4 *>(gamma) + v);
         }
-        if (chain) {
-            // one sequential chain; its operands are read into registers 32
-            // values ahead (H is a multiple of 64)
+        if ((tid >> 5) < TPC) {
             const int tk = tid >> 5;
-            float ss = 0.0f;
-            const float4 *xv = reinterpret_cast<const float4 *>(xf + tk * H);
-            float4 qa[8], qb[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) qa[i] = xv[i];
-            for (int b = 0; b < H / 4; b += 16) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) qb[i] = xv[b + 8 + i];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    ss = __fmaf_rn(qa[i].x, qa[i].x, ss);
-                    ss = __fmaf_rn(qa[i].y, qa[i].y, ss);
-                    ss = __fmaf_rn(qa[i].z, qa[i].z, ss);
-                    ss = __fmaf_rn(qa[i].w, qa[i].w, ss);
-                }
-                if (b + 16 < H / 4) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) qa[i] = xv[b + 16 + i];
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    ss = __fmaf_rn(qb[i].x, qb[i].x, ss);
-                    ss = __fmaf_rn(qb[i].y, qb[i].y, ss);
-                    ss = __fmaf_rn(qb[i].z, qb[i].z, ss);
-                    ss = __fmaf_rn(qb[i].w, qb[i].w, ss);
-                }
+            const int t = tk < ntok ? t0 + tk : t0;
+            const float ss = warp_sumsq_rn_mem(
+                reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H), nvec);
+            if ((tid & 31) == 0) {
+                const float mean = __fdiv_rn(ss, static_cast<float>(H));
+                s_r[tk] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
             }
-            const float mean = __fdiv_rn(ss, static_cast<float>(H));
-            s_r[tk] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
         }
         consumer_sync(nc);
 #pragma unroll
@@ -596,8 +766,7 @@ router_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
             if (v >= nvec) break;
             float gm[8];
             if (gamma) {
-                const uint4 gq =
-                    !chain ? gqs[j] : __ldg(reinterpret_cast<const uint4 *>(gamma) + v);
+                const uint4 gq = gqs[j];
                 const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -753,195 +922,72 @@ topk_kernel(const float *__restrict__ logits, int T, int E, int k, int renorm,
 }
 
 // ---------------------------------------------------------------- RMSNorm alone
-// Used ahead of the tensor-core gate.  The sum of squares of a row is one
-// sequential fused multiply-add chain in ascending h (lane t of warp 0 takes
-// row t of a batch), so what bounds the kernel is how many rows are summed
-// at once: each CTA keeps a batch of whole rows resident in shared memory
-// (as many as fit, at most 32) and normalises them from there once their
-// factors are known, so x is read from memory once.
-//   warp 0     the chains; after a batch it publishes the factors (named
-//              barrier 2, with the workers) and starts on the next batch;
-//   warps 1..7 the workers: normalise the finished batch chunk by chunk
-//              and refill each chunk with the next batch's rows as soon as
-//              every worker is done reading it (named barrier 1), with
-//              16-byte cp.async copies; a chunk's mbarrier completes when
-//              every worker's copies of it have landed.
-// Every worker thread owns one 16-byte column group of a chunk and a
-// stride of rows, so the gamma values it needs are loaded once per chunk.
-// Row stride H*2 + 16 bytes keeps the 32 lanes' 16-byte reads of one
-// column in distinct banks.
+// Used ahead of the tensor-core gate: one warp per row.  The row (at most
+// VPL 16-byte vectors per lane) is held in registers; its sum of squares is
+// the warp's exact one above; then xn = bf16((x * r) * gamma) leaves as
+// 16-byte stores.  No shared memory, no waits.
 constexpr int RN_THREADS = 256;
-constexpr int RN_WORKERS = RN_THREADS - 32;
-constexpr int RN_MAX_CHUNKS = 64;
-constexpr int RN_SMEM_CAP = 220 * 1024;
 
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-__device__ __forceinline__ void named_bar_arrive(int id, int n) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-__global__ void __launch_bounds__(RN_THREADS)
+template <int VPL>
+__global__ void __launch_bounds__(RN_THREADS, 2)
 rmsnorm_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma, int T, int H,
-               float eps, uint16_t *__restrict__ xn, int rows, int chunk_cols, int nchunks,
-               int stride, int32_t *dev_status) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t full[RN_MAX_CHUNKS];
-    __shared__ float s_r[2][32];
-    __shared__ int s_stop[2];    // per batch parity: the chains gave up (bounded wait ran out)
-    __shared__ int s_abort_v;
-    volatile int *s_abort = &s_abort_v;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) {
-        *s_abort = 0;
-        for (int c = 0; c < nchunks; ++c) mbar_init(&full[c], RN_WORKERS);
-        fence_barrier_init();
-    }
-    __syncthreads();
-    const int nbatch = (T + rows - 1) / rows;
-    const int nb = blockIdx.x < nbatch ? (nbatch - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-
-    if (warp == 0) {
-        for (int b = 0; b < nb; ++b) {
-            const int t0 = (blockIdx.x + b * gridDim.x) * rows;
-            const int nr = min(rows, T - t0);
-            const uint32_t parity = b & 1;
-            float ss = 0.0f;
-            bool ok = true;
-            for (int c = 0; c < nchunks; ++c) {
-                if (!mbar_wait_bounded(&full[c], parity, s_abort, dev_status)) {
-                    ok = false;
-                    break;
-                }
-                if (lane < nr) {
-                    const int h0 = c * chunk_cols;
-                    const int nv = min(chunk_cols, H - h0) / 8;   // even: chunks are 128k columns
-                    const uint4 *row = reinterpret_cast<const uint4 *>(smem + lane * stride + h0 * 2);
-                    uint4 q0 = row[0], q1 = row[1];
-                    for (int v = 0; v < nv; v += 2) {
-                        const int vn = v + 2 < nv ? v + 2 : v;  // ahead of the chain
-                        const uint4 n0 = row[vn], n1 = row[vn + 1];
-                        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+               float eps, uint16_t *__restrict__ xn) {
+    const int lane = threadIdx.x & 31;
+    const int nvec = H / 8;
+    const int nwarps = gridDim.x * (RN_THREADS / 32);
+    for (int t = blockIdx.x * (RN_THREADS / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
+        uint4 q[VPL];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float a = __uint_as_float(w[i] << 16);
-                            const float bb = __uint_as_float(w[i] & 0xFFFF0000u);
-                            ss = __fmaf_rn(a, a, ss);
-                            ss = __fmaf_rn(bb, bb, ss);
-                        }
-                        q0 = n0;
-                        q1 = n1;
-                    }
+        for (int i = 0; i < VPL; ++i) {
+            const int v = lane + 32 * i;
+            q[i] = v < nvec ? __ldcs(row + v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const float ss = warp_sumsq_rn<VPL>(q, row, nvec);
+        const float mean = __fdiv_rn(ss, static_cast<float>(H));
+        const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+        uint4 *out = reinterpret_cast<uint4 *>(xn + static_cast<size_t>(t) * H);
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int v = lane + 32 * i;
+            if (v >= nvec) break;
+            float gm[8];
+            if (gamma) {
+                const uint4 gq = __ldg(reinterpret_cast<const uint4 *>(gamma) + v);
+                const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    gm[2 * j] = __uint_as_float(gw[j] << 16);
+                    gm[2 * j + 1] = __uint_as_float(gw[j] & 0xFFFF0000u);
                 }
             }
-            if (ok && lane < nr) {
-                const float mean = __fdiv_rn(ss, static_cast<float>(H));
-                s_r[parity][lane] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
-            }
-            if (lane == 0) s_stop[parity] = ok ? 0 : 1;
-            __syncwarp();
-            named_bar_arrive(2, RN_THREADS);    // factors of batch b (or the stop) published
-            if (!ok) return;
-        }
-        return;
-    }
-
-    // workers
-    const int lt = tid - 32;
-    auto load_chunk = [&](int b, int c) {
-        const int t0 = (blockIdx.x + b * gridDim.x) * rows;
-        const int nr = min(rows, T - t0);
-        const int h0 = c * chunk_cols;
-        const int cg = min(chunk_cols, H - h0) / 8;
-        const int rstep = RN_WORKERS / cg;
-        const int g = lt % cg;
-        if (lt < rstep * cg)
-            for (int r = lt / cg; r < nr; r += rstep)
-                cp_async16(smem + r * stride + h0 * 2 + g * 16,
-                           x + static_cast<size_t>(t0 + r) * H + h0 + g * 8, 16);
-        cp_async_arrive_noinc(&full[c]);
-    };
-    if (nb > 0)
-        for (int c = 0; c < nchunks; ++c) load_chunk(0, c);
-    for (int b = 0; b < nb; ++b) {
-        named_bar_sync(2, RN_THREADS);
-        // s_stop[b & 1] is not written again before every worker has passed
-        // the next barrier 2, so all workers see the same value
-        if (s_stop[b & 1]) break;
-        const int t0 = (blockIdx.x + b * gridDim.x) * rows;
-        const int nr = min(rows, T - t0);
-        const float *rr = s_r[b & 1];
-        // gamma of the thread's column group, one chunk ahead
-        auto gamma_of = [&](int c) {
-            const int h0 = c * chunk_cols;
-            const int cg = min(chunk_cols, H - h0) / 8;
-            return gamma && lt < (RN_WORKERS / cg) * cg
-                       ? __ldg(reinterpret_cast<const uint4 *>(gamma + h0) + lt % cg)
-                       : make_uint4(0u, 0u, 0u, 0u);
-        };
-        uint4 gq_next = gamma_of(0);
-        for (int c = 0; c < nchunks; ++c) {
-            const int h0 = c * chunk_cols;
-            const int cg = min(chunk_cols, H - h0) / 8;
-            const int rstep = RN_WORKERS / cg;
-            const int g = lt % cg;
-            const uint4 gq = gq_next;
-            if (c + 1 < nchunks) gq_next = gamma_of(c + 1);
-            if (lt < rstep * cg) {
-                float gm[8];
+            const uint32_t wd[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+            uint32_t packed[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float lo = __fmul_rn(__uint_as_float(wd[j] << 16), r);
+                float hi = __fmul_rn(__uint_as_float(wd[j] & 0xFFFF0000u), r);
                 if (gamma) {
-                    const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        gm[2 * i] = __uint_as_float(gw[i] << 16);
-                        gm[2 * i + 1] = __uint_as_float(gw[i] & 0xFFFF0000u);
-                    }
+                    lo = __fmul_rn(lo, gm[2 * j]);
+                    hi = __fmul_rn(hi, gm[2 * j + 1]);
                 }
-                for (int r0 = lt / cg; r0 < nr; r0 += 4 * rstep) {
-                    uint4 q[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int r = r0 + j * rstep;
-                        if (r < nr)
-                            q[j] = *reinterpret_cast<const uint4 *>(smem + r * stride + h0 * 2 +
-                                                                    g * 16);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int r = r0 + j * rstep;
-                        if (r >= nr) break;
-                        const float rv = rr[r];
-                        const uint32_t w[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
-                        uint32_t packed[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            float lo = __fmul_rn(__uint_as_float(w[i] << 16), rv);
-                            float hi = __fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), rv);
-                            if (gamma) {
-                                lo = __fmul_rn(lo, gm[2 * i]);
-                                hi = __fmul_rn(hi, gm[2 * i + 1]);
-                            }
-                            const __nv_bfloat162 p2 = __floats2bfloat162_rn(lo, hi);
-                            packed[i] = *reinterpret_cast<const uint32_t *>(&p2);
-                        }
-                        *reinterpret_cast<uint4 *>(xn + static_cast<size_t>(t0 + r) * H + h0 +
-                                                   g * 8) =
-                            make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                    }
-                }
+                const __nv_bfloat162 p2 = __floats2bfloat162_rn(lo, hi);
+                packed[j] = *reinterpret_cast<const uint32_t *>(&p2);
             }
-            if (b + 1 < nb) {
-                named_bar_sync(1, RN_WORKERS);   // every worker is done reading chunk c
-                load_chunk(b + 1, c);
-            }
+            out[v] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
     }
-    cp_async_wait<0>();    // nothing of this CTA's copies is left in flight
+}
+
+// The sum of squares alone, one warp per row (moe_rmsnorm_sumsq).
+__global__ void __launch_bounds__(256)
+sumsq_kernel(const uint16_t *__restrict__ x, int T, int H, float *__restrict__ ss) {
+    const int nwarps = gridDim.x * 8;
+    for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += nwarps) {
+        const float v = warp_sumsq_rn_mem(
+            reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H), H / 8);
+        if ((threadIdx.x & 31) == 0) ss[t] = v;
+    }
 }
 
 // ---------------------------------------------------------------- tensor-core gate
@@ -1205,36 +1251,33 @@ cudaError_t launch_topk(const float *logits, int T, int E, int k, bool renorm,
 
 cudaError_t launch_rmsnorm(const uint16_t *x, const uint16_t *gamma, int T, int H, float eps,
                            uint16_t *xn, int32_t *dev_status, cudaStream_t stream) {
+    (void)dev_status;    // the kernel has no waits to time out
     if (T == 0) return cudaSuccess;
     if (H <= 0 || H % 128 != 0) return cudaErrorInvalidValue;
-    const int stride = H * 2 + 16;
-    const int rows = std::min(32, RN_SMEM_CAP / stride);
-    if (rows < 1) return cudaErrorInvalidValue;
-    // chunks of 256 columns (at most RN_MAX_CHUNKS of them, and at most 8 *
-    // RN_WORKERS columns, so that every worker owns at most one column group)
-    const int chunk_cols = std::max(256, static_cast<int>(ceil_div(H, RN_MAX_CHUNKS * 128)) * 128);
-    const int nchunks = static_cast<int>(ceil_div(H, chunk_cols));
-    if (chunk_cols / 8 > RN_WORKERS || nchunks > RN_MAX_CHUNKS) return cudaErrorInvalidValue;
-    const int smem = rows * stride;
-    static std::mutex mu;
-    static int attr_smem[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev < 64 && attr_smem[dev] < smem) {
-            cudaError_t e = cudaFuncSetAttribute(rmsnorm_kernel,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 RN_SMEM_CAP);
-            if (e != cudaSuccess) return e;
-            attr_smem[dev] = RN_SMEM_CAP;
-        }
-    }
-    const int per_sm = std::max(1, std::min(8, (227 * 1024) / (smem + 1024)));
-    const int64_t nbatch = ceil_div(T, rows);
-    const int grid = static_cast<int>(std::min<int64_t>(nbatch, int64_t{num_sms()} * per_sm));
-    rmsnorm_kernel<<<grid, RN_THREADS, smem, stream>>>(x, gamma, T, H, eps, xn, rows, chunk_cols,
-                                                       nchunks, stride, dev_status);
+    // one warp per row: enough rows in flight to cover the memory latency
+    const int vpl = static_cast<int>(ceil_div(H / 8, 32));
+    const int64_t warps = T;
+    const int grid = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>(ceil_div(warps, RN_THREADS / 32), int64_t{num_sms()} * 4)));
+    if (vpl <= 4)
+        rmsnorm_kernel<4><<<grid, RN_THREADS, 0, stream>>>(x, gamma, T, H, eps, xn);
+    else if (vpl <= 8)
+        rmsnorm_kernel<8><<<grid, RN_THREADS, 0, stream>>>(x, gamma, T, H, eps, xn);
+    else if (vpl <= 16)
+        rmsnorm_kernel<16><<<grid, RN_THREADS, 0, stream>>>(x, gamma, T, H, eps, xn);
+    else if (vpl <= 32)
+        rmsnorm_kernel<32><<<grid, RN_THREADS, 0, stream>>>(x, gamma, T, H, eps, xn);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sumsq(const uint16_t *x, int T, int H, float *ss, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    if (H <= 0 || H % 8 != 0) return cudaErrorInvalidValue;
+    const int grid = static_cast<int>(
+        std::max<int64_t>(1, std::min<int64_t>(ceil_div(T, 8), int64_t{num_sms()} * 8)));
+    sumsq_kernel<<<grid, 256, 0, stream>>>(x, T, H, ss);
     return cudaGetLastError();
 }
 

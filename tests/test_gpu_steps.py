@@ -61,9 +61,9 @@ def test_rmsnorm_gate_bitexact(wl):
     assert np.array_equal(logits.cpu().numpy().view(np.uint32), lg_ref.view(np.uint32))
 
 
-# the RMSNorm-only pass (ahead of the tensor-core gate): rows resident in
-# shared memory, 27 rows per CTA at H=4096, 32 below; chunked fills; many
-# batches per CTA; a ragged last batch; gamma absent (all ones)
+# the RMSNorm-only pass (ahead of the tensor-core gate): one warp per row,
+# rows in registers (up to 4, 8, 16 or 32 vectors per lane), many rows per
+# warp, ragged vector counts (H = 384); gamma absent (all ones)
 @pytest.mark.parametrize("T,H,gamma_std,with_gamma", [
     (1, 128, 0.1, True), (33, 4096, 0.1, True), (5000, 4096, 0.1, True),
     (1000, 1024, 0.0, False), (700, 8192, 0.2, True), (64, 384, 0.1, True),
@@ -78,6 +78,80 @@ def test_rmsnorm_only_bitexact(T, H, gamma_std, with_gamma):
     assert lg is None
     ones = torch.ones(H, dtype=torch.bfloat16)
     assert np.array_equal(u16(xn), oracle.rmsnorm(d["x"], gamma if with_gamma else ones, wl.eps))
+
+
+def _bf16_rows(rows):
+    """float64 rows -> bf16 torch tensor (values rounded once to bf16)."""
+    return torch.from_numpy(np.ascontiguousarray(rows, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _sumsq_cases(H):
+    """Rows whose sums of squares exercise the exact rounding: random rows of
+    many scales and of a 120-binade spread, exact ties and sums just above
+    them, sums that the fast path cannot decide (its residual bound straddles
+    a tie), largest values outside its exponent range, values below 2^-60 next
+    to normal ones, bf16 subnormals, fp32 subnormal and overflowing sums,
+    zeros and single nonzero values."""
+    rng = np.random.default_rng(21 + H)
+    rows = []
+    for scale in (1.0, 2.0 ** -10, 2.0 ** 12, 2.0 ** -19, 2.0 ** 38):
+        rows += [rng.standard_normal(H) * scale for _ in range(3)]
+    rows.append(rng.standard_normal(H) * 2.0 ** rng.integers(-60, 60, H))
+    z = np.zeros(H)
+
+    def row(vals):
+        r = z.copy()
+        r[:len(vals)] = vals
+        return r
+    big = [2.0 ** 11] * 4
+    rows.append(row(big + [1.0]))                          # 2^24 + 1: tie, to even
+    rows.append(row(big + [1.0, 2.0 ** -30]))              # just above the tie
+    rows.append(row(big + [1.0] * 3))                      # 2^24 + 3: tie, to even
+    near = [1.0] + [2.0 ** -13] * 3 + [2.0 ** -14] * 3 + [2.0 ** -15] * 3
+    rows.append(row(near + [2.0 ** -16] * 4))              # an exact tie the bound straddles
+    rows.append(row(near + [2.0 ** -16] * 4 + [2.0 ** -40]))   # 2^-80 above it
+    rows.append(row(near + [2.0 ** -16] * 5))              # a quarter unit above it
+    rows.append(rng.standard_normal(H) * 2.0 ** 45)         # largest exponent > 40
+    rows.append(rng.standard_normal(H) * 2.0 ** -40)        # largest exponent < -20
+    rows.append(row([1.5, 2.0 ** -70, -(2.0 ** -80)]))     # nonzero values below 2^-60
+    rows.append(row([2.0 ** -130, 3 * 2.0 ** -133, 2.0 ** -127]))   # bf16 subnormals
+    rows.append(row([2.0 ** -70] * 4))                     # fp32 subnormal sum
+    rows.append(row([2.0 ** -75] * 3))                     # 1.5 * 2^-149: tie to 2^-148
+    rows.append(row([2.0 ** 64]))                          # overflows to infinity
+    rows.append(z.copy())
+    rows.append(row([-3.0]))
+    return _bf16_rows(np.array(rows))
+
+
+@pytest.mark.parametrize("H", [4096, 16, 136, 1024, 8192])
+def test_rmsnorm_sumsq_is_the_exact_sum_rounded_once(H):
+    x = _sumsq_cases(H)
+    ss = moe.rmsnorm_sumsq(x.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.sumsq(x)
+    got = ss.cpu().numpy()
+    bad = np.nonzero(got.view(np.uint32) != ref.view(np.uint32))[0]
+    assert bad.size == 0, f"rows {bad.tolist()}: {got[bad]} vs {ref[bad]}"
+
+
+def test_rmsnorm_only_on_exact_sum_edge_rows():
+    """xn of the RMSNorm pass on the same edge rows (finite ones; ties,
+    straddled bounds, subnormals) equals the oracle's bit for bit."""
+    x = _sumsq_cases(4096)
+    keep = np.isfinite(oracle.sumsq(x)) & (oracle.sumsq(x) > 0)
+    x = x[torch.from_numpy(keep)]
+    gamma = _bf16_rows(1 + 0.1 * np.random.default_rng(5).standard_normal(4096))
+    for eps in (1e-6, 0.0):
+        xn, _ = moe.rmsnorm_gate(x.to(DEV), None, gamma.to(DEV), None, eps)
+        torch.cuda.synchronize()
+        got, ref = u16(xn), oracle.rmsnorm(x, gamma, eps)
+        # with eps = 0 a row whose mean of squares underflows to zero gives
+        # 0 * inf = NaN: NaN in the same places (the payloads may differ)
+        nan_g = (got & 0x7F80) == 0x7F80
+        nan_g &= (got & 0x7F) != 0
+        nan_r = ((ref & 0x7F80) == 0x7F80) & ((ref & 0x7F) != 0)
+        assert np.array_equal(nan_g, nan_r), eps
+        assert np.array_equal(got[~nan_g], ref[~nan_r]), eps
 
 
 def test_rmsnorm_gate_empty():
@@ -164,7 +238,11 @@ def _grouped_case(counts, H, I, seed):
     ([0, 1, 129, 0, 255, 37, 0, 512], 384, 256),
     ([5, 0, 0, 128, 127], 128, 384),            # H=128: 128-wide down tiles
     ([700, 3, 64], 512, 128),
-], ids=["dense", "ragged", "h128", "mixed"])
+    # shapes the wide pair kernel takes (I % 256 == 0, H % 512 == 0): empty,
+    # one-row, half-tile (<= 128 rows) and multi-block groups
+    ([0, 1, 129, 0, 255, 37, 0, 512, 300], 512, 256),
+    ([1000, 600, 64, 257], 1024, 512),
+], ids=["dense", "ragged", "h128", "mixed", "wide-ragged", "wide-big"])
 def test_grouped_mlp(counts, H, I):
     x, w13, w2, off = _grouped_case(counts, H, I, len(counts) * 31 + H)
     st = moe.new_status(DEV)
