@@ -303,6 +303,44 @@ __device__ __forceinline__ void sumsq_split8(const uint4 &q, float s1, float s2,
     }
 }
 
+// Packed fp32 pairs (the two halves of a 64-bit register) for the RMSNorm
+// pass: one instruction works on both values.
+__device__ __forceinline__ uint64_t f2_add_rz(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// a bf16 pair word -> the fp32 pair (low value, high value)
+__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w) {
+    return static_cast<uint64_t>(w << 16) | (static_cast<uint64_t>(w & 0xFFFF0000u) << 32);
+}
+__device__ __forceinline__ uint64_t f2_splat(float v) {
+    const uint64_t u = __float_as_uint(v);
+    return u | (u << 32);
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // Scales of the fast path for the row's largest exponent ex: s1, s2 and the
 // factors that turn multiples of u1 and u2 into integers.
 struct SumsqScales {
@@ -389,6 +427,67 @@ __device__ __forceinline__ float warp_sumsq_rn(const uint4 (&vec)[VPL], const ui
         n2 += __float2ll_rn(__fmul_rn(a2, sc.k2));
     }
     return sumsq_finish(n1, n2, a3, ex, 8 * VPL, sc, row, nvec);
+}
+
+// The register variant on packed fp32 pairs, for the RMSNorm pass.  Only the
+// largest magnitude is taken in the first pass (packed 16-bit maxima): a
+// nonzero |x| below 2^-63 would give an inexact fp32 square (at most 2^-149
+// off, or zero), so the residual interval is widened by H * 2^-149 and an
+// exact tie with no residual at all goes to the slow path.
+template <int VPL>
+__device__ __forceinline__ float warp_sumsq_rn_packed(const uint4 (&vec)[VPL], const uint4 *row,
+                                                      int nvec) {
+    uint32_t mx = 0u;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        mx = max_u16x2(mx, vec[i].x & 0x7FFF7FFFu);
+        mx = max_u16x2(mx, vec[i].y & 0x7FFF7FFFu);
+        mx = max_u16x2(mx, vec[i].z & 0x7FFF7FFFu);
+        mx = max_u16x2(mx, vec[i].w & 0x7FFF7FFFu);
+    }
+    const uint32_t amax = warp_max_u32(max(mx & 0xFFFFu, mx >> 16) << 16);
+    if (amax == 0u) return 0.0f;
+    if (amax >= 0x7F800000u) return __uint_as_float(amax);   // inf, or NaN
+    const int ex = static_cast<int>(amax >> 23) - 127;
+    if (ex < -20 || ex > 40) return sumsq_row_exact(row, nvec);
+    const SumsqScales sc = sumsq_scales(ex);
+    const uint64_t s1 = f2_splat(sc.s1), s2 = f2_splat(sc.s2);
+    long long n1 = 0, n2 = 0;
+    uint64_t a3 = 0;
+#pragma unroll
+    for (int g = 0; g < VPL; g += 16) {
+        uint64_t a1 = 0, a2 = 0;       // 64 squares per half at most: exact
+#pragma unroll
+        for (int i = g; i < g + 16 && i < VPL; ++i) {
+            const uint32_t wd[4] = {vec[i].x, vec[i].y, vec[i].z, vec[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint64_t x2 = f2_from_bf16x2(wd[j]);
+                const uint64_t sq = f2_mul(x2, x2);
+                const uint64_t q1 = f2_sub(f2_add_rz(s1, sq), s1);
+                a1 = f2_add(a1, q1);
+                const uint64_t r1 = f2_sub(sq, q1);
+                const uint64_t q2 = f2_sub(f2_add_rz(s2, r1), s2);
+                a2 = f2_add(a2, q2);
+                a3 = f2_add(a3, f2_sub(r1, q2));
+            }
+        }
+        n1 += __float2ll_rn(__fmul_rn(f2_lo(a1), sc.k1)) + __float2ll_rn(__fmul_rn(f2_hi(a1), sc.k1));
+        n2 += __float2ll_rn(__fmul_rn(f2_lo(a2), sc.k2)) + __float2ll_rn(__fmul_rn(f2_hi(a2), sc.k2));
+    }
+    n1 = warp_sum_ll(n1);
+    n2 = warp_sum_ll(n2);
+    float r = __fadd_rn(f2_lo(a3), f2_hi(a3));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) r = __fadd_rn(r, __shfl_xor_sync(0xffffffffu, r, off));
+    const long long T = (n1 << 16) + n2;          // units u2 = 2^(2ex - 30)
+    const double A = static_cast<double>(r) * static_cast<double>(sc.k2);
+    const double d = (8.0 * VPL + 8.0) * 0x1p-23;
+    // squares of values below 2^-63: at most 2^-149 each from exact, in units of u2
+    const double tiny = 8.0 * 32 * VPL * ldexp(1.0, -119 - 2 * ex);
+    const long long res = round24(T, A * (1.0 - d));
+    if (round24(T, A * (1.0 + d) + tiny) != res) return sumsq_row_exact(row, nvec);
+    return __fmul_rn(__ll2float_rn(res), pow2f(2 * ex - 30));
 }
 
 // The same, reading the row (global or shared memory) twice instead of
@@ -943,35 +1042,25 @@ rmsnorm_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamm
             const int v = lane + 32 * i;
             q[i] = v < nvec ? __ldcs(row + v) : make_uint4(0u, 0u, 0u, 0u);
         }
-        const float ss = warp_sumsq_rn<VPL>(q, row, nvec);
+        const float ss = warp_sumsq_rn_packed<VPL>(q, row, nvec);
         const float mean = __fdiv_rn(ss, static_cast<float>(H));
-        const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+        const uint64_t r2 = f2_splat(__fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps))));
         uint4 *out = reinterpret_cast<uint4 *>(xn + static_cast<size_t>(t) * H);
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
             const int v = lane + 32 * i;
             if (v >= nvec) break;
-            float gm[8];
-            if (gamma) {
-                const uint4 gq = __ldg(reinterpret_cast<const uint4 *>(gamma) + v);
-                const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    gm[2 * j] = __uint_as_float(gw[j] << 16);
-                    gm[2 * j + 1] = __uint_as_float(gw[j] & 0xFFFF0000u);
-                }
-            }
+            uint4 gq = make_uint4(0u, 0u, 0u, 0u);
+            if (gamma) gq = __ldg(reinterpret_cast<const uint4 *>(gamma) + v);
+            const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
             const uint32_t wd[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
             uint32_t packed[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float lo = __fmul_rn(__uint_as_float(wd[j] << 16), r);
-                float hi = __fmul_rn(__uint_as_float(wd[j] & 0xFFFF0000u), r);
-                if (gamma) {
-                    lo = __fmul_rn(lo, gm[2 * j]);
-                    hi = __fmul_rn(hi, gm[2 * j + 1]);
-                }
-                const __nv_bfloat162 p2 = __floats2bfloat162_rn(lo, hi);
+                // (x * r) * gamma, each product rounded, on both values at once
+                uint64_t y = f2_mul(f2_from_bf16x2(wd[j]), r2);
+                if (gamma) y = f2_mul(y, f2_from_bf16x2(gw[j]));
+                const __nv_bfloat162 p2 = __floats2bfloat162_rn(f2_lo(y), f2_hi(y));
                 packed[j] = *reinterpret_cast<const uint32_t *>(&p2);
             }
             out[v] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
