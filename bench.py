@@ -226,12 +226,18 @@ def kernel_fingerprint() -> str:
     return h.hexdigest()[:12]
 
 
+# the committed ncu summary that holds each workload's w13 DRAM bytes per launch
+TRAFFIC_PROFILES = {"imagegen-16k": "grouped_gemm_wide_small.md"}
+
+
 def recorded_traffic(workload: str):
     """DRAM bytes per launch of the w13 GEMM from the committed ncu summary,
     if it was taken on the current kernel source for this workload."""
-    path = os.path.join(ROOT, "profiles", "gemm_w13_swiglu_" + workload + ".md")
+    name = TRAFFIC_PROFILES.get(workload)
+    if name is None:
+        return None
     try:
-        text = open(path).read()
+        text = open(os.path.join(ROOT, "profiles", name)).read()
     except OSError:
         return None
     fp = kernel_fingerprint()
