@@ -92,6 +92,9 @@ def parse_args():
     ap.add_argument("--y-f32", action="store_true",
                     help="time the layer with fp32 routed expert outputs (MOE_Y_F32) as the "
                          "main line")
+    ap.add_argument("--gather-a", default="off", choices=["on", "off"],
+                    help="MOE_GATHER_A: the routed w13 matmul reads its rows by source token "
+                         "(no permute pass) where it runs as the wide pair kernel")
     ap.add_argument("--steady-seconds", type=float, default=4.0,
                     help="length of the steady-state loop (0 skips it)")
     return ap.parse_args()
@@ -267,21 +270,22 @@ def cpu_oracle_rate(inputs_cpu, wl, seconds, first_token=0):
 
 
 # --------------------------------------------------------------- our arm
-def stage_bytes_flops(wl, two_streams=False, active=None, y_f32=False):
+def stage_bytes_flops(wl, two_streams=False, active=None, y_f32=False, gather=False):
     """Algorithmic work of each timed stage.  With two streams the row copies
     run on the second stream beside the shared expert's w13, so the permute
     stage of the main stream is empty and gets no bytes; both matmul stages
     still run every matmul on the main stream.  Given the number of experts
     that receive rows, the matmul stages also get their bytes: the weights of
     those experts (and the shared expert's) once, their input rows and their
-    outputs."""
+    outputs.  With the rows gathered inside the w13 matmul there is no
+    permute pass either."""
     T, H, E, k, I, Is = wl.T, wl.H, wl.E, wl.k, wl.I, wl.I_s
     N = T * k
     # algorithmic work of each stage (what the step must touch or compute once)
     work = {
         "router": {"bytes": T * H * 2 + (T * H * 2 if wl.rmsnorm else 0) + E * H * 4 + N * 8,
                    "gate_flops": 2.0 * T * H * E},
-        "permute": {"bytes": 0 if two_streams else T * H * 2 + N * H * 2 + N * 4},
+        "permute": {"bytes": 0 if two_streams or gather else T * H * 2 + N * H * 2 + N * 4},
         "gemm_w13_swiglu": {"flops": 4.0 * N * H * I + 4.0 * T * H * Is},
         "gemm_down": {"flops": 2.0 * N * H * I + 2.0 * T * H * Is},
         "finalize": {"bytes": N * H * (4 if y_f32 else 2) + (T * H * 4 if wl.I_s else 0) +
@@ -376,11 +380,16 @@ def run_ours(args, rank, world, local):
     weights = moe.LayerWeights(wg=g["wg"], w13=g["w13"], w2=g["w2"], gamma=g["gamma"],
                                gate_bias=g["gate_bias"], w13_s=g["w13_s"], w2_s=g["w2_s"])
 
-    def desc_for(y_f32):
+    def desc_for(y_f32, gather_a=args.gather_a == "on"):
         return moe.make_desc(wl.T, wl.H, wl.E, wl.k, wl.I, wl.I_s, rmsnorm=wl.rmsnorm,
                              eps=wl.eps, renorm=wl.renorm, out_f32=False,
-                             gate_sequential=args.gate_sequential, y_f32=y_f32)
+                             gate_sequential=args.gate_sequential, y_f32=y_f32,
+                             gather_a=gather_a)
     desc = desc_for(args.y_f32)
+    # MOE_GATHER_A takes effect only on the wide kernel's shapes; where it does,
+    # the workspace holds source tokens instead of the permuted rows
+    gather = moe.layer_workspace_size(desc) < moe.layer_workspace_size(
+        desc_for(args.y_f32, gather_a=False))
     alt_desc = desc_for(not args.y_f32)
     ws = torch.empty(max(moe.layer_workspace_size(desc), moe.layer_workspace_size(alt_desc)),
                      dtype=torch.uint8, device=dev)
@@ -483,7 +492,7 @@ def run_ours(args, rank, world, local):
     # end to end on host buffers (pinned), through the same public call
     if args.no_e2e:
         return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, None, g,
-                           two_streams, active, res_extra)
+                           two_streams, active, res_extra, gather)
     # two host batches (this rank's tokens and a second draw) used in turn,
     # two host output buffers; every step copies its tokens in and its output
     # out, overlapped with the neighbouring steps' compute
@@ -509,11 +518,11 @@ def run_ours(args, rank, world, local):
     check("in the end-to-end steps")
     e2e_value = job_throughput(world, wl.T, Ke, e2e_ms)
     return finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g,
-                       two_streams, active, res_extra)
+                       two_streams, active, res_extra, gather)
 
 
 def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_value, g,
-                two_streams=False, active=None, res_extra=None):
+                two_streams=False, active=None, res_extra=None, gather=False):
     import moe_expert_routing_fp32_gb300 as moe  # noqa: F401
     res_extra = res_extra or {}
     step_ms = elapsed_ms / K
@@ -522,8 +531,9 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
     # the recorded DRAM bytes were captured on the named workload as-is, with
     # the shared expert inside the w13 launch and bf16 routed outputs
     from moe_inputs import WORKLOADS
-    traffic_applies = wl == WORKLOADS[args.workload] and not two_streams
-    work = stage_bytes_flops(wl, two_streams, wl.E if active is None else active, args.y_f32)
+    traffic_applies = wl == WORKLOADS[args.workload] and not two_streams and not gather
+    work = stage_bytes_flops(wl, two_streams, wl.E if active is None else active, args.y_f32,
+                             gather)
     dom = "gemm_w13_swiglu"
     dom_s = stage_ms[dom] / 1e3
     tc_peak, tc_how = tensor_peak(peaks, clk)
@@ -572,7 +582,7 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
         if ratio:
             roof["frac_nominal_at_sampled_clock"] = round(
                 w13_tf / (NOMINAL_BF16_TFLOPS * min(ratio, 1.0)), 4)
-    launches = launches_per_step(wl, args.gate_sequential, two_streams)
+    launches = launches_per_step(wl, args.gate_sequential, two_streams) - (1 if gather else 0)
     y_mode = "fp32 (MOE_Y_F32)" if args.y_f32 else "bf16"
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -582,6 +592,8 @@ def finish_ours(args, wl, world, rank, K, W, elapsed_ms, stage_ms, clk, e2e_valu
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
                    "I_shared": wl.I_s, "rmsnorm": wl.rmsnorm, "out": "bf16",
                    "routed_expert_outputs": y_mode,
+                   "w13_rows": ("gathered by source token inside the w13 matmul (MOE_GATHER_A)"
+                                if gather else "permuted into expanded_x first"),
                    "shared_expert": ("none" if not wl.I_s else
                                      "second stream" if two_streams else "same launches"),
                    "gate": ("fp32, sequential FMA order" if args.gate_sequential or wl.T <= 512

@@ -68,9 +68,19 @@ enum {
     MOE_SHARED_F32 = 1u << 4,  /* finalize: `shared` is fp32 (else bf16) */
     MOE_GATE_SEQUENTIAL = 1u << 5, /* layer: the sequential fp32 gate for every T
                                       (see moe_gate_tensor for the default) */
-    MOE_Y_F32 = 1u << 6            /* layer: keep the routed expert outputs y_exp in
+    MOE_Y_F32 = 1u << 6,           /* layer: keep the routed expert outputs y_exp in
                                       fp32, the down matmul's accumulator, instead of
                                       rounding them to bf16 (finalize: y_exp is fp32) */
+    MOE_GATHER_A = 1u << 7         /* layer: no permute pass; the routed w13 matmul
+                                      reads each expanded row from the (normalised)
+                                      input by its source token, and the workspace
+                                      holds no expanded_x.  Takes effect only where
+                                      that matmul runs as the 256 x 512 pair kernel
+                                      (>= 1024 rows per expert on average,
+                                      I % 256 == 0); ignored elsewhere.  Same results
+                                      bit for bit: the rows are copies either way.
+                                      Off by default: the in-kernel row copies make
+                                      the matmul slower than the permute pass costs. */
 };
 
 typedef struct {

@@ -34,6 +34,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_S
                 3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_NO_DEVICE"}
 DEV_BAD_EXPERT_ID, DEV_TIMEOUT, DEV_BAD_OFFSETS, DEV_UNSORTED = 1, 2, 4, 8
 RENORM, RMSNORM, SHARED, OUT_F32, SHARED_F32, GATE_SEQUENTIAL, Y_F32 = 1, 2, 4, 8, 16, 32, 64
+GATHER_A = 128
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_status_string", "moe_rmsnorm_gate", "moe_rmsnorm_sumsq",
@@ -323,14 +324,17 @@ def finalize_routing(y_exp, row_idx, topk_w, shared=None, out_f32=False):
 
 
 def make_desc(T, H, E, k, I, I_shared=0, rmsnorm=False, eps=1e-6, renorm=True,
-              out_f32=False, gate_sequential=False, y_f32=False) -> MoeDesc:
+              out_f32=False, gate_sequential=False, y_f32=False, gather_a=False) -> MoeDesc:
     """``gate_sequential``: the sequential fp32 gate (moe_rmsnorm_gate's
     logits, bit for bit) instead of the tensor-core gate for T > 512.
     ``y_f32``: the routed expert outputs enter the weighted sum as the down
-    matmul's fp32 accumulator instead of rounded to bf16 (MOE_Y_F32)."""
+    matmul's fp32 accumulator instead of rounded to bf16 (MOE_Y_F32).
+    ``gather_a``: the routed w13 matmul reads its rows by source token, with
+    no permute pass, where it runs as the wide pair kernel (MOE_GATHER_A)."""
     flags = (RENORM if renorm else 0) | (RMSNORM if rmsnorm else 0) | \
         (SHARED if I_shared > 0 else 0) | (OUT_F32 if out_f32 else 0) | \
-        (GATE_SEQUENTIAL if gate_sequential else 0) | (Y_F32 if y_f32 else 0)
+        (GATE_SEQUENTIAL if gate_sequential else 0) | (Y_F32 if y_f32 else 0) | \
+        (GATHER_A if gather_a else 0)
     return MoeDesc(T, H, E, k, I, I_shared, eps, flags)
 
 

@@ -83,6 +83,13 @@ struct Params {
     CUtensorMap tmA0h, tmA1h, tmB0h, tmB1h;
     // wide pair kernel: B of both segments as 256-row boxes
     CUtensorMap tmB0w, tmB1w;
+    // wide pair kernel with gathered A (SwiGLU): routed row r is row
+    // ga_rows0[r] of gA0 (clamped into its ga_n0 rows), segment-1 row r is
+    // row r of gA1; both row-major with K0 / K1 columns
+    const uint16_t *gA0;
+    const int32_t *ga_rows0;
+    int32_t ga_n0;
+    const uint16_t *gA1;
 };
 
 struct Tile {
@@ -1018,11 +1025,17 @@ constexpr int W_STAGE_BYTES = A_BYTES + W_B_BYTES;      // 48 KB per CTA
 constexpr int W_EPI_WARPS = 8;
 constexpr int W_THREADS = 64 + 32 * W_EPI_WARPS;
 constexpr int WQ_CONSUMERS = 2 + 2 * W_EPI_WARPS;       // MMA thread, odd producer, epilogue
+// With gathered A, four more warps per CTA copy each stage's A rows (16-byte
+// cp.async, straight into the 128-byte swizzle), and the odd CTA's warp 1
+// relays "A landed" to the even CTA's full barrier.
+constexpr int W_GATHER_WARPS = 4;
+constexpr int W_THREADS_G = W_THREADS + 32 * W_GATHER_WARPS;
+constexpr int WQ_CONSUMERS_G = WQ_CONSUMERS + 2 * W_GATHER_WARPS + 1;
 struct CfgW {
     static constexpr int EPI_OFF = WSTAGES * W_STAGE_BYTES;
     static constexpr int BAR_OFF = EPI_OFF + W_EPI_WARPS * W_BOXES * EPI_BYTES;
-    // full[S], empty[S], tfull, tempty[2], drain, q_full[QD], q_empty[QD]
-    static constexpr int NBARS = 2 * WSTAGES + 4 + 2 * QD;
+    // full[S], empty[S], tfull, tempty[2], drain, q_full[QD], q_empty[QD], a_full[S]
+    static constexpr int NBARS = 3 * WSTAGES + 4 + 2 * QD;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int QT_OFF = MISC_OFF + 16;
     static constexpr int OFFS_OFF = QT_OFF + QD * 4;
@@ -1032,9 +1045,10 @@ struct CfgW {
 static_assert(CfgW::SMEM <= 227 * 1024, "wide pair kernel: shared memory");
 
 
-template <int MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
+template <int MODE, bool GATHER>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? W_THREADS_G : W_THREADS, 1)
     grouped_gemm_wide_kernel(const __grid_constant__ Params p) {
+    constexpr int NT = GATHER ? W_THREADS_G : W_THREADS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1046,6 +1060,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
     uint64_t *drain = tempty + 2;
     uint64_t *q_full = drain + 1;               // [QD]
     uint64_t *q_empty = q_full + QD;            // [QD], used in the even CTA only
+    uint64_t *a_full = q_empty + QD;            // [WSTAGES]: this CTA's gathered A landed
     volatile int *q_tile = reinterpret_cast<volatile int *>(smem + CfgW::QT_OFF);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + CfgW::MISC_OFF);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + CfgW::MISC_OFF + 4);
@@ -1064,7 +1079,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
         *s_abort = 0;
         *s_bad = 0;
     }
-    for (int g = tid; g <= p.G; g += W_THREADS) s_off[g] = p.offsets[g];
+    for (int g = tid; g <= p.G; g += NT) s_off[g] = p.offsets[g];
     __syncthreads();
     if (warp == 0) {
         int run = 0;
@@ -1091,8 +1106,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
     }
     if (tid == 32) {
         for (int s = 0; s < WSTAGES; ++s) {
-            mbar_init(&full[s], 1);
+            // even CTA: its producer's arming arrival (+ the odd CTA's relay of
+            // its gathered A)
+            mbar_init(&full[s], GATHER ? 2 : 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&a_full[s], 32 * W_GATHER_WARPS);
         }
         mbar_init(tfull, 1);
         mbar_init(&tempty[0], 2 * W_EPI_WARPS);   // lane 0 of every epilogue warp of both CTAs
@@ -1100,7 +1118,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
         mbar_init(drain, 1);
         for (int q = 0; q < QD; ++q) {
             mbar_init(&q_full[q], 1);
-            mbar_init(&q_empty[q], WQ_CONSUMERS);
+            mbar_init(&q_empty[q], GATHER ? WQ_CONSUMERS_G : WQ_CONSUMERS);
         }
         fence_barrier_init();
     }
@@ -1141,10 +1159,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
     if (warp == 0) {
         // ================= TMA producer (both CTAs)
         if (lane == 0) {
-            tma_prefetch_desc(&p.tmA0);
+            if (!GATHER) tma_prefetch_desc(&p.tmA0);
             tma_prefetch_desc(&p.tmB0w);
             if (p.rows1 > 0) {
-                tma_prefetch_desc(&p.tmA1);
+                if (!GATHER) tma_prefetch_desc(&p.tmA1);
                 tma_prefetch_desc(&p.tmB1w);
             }
             int stage = 0;
@@ -1174,8 +1192,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
                 if (tile >= total) break;
                 const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0, 1);
                 const int arow = t.row0 + (t.half ? 64 : 128) * static_cast<int>(rank);
+                // bytes of both CTAs (with gathered A: B only)
                 const uint32_t stage_tx =
-                    t.half ? 2u * (A_BYTES / 2 + W_B_BYTES) : 2u * W_STAGE_BYTES;
+                    GATHER ? 2u * W_B_BYTES
+                           : (t.half ? 2u * (A_BYTES / 2 + W_B_BYTES) : 2u * W_STAGE_BYTES);
                 const int whalf = t.seg == 0 ? p.half0 : p.half1;
                 const CUtensorMap *mA = t.seg == 0 ? (t.half ? &p.tmA0h : &p.tmA0)
                                                    : (t.half ? &p.tmA1h : &p.tmA1);
@@ -1193,7 +1213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
                     if (leader) mbar_arrive_expect_tx(&full[stage], stage_tx);
                     const uint32_t fb = lead_full + 8u * static_cast<uint32_t>(stage);
                     const int k0 = kb * BK;
-                    tma_load_2d_pair(a_dst, mA, fb, k0, arow);
+                    if (!GATHER) tma_load_2d_pair(a_dst, mA, fb, k0, arow);
                     if (MODE == MODE_SWIGLU && t.half) {
                         // per half: 64 gate rows, then the matching 64 up rows
 #pragma unroll
@@ -1271,10 +1291,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
                 };
                 bool ok = true;
                 for (int kb = 0; kb < t.kblocks; ++kb) {
-                    if (!mbar_wait_bounded(&full[stage], phase, s_abort, p.dev_status)) {
+                    // with gathered A: the odd CTA's A arrives through full[] (its
+                    // relay), this CTA's through a_full[]
+                    const bool got_full =
+                        GATHER ? mbar_wait_bounded_cluster(&full[stage], phase, s_abort, p.dev_status)
+                               : mbar_wait_bounded(&full[stage], phase, s_abort, p.dev_status);
+                    if (!got_full ||
+                        (GATHER && !mbar_wait_bounded(&a_full[stage], phase, s_abort, p.dev_status))) {
                         ok = false;
                         break;
                     }
+                    // the gathered rows were written through the generic proxy;
+                    // the tensor core reads them through the async proxy
+                    if (GATHER) fence_proxy_async();
                     tc_fence_after();
                     mma_half(stage, kb, 0);
                     issued = true;
@@ -1323,9 +1352,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
                 tc_commit_pair_mc(drain, 0x1);
                 mbar_wait_drain(drain, 0);
             }
+        } else if (GATHER && lane == 0 && !leader) {
+            // ================= relay (odd CTA): each stage's gathered A rows of
+            // this CTA have landed -> arrive on the even CTA's full barrier
+            int stage = 0;
+            uint32_t phase = 0;
+            int qi = 0;
+            uint32_t qph = 0;
+            while (!*s_abort) {
+                int tile;
+                if (!next_tile(qi, qph, tile) || tile >= total) break;
+                const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0, 1);
+                bool ok = true;
+                for (int kb = 0; kb < t.kblocks; ++kb) {
+                    if (!mbar_wait_bounded(&a_full[stage], phase, s_abort, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async();
+                    mbar_arrive_cluster(lead_full + 8u * static_cast<uint32_t>(stage));
+                    if (++stage == WSTAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+            }
         }
         __syncwarp();
-    } else {
+    } else if (warp < W_THREADS / 32) {
         // ================= epilogue (warps 2..9 of both CTAs)
         const int q = warp & 3;            // TMEM lane quarter this warp may read
         const int sub = (warp - 2) >> 2;   // which half of the quarter's columns
@@ -1378,19 +1433,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
                     const uint32_t gbase = tq + 256u * static_cast<uint32_t>(h) + j0;
 #pragma unroll 1
                     for (int c = 0; c < ncol; c += 32) {
-                        float g[32], u[32];
-                        __syncwarp();
-                        tmem_ld32(gbase + c, g);
-                        tmem_ld32(gbase + uoff + c, u);
-                        tmem_ld_wait();
                         uint32_t pk[16];
+                        // 16 columns of g and u at a time (fewer live registers)
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float a0 =
-                                __fdividef(g[2 * i], 1.0f + __expf(-g[2 * i])) * u[2 * i];
-                            const float a1 = __fdividef(g[2 * i + 1], 1.0f + __expf(-g[2 * i + 1])) *
-                                             u[2 * i + 1];
-                            pk[i] = pack_bf16x2(a0, a1);
+                        for (int hc = 0; hc < 32; hc += 16) {
+                            float g[16], u[16];
+                            __syncwarp();
+                            tmem_ld16(gbase + c + hc, g);
+                            tmem_ld16(gbase + uoff + c + hc, u);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float a0 =
+                                    __fdividef(g[2 * i], 1.0f + __expf(-g[2 * i])) * u[2 * i];
+                                const float a1 =
+                                    __fdividef(g[2 * i + 1], 1.0f + __expf(-g[2 * i + 1])) *
+                                    u[2 * i + 1];
+                                pk[hc / 2 + i] = pack_bf16x2(a0, a1);
+                            }
                         }
                         if (boxed) {
                             emit_box(pk, omap, act0 + c, row_base);
@@ -1467,6 +1527,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
         }
         if (lane == 0) bulk_wait<0>();
         __syncwarp();
+    } else if (GATHER) {
+        // ================= A gather (warps 10..13 of both CTAs): this CTA's
+        // 128 (half tile: 64) A rows of each stage, 16-byte cp.async copies
+        // into the 128-byte swizzle (chunk j of row r at (j ^ (r & 7)) * 16),
+        // 8 threads per 128-byte row piece.  Each thread's copies of a stage
+        // arrive on a_full[stage] by themselves once they have landed, so the
+        // gather runs as far ahead as the free slots allow.
+        const int gt = tid - W_THREADS;     // 0..127
+        const int j = gt & 7;               // 16-byte chunk of the row piece
+        const int rsub = gt >> 3;           // rows rsub + 16 i
+        int stage = 0;
+        uint32_t phase = 0;
+        int qi = 0;
+        uint32_t qph = 0;
+        for (;;) {
+            int tile = 0, got = 1;
+            if (lane == 0) {
+                if (mbar_wait_bounded_cluster(&q_full[qi], qph, s_abort, p.dev_status)) {
+                    tile = q_tile[qi];
+                    mbar_arrive_cluster(lead_qempty + 8u * static_cast<uint32_t>(qi));
+                } else {
+                    got = 0;
+                }
+            }
+            got = __shfl_sync(0xffffffffu, got, 0);
+            tile = __shfl_sync(0xffffffffu, tile, 0);
+            if (++qi == QD) {
+                qi = 0;
+                qph ^= 1;
+            }
+            if (!got || tile >= total) break;
+            const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0, 1);
+            const int nrows = t.half ? 64 : 128;
+            const int arow = t.row0 + nrows * static_cast<int>(rank);
+            const bool seg0 = t.seg == 0;
+            const int K = seg0 ? p.K0 : p.K1;
+            // rows past the problem's end read its last row (their results are not stored)
+            const int nlim = seg0 ? p.rows0 : p.rows1;
+            const uint16_t *src[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = min(arow + rsub + 16 * i, nlim - 1);
+                int sr = r;
+                if (seg0) sr = min(max(__ldg(p.ga_rows0 + r), 0), p.ga_n0 - 1);
+                src[i] = (seg0 ? p.gA0 : p.gA1) + static_cast<size_t>(sr) * K + 8 * j;
+            }
+            bool ok = true;
+            for (int kb = 0; kb < t.kblocks; ++kb) {
+                int e_ok = 1;
+                if (lane == 0)
+                    e_ok = mbar_wait_bounded(&empty[stage], phase ^ 1, s_abort, p.dev_status);
+                if (!__shfl_sync(0xffffffffu, e_ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *a_dst = smem + stage * W_STAGE_BYTES;
+                const int k0 = kb * BK;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (16 * i >= nrows) break;
+                    const int r = rsub + 16 * i;
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(
+                                     a_dst + (r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4))),
+                                 "l"(reinterpret_cast<uint64_t>(src[i] + k0))
+                                 : "memory");
+                }
+                cp_async_mbar_arrive(&a_full[stage]);
+                if (++stage == WSTAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");   // none of this thread's copies in flight
     }
 
     tc_fence_before();
@@ -1699,8 +1834,9 @@ cudaError_t launch_pair(Params &p, int max_rows0, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <int MODE>
+template <int MODE, bool GATHER>
 cudaError_t launch_wide(Params &p, int max_rows0, cudaStream_t stream) {
+    constexpr int NT = GATHER ? W_THREADS_G : W_THREADS;
     static std::mutex mu;
     static bool attr_done[64] = {};
     static int max_clusters[64] = {};
@@ -1709,7 +1845,7 @@ cudaError_t launch_wide(Params &p, int max_rows0, cudaStream_t stream) {
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 64 && !attr_done[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(grouped_gemm_wide_kernel<MODE>,
+            cudaError_t e = cudaFuncSetAttribute(grouped_gemm_wide_kernel<MODE, GATHER>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  CfgW::SMEM);
             if (e != cudaSuccess) return e;
@@ -1718,11 +1854,11 @@ cudaError_t launch_wide(Params &p, int max_rows0, cudaStream_t stream) {
         if (dev < 64 && max_clusters[dev] == 0) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(static_cast<unsigned>(num_sms()), 1, 1);
-            cfg.blockDim = dim3(W_THREADS, 1, 1);
+            cfg.blockDim = dim3(NT, 1, 1);
             cfg.dynamicSmemBytes = CfgW::SMEM;
             cfg.stream = stream;
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_wide_kernel<MODE>, &cfg) !=
+            if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_wide_kernel<MODE, GATHER>, &cfg) !=
                     cudaSuccess ||
                 n <= 0) {
                 cudaGetLastError();
@@ -1739,7 +1875,7 @@ cudaError_t launch_wide(Params &p, int max_rows0, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(p.tile_counter, 0, sizeof(unsigned int), stream);
     if (e != cudaSuccess) return e;
-    grouped_gemm_wide_kernel<MODE><<<2 * clusters, W_THREADS, CfgW::SMEM, stream>>>(p);
+    grouped_gemm_wide_kernel<MODE, GATHER><<<2 * clusters, NT, CfgW::SMEM, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -1747,11 +1883,19 @@ cudaError_t launch_wide(Params &p, int max_rows0, cudaStream_t stream) {
 
 bool tensor_maps_available() { return encode_fn() != nullptr; }
 
+bool gemm_can_gather(int n, int G, int K, int N, const GemmSegment1 &seg1) {
+    return use_wide(true, N, K, seg1, n, G) && K % 8 == 0 && (seg1.rows == 0 || seg1.K1 % 8 == 0);
+}
+
 cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G, int n, int K,
                                const uint16_t *W13, int N, uint16_t *act,
                                const GemmSegment1 &seg1, int32_t *dev_status,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const uint16_t *gather_src,
+                               const int32_t *gather_rows, int gather_n) {
     if (G > MAX_GROUPS) return cudaErrorInvalidValue;
+    const bool gather = gather_src != nullptr;
+    if (gather && (!gather_rows || gather_n <= 0 || !gemm_can_gather(n, G, K, N, seg1)))
+        return cudaErrorInvalidValue;
     Params p{};
     // the pair kernel's stages hold 128 columns of K
     const bool pair = use_pair(n, G, seg1.rows) && K % 128 == 0 &&
@@ -1760,8 +1904,10 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
         const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
         const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(2 * N),
                                 static_cast<uint64_t>(G)};
-        if (!make_map(&p.tmA0, A, 2, a0, BM) || !make_map(&p.tmB0, W13, 3, b0, 128))
+        // gathered A: the rows are not a tensor; the B map stands in for the unused A map
+        if ((!gather && !make_map(&p.tmA0, A, 2, a0, BM)) || !make_map(&p.tmB0, W13, 3, b0, 128))
             return cudaErrorInvalidValue;
+        if (gather) p.tmA0 = p.tmB0;
         p.tmA1 = p.tmA0;
         p.tmB1 = p.tmB0;
     }
@@ -1777,6 +1923,10 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
     } else if (G == 0) {
         return cudaSuccess;
     }
+    p.gA0 = gather_src;
+    p.ga_rows0 = gather_rows;
+    p.ga_n0 = gather_n;
+    p.gA1 = seg1.A;
     p.offsets = offsets;
     p.G = G;
     p.rows0 = n;
@@ -1806,9 +1956,10 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
             const uint64_t a0[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(std::max(n, 1))};
             const uint64_t b0[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(2 * N),
                                     static_cast<uint64_t>(G)};
-            if (!make_map(&p.tmA0h, A, 2, a0, 64) || !make_map(&p.tmB0h, W13, 3, b0, 64) ||
-                !make_map(&p.tmB0w, W13, 3, b0, 256))
+            if ((!gather && !make_map(&p.tmA0h, A, 2, a0, 64)) ||
+                !make_map(&p.tmB0h, W13, 3, b0, 64) || !make_map(&p.tmB0w, W13, 3, b0, 256))
                 return cudaErrorInvalidValue;
+            if (gather) p.tmA0h = p.tmB0h;
         }
         if (seg1.rows > 0) {
             const uint64_t a1[2] = {static_cast<uint64_t>(seg1.K1), static_cast<uint64_t>(seg1.rows)};
@@ -1827,7 +1978,8 @@ cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G,
             p.tmB1h = p.tmB0h;
             p.tmB1w = p.tmB0w;
         }
-        return launch_wide<MODE_SWIGLU>(p, n, stream);
+        return gather ? launch_wide<MODE_SWIGLU, true>(p, n, stream)
+                      : launch_wide<MODE_SWIGLU, false>(p, n, stream);
     }
     if (pair) {
         if (!make_out_maps(p, N, seg1.N1)) return cudaErrorInvalidValue;
@@ -1936,7 +2088,7 @@ cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, 
         }
         p.tmB0h = p.tmB0w;
         p.tmB1h = p.tmB1w;
-        return launch_wide<MODE_STORE>(p, n, stream);
+        return launch_wide<MODE_STORE, false>(p, n, stream);
     }
     if (pair) {
         if (!make_out_maps(p, N, seg1.N1)) return cudaErrorInvalidValue;

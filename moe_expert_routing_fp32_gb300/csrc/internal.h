@@ -97,10 +97,15 @@ struct GemmSegment1 {       // an optional dense problem appended to the grouped
 
 // G may be 0 (segment 1 only; `offsets` must still point at one readable int).
 // act[r, :] = bf16(SiLU(A W13g^T) * (A W13u^T)) per group; A [n, K], W13 [G, 2N, K]
+// With gather_src, A is not read: routed row r is row gather_rows[r] of
+// gather_src ([gather_n, K]), copied in by the kernel itself (only where
+// gemm_can_gather holds: the wide pair kernel's shapes).
 cudaError_t launch_gemm_swiglu(const uint16_t *A, const int32_t *offsets, int G, int n, int K,
                                const uint16_t *W13, int N, uint16_t *act,
                                const GemmSegment1 &seg1, int32_t *dev_status,
-                               cudaStream_t stream);
+                               cudaStream_t stream, const uint16_t *gather_src = nullptr,
+                               const int32_t *gather_rows = nullptr, int gather_n = 0);
+bool gemm_can_gather(int n, int G, int K, int N, const GemmSegment1 &seg1);
 // y[r, :] = bf16(A W^T) per group (fp32, unrounded, with y_f32); A [n, K], W [G, N, K]
 cudaError_t launch_gemm_store(const uint16_t *A, const int32_t *offsets, int G, int n, int K,
                               const uint16_t *W, int N, void *y, const GemmSegment1 &seg1,

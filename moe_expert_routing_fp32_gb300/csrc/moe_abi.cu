@@ -50,8 +50,8 @@ inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255);
 // Layout of the layer workspace (offsets in bytes, each 256-aligned).
 struct LayerWs {
     size_t xn = 0, logits = 0, wsplit = 0, parts = 0, idx = 0, w = 0, hist = 0, counts = 0,
-           offsets = 0, row_idx = 0, expanded_x = 0, act = 0, y = 0, act_s = 0, y_s = 0,
-           total = 0;
+           offsets = 0, row_idx = 0, src_token = 0, expanded_x = 0, act = 0, y = 0, act_s = 0,
+           y_s = 0, total = 0;
 };
 
 // The layer's gate runs on the tensor cores for batches above the small
@@ -94,6 +94,19 @@ cudaError_t launch_gate_tc(const uint16_t *xs, const float *wg, const float *gat
                                hist, s);
 }
 
+// MOE_GATHER_A takes effect where the routed w13 matmul runs as the wide pair
+// kernel (a shape decision, the same for every call with this descriptor).
+bool layer_gathers(const moe_desc_t &d) {
+    if (!(d.flags & MOE_GATHER_A)) return false;
+    GemmSegment1 sh;
+    if (d.flags & MOE_SHARED) {
+        sh.rows = d.T;
+        sh.K1 = d.H;
+        sh.N1 = d.I_shared;
+    }
+    return gemm_can_gather(d.T * d.k, d.E, d.H, d.I, sh);
+}
+
 LayerWs layer_layout(const moe_desc_t &d) {
     LayerWs L;
     const size_t T = d.T, H = d.H, E = d.E, k = d.k, I = d.I, Is = d.I_shared;
@@ -117,7 +130,10 @@ LayerWs layer_layout(const moe_desc_t &d) {
     L.counts = take(E * 4);
     L.offsets = take((E + 1) * 4);
     L.row_idx = take(N * 4);
-    L.expanded_x = take(N * H * 2);
+    if (layer_gathers(d))
+        L.src_token = take(N * 4);      // the w13 matmul reads x's rows through it
+    else
+        L.expanded_x = take(N * H * 2);
     L.act = take(N * I * 2);
     L.y = take(N * H * ((d.flags & MOE_Y_F32) ? 4 : 2));
     if (d.flags & MOE_SHARED) {
@@ -401,7 +417,9 @@ moe_status_t layer_forward_impl(const moe_desc_t *desc, const moe_bf16_t *x,
     int32_t *counts = static_cast<int32_t *>(at(L.counts));
     int32_t *offsets = static_cast<int32_t *>(at(L.offsets));
     int32_t *row_idx = static_cast<int32_t *>(at(L.row_idx));
-    uint16_t *ex = static_cast<uint16_t *>(at(L.expanded_x));
+    const bool gather = layer_gathers(d);
+    uint16_t *ex = gather ? nullptr : static_cast<uint16_t *>(at(L.expanded_x));
+    int32_t *src_token = gather ? static_cast<int32_t *>(at(L.src_token)) : nullptr;
     uint16_t *act = static_cast<uint16_t *>(at(L.act));
     void *y = at(L.y);   // bf16, or fp32 with MOE_Y_F32
     const bool y_f32 = (d.flags & MOE_Y_F32) != 0;
@@ -460,9 +478,10 @@ moe_status_t layer_forward_impl(const moe_desc_t *desc, const moe_bf16_t *x,
     MOE_TRY(mark(1));
     MOE_TRY(launch_route_scan(hist, B, E, counts, offsets, scan_hist ? idx : nullptr, T, k,
                               dev_status, s));
-    MOE_TRY(launch_route_scatter(idx, hist, T, k, E, row_idx, nullptr, nullptr, dev_status, s));
+    MOE_TRY(launch_route_scatter(idx, hist, T, k, E, row_idx, src_token, nullptr, dev_status, s));
     MOE_TRY(mark(2));
-    const bool two_streams = shared && shared_stream != nullptr;
+    // with the rows gathered inside the w13 matmul there is no copy to overlap
+    const bool two_streams = shared && shared_stream != nullptr && !gather;
     GemmSegment1 sh13;       // the shared expert's w13 + SwiGLU as a dense segment
     if (shared) {
         sh13.A = xs;
@@ -489,6 +508,11 @@ moe_status_t layer_forward_impl(const moe_desc_t *desc, const moe_bf16_t *x,
         MOE_TRY(cudaStreamWaitEvent(s, join, 0));
         const GemmSegment1 none{};
         MOE_TRY(launch_gemm_swiglu(ex, offsets, E, N, H, w13, I, act, none, dev_status, s));
+    } else if (gather) {
+        // 3. grouped w13 + SwiGLU, its A rows read from xs by source token
+        MOE_TRY(mark(3));
+        MOE_TRY(launch_gemm_swiglu(nullptr, offsets, E, N, H, w13, I, act, sh13, dev_status, s,
+                                   xs, src_token, T));
     } else {
         MOE_TRY(launch_permute(xs, row_idx, T, H, k, ex, s));
         // 3. grouped w13 + SwiGLU (the shared expert rides along as a dense segment)

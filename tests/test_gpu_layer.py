@@ -45,15 +45,16 @@ def _weights(g):
                             gate_bias=g["gate_bias"], w13_s=g["w13_s"], w2_s=g["w2_s"])
 
 
-def _desc(wl, T=None, out_f32=True, seq=False, y_f32=False):
+def _desc(wl, T=None, out_f32=True, seq=False, y_f32=False, gather_a=False):
     return moe.make_desc(wl.T if T is None else T, wl.H, wl.E, wl.k, wl.I, wl.I_s,
                          rmsnorm=wl.rmsnorm, eps=wl.eps, renorm=wl.renorm, out_f32=out_f32,
-                         gate_sequential=seq, y_f32=y_f32)
+                         gate_sequential=seq, y_f32=y_f32, gather_a=gather_a)
 
 
-def _run_layer(wl, g, out_f32, T=None, seq=False, y_f32=False):
+def _run_layer(wl, g, out_f32, T=None, seq=False, y_f32=False, gather_a=False):
     st = moe.new_status(DEV)
-    out = moe.layer_forward(_desc(wl, T, out_f32, seq, y_f32), g["x"], _weights(g), status=st)
+    out = moe.layer_forward(_desc(wl, T, out_f32, seq, y_f32, gather_a), g["x"], _weights(g),
+                            status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0, f"device status {int(st.item())}"
     return out
@@ -132,6 +133,10 @@ def test_layer_small_all_tokens(wl, out_f32):
         # fp32 routed outputs: the strict bar, no allowance
         out = _run_layer(wl, g, out_f32, seq=seq, y_f32=True)
         check_out(t2f64(out)[sel], ref_yf[sel], bf16_out=not out_f32, what=what + " y_f32")
+        # rows gathered inside the w13 matmul (where it runs as the wide pair
+        # kernel; elsewhere the flag is ignored): the same bytes
+        gat = _run_layer(wl, g, out_f32, seq=seq, y_f32=True, gather_a=True)
+        assert torch.equal(gat, out), what + " gather_a"
 
 
 def test_layer_deterministic_and_workspace_reuse():
@@ -226,10 +231,14 @@ def test_layer_full_size(name, seed):
             got = t2f64(_run_layer(wl, g, out_f32, seq=seq)[tok_dev])
             check_out(got[sel], ref[sel], bf16_out=not out_f32, what=what,
                       flip_allowance=allow[sel])
-            got = t2f64(_run_layer(wl, g, out_f32, seq=seq, y_f32=True)[tok_dev])
+            full = _run_layer(wl, g, out_f32, seq=seq, y_f32=True)
+            got = t2f64(full[tok_dev])
             mx, rel = check_out(got[sel], ref_yf[sel], bf16_out=not out_f32,
                                 what=what + " y_f32")
             print(f"{what} y_f32: {int(sel.sum())} tokens, max-abs {mx:.3e}, rel-L2 {rel:.3e}")
+            # rows gathered inside the w13 matmul: every token, the same bytes
+            gat = _run_layer(wl, g, out_f32, seq=seq, y_f32=True, gather_a=True)
+            assert torch.equal(gat, full), what + " gather_a"
 
 
 def test_shared_expert_on_second_stream_matches():
