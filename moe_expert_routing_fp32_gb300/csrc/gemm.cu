@@ -1028,14 +1028,20 @@ constexpr int WQ_CONSUMERS = 2 + 2 * W_EPI_WARPS;       // MMA thread, odd produ
 // With gathered A, four more warps per CTA copy each stage's A rows (16-byte
 // cp.async, straight into the 128-byte swizzle), and the odd CTA's warp 1
 // relays "A landed" to the even CTA's full barrier.
+// The last W_TAIL k-blocks of a tile issue their half-1 MMAs after all
+// half-0 ones: half 0 is reported complete that much earlier and the
+// epilogue drains it while they run.  Measured on T=16384, H=4096, I=3072:
+// both matmuls ~1% faster with 3 than with none; with 4 (the whole ring
+// held back) the gain is gone.
+constexpr int W_TAIL = 3;
 constexpr int W_GATHER_WARPS = 4;
 constexpr int W_THREADS_G = W_THREADS + 32 * W_GATHER_WARPS;
 constexpr int WQ_CONSUMERS_G = WQ_CONSUMERS + 2 * W_GATHER_WARPS + 1;
 struct CfgW {
     static constexpr int EPI_OFF = WSTAGES * W_STAGE_BYTES;
     static constexpr int BAR_OFF = EPI_OFF + W_EPI_WARPS * W_BOXES * EPI_BYTES;
-    // full[S], empty[S], tfull, tempty[2], drain, q_full[QD], q_empty[QD], a_full[S]
-    static constexpr int NBARS = 3 * WSTAGES + 4 + 2 * QD;
+    // full[S], empty[S], tfull[2], tempty[2], drain, q_full[QD], q_empty[QD], a_full[S]
+    static constexpr int NBARS = 3 * WSTAGES + 5 + 2 * QD;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int QT_OFF = MISC_OFF + 16;
     static constexpr int OFFS_OFF = QT_OFF + QD * 4;
@@ -1055,8 +1061,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? W_THREADS_G
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + CfgW::BAR_OFF);
     uint64_t *full = bars;                      // used in the even CTA only
     uint64_t *empty = bars + WSTAGES;
-    uint64_t *tfull = bars + 2 * WSTAGES;
-    uint64_t *tempty = tfull + 1;               // [2], used in the even CTA only
+    uint64_t *tfull = bars + 2 * WSTAGES;       // [2]: accumulator half h complete
+    uint64_t *tempty = tfull + 2;               // [2], used in the even CTA only
     uint64_t *drain = tempty + 2;
     uint64_t *q_full = drain + 1;               // [QD]
     uint64_t *q_empty = q_full + QD;            // [QD], used in the even CTA only
@@ -1112,7 +1118,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? W_THREADS_G
             mbar_init(&empty[s], 1);
             mbar_init(&a_full[s], 32 * W_GATHER_WARPS);
         }
-        mbar_init(tfull, 1);
+        mbar_init(&tfull[0], 1);
+        mbar_init(&tfull[1], 1);
         mbar_init(&tempty[0], 2 * W_EPI_WARPS);   // lane 0 of every epilogue warp of both CTAs
         mbar_init(&tempty[1], 2 * W_EPI_WARPS);
         mbar_init(drain, 1);
@@ -1280,6 +1287,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? W_THREADS_G
                 if (!mbar_wait_bounded_cluster(&tempty[0], tph ^ 1, s_abort, p.dev_status)) break;
                 tc_fence_after();
                 bool h1 = false;
+                const int tail_from = t.kblocks - min(W_TAIL, t.kblocks);
                 int pend_st[WSTAGES];
                 int npend = 0, pend_kb0 = 0;
                 auto flush = [&]() {
@@ -1307,11 +1315,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? W_THREADS_G
                     tc_fence_after();
                     mma_half(stage, kb, 0);
                     issued = true;
-                    if (!h1 && mbar_test_wait_cluster(&tempty[1], tph ^ 1)) {
+                    // the tile's last k-blocks keep their half-1 MMAs back
+                    const bool tail = kb >= tail_from;
+                    if (!tail && !h1 && mbar_test_wait_cluster(&tempty[1], tph ^ 1)) {
                         tc_fence_after();
                         h1 = true;
                     }
-                    if (h1) {
+                    if (h1 && !tail) {
                         flush();
                         mma_half(stage, kb, 1);
                         tc_commit_pair_mc(&empty[stage], 0x3);
@@ -1320,13 +1330,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? W_THREADS_G
                         pend_st[npend++] = stage;
                         if (npend == WSTAGES) {
                             // every stage waits for half 1: the producer cannot go on
-                            if (!mbar_wait_bounded_cluster(&tempty[1], tph ^ 1, s_abort,
-                                                           p.dev_status)) {
-                                ok = false;
-                                break;
+                            if (!h1) {
+                                if (!mbar_wait_bounded_cluster(&tempty[1], tph ^ 1, s_abort,
+                                                               p.dev_status)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                h1 = true;
                             }
-                            tc_fence_after();
-                            h1 = true;
                             flush();
                         }
                     }
@@ -1335,17 +1347,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? W_THREADS_G
                         phase ^= 1;
                     }
                 }
-                if (ok && npend > 0) {
-                    // a tile of fewer k-blocks than stages
-                    if (!mbar_wait_bounded_cluster(&tempty[1], tph ^ 1, s_abort, p.dev_status)) {
-                        ok = false;
-                    } else {
-                        tc_fence_after();
-                        flush();
-                    }
-                }
                 if (!ok) break;
-                tc_commit_pair_mc(tfull, 0x3);
+                // half 0 is complete once every MMA issued so far is: the
+                // epilogue drains it while the held-back half-1 MMAs run
+                tc_commit_pair_mc(&tfull[0], 0x3);
+                if (npend > 0) {
+                    if (!h1) {
+                        if (!mbar_wait_bounded_cluster(&tempty[1], tph ^ 1, s_abort,
+                                                       p.dev_status))
+                            break;
+                        tc_fence_after();
+                        h1 = true;
+                    }
+                    flush();
+                }
+                tc_commit_pair_mc(&tfull[1], 0x3);
                 tph ^= 1;
             }
             if (*s_abort && issued) {
@@ -1410,8 +1426,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? W_THREADS_G
             }
             if (!got || tile >= total) break;
             const Tile t = decode_tile_pair(p, tile, s_off, s_prefix, total0, 1);
-            if (!mbar_wait_bounded(tfull, tph, s_abort, p.dev_status)) break;
-            tc_fence_after();
             const int hq = q >> 1;
             const int row = t.half ? t.row0 + 64 * static_cast<int>(rank) + 32 * (q & 1) + lane
                                    : t.row0 + 128 * static_cast<int>(rank) + 32 * q + lane;
@@ -1420,7 +1434,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? W_THREADS_G
             const bool boxed = row_base + 32 <= t.row_end;
             const CUtensorMap *omap = t.seg == 0 ? &p.tmO0 : &p.tmO1;
             const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+            bool stop = false;
             for (int h = 0; h < 2; ++h) {
+                if (!mbar_wait_bounded(&tfull[h], tph, s_abort, p.dev_status)) {
+                    stop = true;
+                    break;
+                }
+                tc_fence_after();
                 if (MODE == MODE_SWIGLU) {
                     uint16_t *out = static_cast<uint16_t *>(t.seg == 0 ? p.out0 : p.out1);
                     const int64_t ldo = t.seg == 0 ? p.ldo0 : p.ldo1;
@@ -1523,6 +1543,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? W_THREADS_G
                 tc_fence_before();
                 if (lane == 0) mbar_arrive_cluster(lead_tempty + 8u * static_cast<uint32_t>(h));
             }
+            if (stop) break;
             tph ^= 1;
         }
         if (lane == 0) bulk_wait<0>();
