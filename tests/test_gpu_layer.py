@@ -113,6 +113,10 @@ SMALL = [
     # shapes the wide pair kernel takes (I, I_s % 256 == 0, H % 512 == 0)
     Workload("mid-wide", T=900, H=512, E=8, k=2, I=256, I_s=256, rmsnorm=True,
              gamma_std=0.1, x_std=1.0),
+    # 1100 rows per expert and in the shared segment: the wide pair kernel by
+    # default, each group ending in a 76-row block
+    Workload("mid-wide-tails", T=1100, H=512, E=2, k=2, I=256, I_s=256, rmsnorm=True,
+             gamma_std=0.1, x_std=1.0),
 ]
 
 

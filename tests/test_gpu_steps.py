@@ -242,7 +242,10 @@ def _grouped_case(counts, H, I, seed):
     # one-row, half-tile (<= 128 rows) and multi-block groups
     ([0, 1, 129, 0, 255, 37, 0, 512, 300], 512, 256),
     ([1000, 600, 64, 257], 1024, 512),
-], ids=["dense", "ragged", "h128", "mixed", "wide-ragged", "wide-big"])
+    # >= 1024 rows per group on average (the wide pair kernel by default):
+    # last blocks of 1, 128, 129 and 76 rows, and none
+    ([1025, 1280, 1408, 1409, 1100], 512, 256),
+], ids=["dense", "ragged", "h128", "mixed", "wide-ragged", "wide-big", "wide-tails"])
 def test_grouped_mlp(counts, H, I):
     x, w13, w2, off = _grouped_case(counts, H, I, len(counts) * 31 + H)
     st = moe.new_status(DEV)
