@@ -147,23 +147,26 @@ __device__ __forceinline__ float slot_weight(const float (&v)[NV], int k, bool r
 // rounded once to fp32 (nearest, ties to even), a value that does not depend
 // on a summation order, so one warp sums a row in parallel.
 //
-// Fast path (finite rows whose largest |x| lies in [2^-20, 2^40] and whose
-// smallest nonzero |x| is at least 2^-60; then every square is exact in
-// fp32).  With ex the exponent of the largest |x|, every square is below
-// 2^(2ex+2).  Each square v is split exactly into
+// Fast path (finite rows whose largest |x| lies in [2^-20, 2^40]), on packed
+// fp32 pairs (one instruction for two values).  With ex the exponent of the
+// largest |x|, every square is below 2^(2ex+2).  Each square v is split
+// exactly into
 //   q1 = v truncated to a multiple of u1 = 2^(2ex-14) (s1 + v rounded toward
 //        zero, minus s1, with s1 = 2^(2ex+9)),
 //   q2 = the rest truncated to a multiple of u2 = 2^(2ex-30) (s2 = 2^(2ex-7)),
 //   r2 = the rest, 0 <= r2 < u2.
-// The q1 of at most 128 squares (16 vectors of a lane) add up exactly in fp32
-// (multiples of u1 below 2^24 u1), likewise the q2; those group sums become
-// exact integers (units u1, u2) summed across lanes in 64 bits, giving
-// T = sum(q1 + q2) / u2 exactly.  The r2 are summed in fp32 (A, in units of
-// u2 after scaling) with a relative error below (n + 8) 2^-23 for n squares
-// per lane, so the exact sum is T + R, R in [A (1 - d), A (1 + d)] (R = 0
-// exactly when A = 0).  Rounded to 24 bits, both ends of that interval giving
-// the same fp32 value decides the result; otherwise (the interval holds a
-// rounding tie) the slow path decides.
+// The q1 of at most 64 squares (one half of the pairs of 16 vectors of a
+// lane) add up exactly in fp32 (multiples of u1 below 2^24 u1), likewise the
+// q2; those group sums become exact integers (units u1, u2) summed across
+// lanes in 64 bits, giving T = sum(q1 + q2) / u2 exactly.  The r2 are summed
+// in fp32 (A, in units of u2 after scaling) with a relative error below
+// (n + 8) 2^-23 for n squares per lane.  A nonzero |x| below 2^-63 has an
+// inexact fp32 square (at most 2^-149 off, or zero), which widens the
+// interval by H 2^-149: the exact sum is T + R with R in
+// [A (1 - d), A (1 + d) + H 2^-149 / u2].  Rounded to 24 bits, both ends of
+// that interval giving the same fp32 value decides the result; otherwise (the
+// interval holds a rounding tie, or the sum sits exactly on one with no
+// residual) the slow path decides.
 // Slow path: every square m^2 * 2^(2E-268) (m the 8-bit significand, E the
 // biased exponent, at least 1) is added exactly into a fixed-point number of
 // 20 32-bit limbs per lane (unit 2^-266), the lanes' numbers are added
@@ -175,11 +178,6 @@ constexpr int SQ_LIMBS = 20;
 __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
-    return v;
-}
-__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, off));
     return v;
 }
 __device__ __forceinline__ long long warp_sum_ll(long long v) {
@@ -253,18 +251,6 @@ __device__ __noinline__ float sumsq_row_exact(const uint4 *row, int nvec) {
     return __shfl_sync(0xffffffffu, res, 0);
 }
 
-// x^2 split into its q1 + q2 and the rest, accumulated (see above)
-__device__ __forceinline__ void sumsq_split(float x, float s1, float s2, float &a1, float &a2,
-                                            float &a3) {
-    const float v = __fmul_rn(x, x);
-    const float q1 = __fsub_rn(__fadd_rz(s1, v), s1);
-    a1 = __fadd_rn(a1, q1);
-    const float r1 = __fsub_rn(v, q1);
-    const float q2 = __fsub_rn(__fadd_rz(s2, r1), s2);
-    a2 = __fadd_rn(a2, q2);
-    a3 = __fadd_rn(a3, __fsub_rn(r1, q2));
-}
-
 // n + f (an integer n >= 2^30 and a real f >= 0, in units u2) rounded to 24
 // significant bits, nearest-even: the rounded value, an integer of at most 24
 // significant bits.  (n >= 2^30: the largest square alone is at least 2^30 u2.)
@@ -282,29 +268,8 @@ __device__ __forceinline__ long long round24(long long n0, double f) {
     return (q + (up ? 1 : 0)) << L;
 }
 
-// Largest and smallest nonzero |x| of 8 bf16 values, as fp32 bit patterns
-// (for non-negative floats the integer order is the value order).
-__device__ __forceinline__ void sumsq_extent(const uint4 &q, uint32_t &amax, uint32_t &amin) {
-    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = (wd[j] << 16) & 0x7FFF0000u, hi = wd[j] & 0x7FFF0000u;
-        amax = max(amax, max(lo, hi));
-        amin = min(amin, min(lo ? lo : 0x7F800000u, hi ? hi : 0x7F800000u));
-    }
-}
-__device__ __forceinline__ void sumsq_split8(const uint4 &q, float s1, float s2, float &a1,
-                                             float &a2, float &a3) {
-    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        sumsq_split(__uint_as_float(wd[j] << 16), s1, s2, a1, a2, a3);
-        sumsq_split(__uint_as_float(wd[j] & 0xFFFF0000u), s1, s2, a1, a2, a3);
-    }
-}
-
-// Packed fp32 pairs (the two halves of a 64-bit register) for the RMSNorm
-// pass: one instruction works on both values.
+// Packed fp32 pairs (the two halves of a 64-bit register): one instruction
+// works on both values.
 __device__ __forceinline__ uint64_t f2_add_rz(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("add.rz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -353,13 +318,19 @@ __device__ __forceinline__ SumsqScales sumsq_scales(int ex) {
     return SumsqScales{pow2f(2 * ex + 9), pow2f(2 * ex - 7), pow2f(14 - 2 * ex), pow2f(30 - 2 * ex)};
 }
 
-// Pass 1 across the warp: 0 = the fast path applies (ex set), else the
-// result to return now: +0 for an all-zero row, inf/NaN for a non-finite
-// one, or a request for the slow path (flagged in *slow).
-__device__ __forceinline__ bool sumsq_plan(uint32_t amax, uint32_t amin, int *ex, float *early,
-                                           bool *slow) {
-    amax = warp_max_u32(amax);
-    amin = warp_min_u32(amin);
+// Pass 1 over a vector: the packed maximum of its 16-bit magnitudes.
+__device__ __forceinline__ uint32_t sumsq_vmax(uint32_t mx, const uint4 &q) {
+    mx = max_u16x2(mx, q.x & 0x7FFF7FFFu);
+    mx = max_u16x2(mx, q.y & 0x7FFF7FFFu);
+    mx = max_u16x2(mx, q.z & 0x7FFF7FFFu);
+    return max_u16x2(mx, q.w & 0x7FFF7FFFu);
+}
+
+// Pass 1 across the warp: true = the fast path applies (ex set), else *early
+// is the result to return now (+0 for an all-zero row, inf/NaN for a
+// non-finite one) or *slow asks for the slow path.
+__device__ __forceinline__ bool sumsq_plan(uint32_t mx, int *ex, float *early, bool *slow) {
+    const uint32_t amax = warp_max_u32(max(mx & 0xFFFFu, mx >> 16) << 16);
     *slow = false;
     if (amax == 0u) {
         *early = 0.0f;
@@ -370,33 +341,52 @@ __device__ __forceinline__ bool sumsq_plan(uint32_t amax, uint32_t amin, int *ex
         return false;
     }
     *ex = static_cast<int>(amax >> 23) - 127;
-    if (*ex < -20 || *ex > 40 || amin < (67u << 23)) {   // 67 << 23 = 2^-60
+    if (*ex < -20 || *ex > 40) {
         *slow = true;
         return false;
     }
     return true;
 }
 
-// Lanes' exact integer sums and fp32 residual sums -> the rounded result, or
-// the slow path when the residual's error interval holds a rounding tie.
-// nsq: squares per lane at most.
-__device__ __forceinline__ float sumsq_finish(long long n1, long long n2, float a3, int ex,
-                                              int nsq, const SumsqScales &sc, const uint4 *row,
+// Pass 2 over one word (two bf16 values): the squares split into q1, q2 and
+// the rest, accumulated into a1, a2 and a3.
+__device__ __forceinline__ void sumsq_word(uint32_t w, uint64_t s1, uint64_t s2, uint64_t &a1,
+                                           uint64_t &a2, uint64_t &a3) {
+    const uint64_t x2 = f2_from_bf16x2(w);
+    const uint64_t sq = f2_mul(x2, x2);
+    const uint64_t q1 = f2_sub(f2_add_rz(s1, sq), s1);
+    a1 = f2_add(a1, q1);
+    const uint64_t r1 = f2_sub(sq, q1);
+    const uint64_t q2 = f2_sub(f2_add_rz(s2, r1), s2);
+    a2 = f2_add(a2, q2);
+    a3 = f2_add(a3, f2_sub(r1, q2));
+}
+
+// A group's exact q1 and q2 sums (both halves) as integers in units u1, u2.
+__device__ __forceinline__ void sumsq_group_end(uint64_t a1, uint64_t a2, const SumsqScales &sc,
+                                                long long &n1, long long &n2) {
+    n1 += __float2ll_rn(__fmul_rn(f2_lo(a1), sc.k1)) + __float2ll_rn(__fmul_rn(f2_hi(a1), sc.k1));
+    n2 += __float2ll_rn(__fmul_rn(f2_lo(a2), sc.k2)) + __float2ll_rn(__fmul_rn(f2_hi(a2), sc.k2));
+}
+
+// The lanes' integer sums and residual sums -> the rounded result, or the
+// slow path when the error interval holds a rounding tie.  vpl: vectors per
+// lane at most.
+__device__ __forceinline__ float sumsq_finish(long long n1, long long n2, uint64_t a3, int ex,
+                                              int vpl, const SumsqScales &sc, const uint4 *row,
                                               int nvec) {
     n1 = warp_sum_ll(n1);
     n2 = warp_sum_ll(n2);
+    float r = __fadd_rn(f2_lo(a3), f2_hi(a3));
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) a3 = __fadd_rn(a3, __shfl_xor_sync(0xffffffffu, a3, off));
+    for (int off = 16; off > 0; off >>= 1) r = __fadd_rn(r, __shfl_xor_sync(0xffffffffu, r, off));
     const long long T = (n1 << 16) + n2;          // units u2 = 2^(2ex - 30)
-    long long res;
-    if (a3 == 0.0f) {
-        res = round24(T, 0.0);
-    } else {
-        const double A = static_cast<double>(a3) * static_cast<double>(sc.k2);
-        const double d = (nsq + 8.0) * 0x1p-23;
-        res = round24(T, A * (1.0 - d));
-        if (round24(T, A * (1.0 + d)) != res) return sumsq_row_exact(row, nvec);
-    }
+    const double A = static_cast<double>(r) * static_cast<double>(sc.k2);
+    const double d = (8.0 * vpl + 8.0) * 0x1p-23;
+    // squares of values below 2^-63: at most 2^-149 each from exact, in units of u2
+    const double tiny = 8.0 * 32 * vpl * ldexp(1.0, -119 - 2 * ex);
+    const long long res = round24(T, A * (1.0 - d));
+    if (round24(T, A * (1.0 + d) + tiny) != res) return sumsq_row_exact(row, nvec);
     // res has at most 24 significant bits: exact in fp32, and so is the
     // power-of-two scaling (the result is normal)
     return __fmul_rn(__ll2float_rn(res), pow2f(2 * ex - 30));
@@ -407,49 +397,15 @@ __device__ __forceinline__ float sumsq_finish(long long n1, long long n2, float 
 // caller passes zeros past the row's nvec vectors).  `row` is the row in
 // memory, for the slow path.
 template <int VPL>
-__device__ __forceinline__ float warp_sumsq_rn(const uint4 (&vec)[VPL], const uint4 *row, int nvec) {
-    uint32_t amax = 0u, amin = 0x7F800000u;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) sumsq_extent(vec[i], amax, amin);
-    int ex = 0;
-    float early = 0.0f;
-    bool slow;
-    if (!sumsq_plan(amax, amin, &ex, &early, &slow)) return slow ? sumsq_row_exact(row, nvec) : early;
-    const SumsqScales sc = sumsq_scales(ex);
-    long long n1 = 0, n2 = 0;
-    float a3 = 0.0f;
-#pragma unroll
-    for (int g = 0; g < VPL; g += 16) {
-        float a1 = 0.0f, a2 = 0.0f;       // at most 128 squares: exact
-#pragma unroll
-        for (int i = g; i < g + 16 && i < VPL; ++i) sumsq_split8(vec[i], sc.s1, sc.s2, a1, a2, a3);
-        n1 += __float2ll_rn(__fmul_rn(a1, sc.k1));
-        n2 += __float2ll_rn(__fmul_rn(a2, sc.k2));
-    }
-    return sumsq_finish(n1, n2, a3, ex, 8 * VPL, sc, row, nvec);
-}
-
-// The register variant on packed fp32 pairs, for the RMSNorm pass.  Only the
-// largest magnitude is taken in the first pass (packed 16-bit maxima): a
-// nonzero |x| below 2^-63 would give an inexact fp32 square (at most 2^-149
-// off, or zero), so the residual interval is widened by H * 2^-149 and an
-// exact tie with no residual at all goes to the slow path.
-template <int VPL>
 __device__ __forceinline__ float warp_sumsq_rn_packed(const uint4 (&vec)[VPL], const uint4 *row,
                                                       int nvec) {
     uint32_t mx = 0u;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        mx = max_u16x2(mx, vec[i].x & 0x7FFF7FFFu);
-        mx = max_u16x2(mx, vec[i].y & 0x7FFF7FFFu);
-        mx = max_u16x2(mx, vec[i].z & 0x7FFF7FFFu);
-        mx = max_u16x2(mx, vec[i].w & 0x7FFF7FFFu);
-    }
-    const uint32_t amax = warp_max_u32(max(mx & 0xFFFFu, mx >> 16) << 16);
-    if (amax == 0u) return 0.0f;
-    if (amax >= 0x7F800000u) return __uint_as_float(amax);   // inf, or NaN
-    const int ex = static_cast<int>(amax >> 23) - 127;
-    if (ex < -20 || ex > 40) return sumsq_row_exact(row, nvec);
+    for (int i = 0; i < VPL; ++i) mx = sumsq_vmax(mx, vec[i]);
+    int ex = 0;
+    float early = 0.0f;
+    bool slow;
+    if (!sumsq_plan(mx, &ex, &early, &slow)) return slow ? sumsq_row_exact(row, nvec) : early;
     const SumsqScales sc = sumsq_scales(ex);
     const uint64_t s1 = f2_splat(sc.s1), s2 = f2_splat(sc.s2);
     long long n1 = 0, n2 = 0;
@@ -459,59 +415,43 @@ __device__ __forceinline__ float warp_sumsq_rn_packed(const uint4 (&vec)[VPL], c
         uint64_t a1 = 0, a2 = 0;       // 64 squares per half at most: exact
 #pragma unroll
         for (int i = g; i < g + 16 && i < VPL; ++i) {
-            const uint32_t wd[4] = {vec[i].x, vec[i].y, vec[i].z, vec[i].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint64_t x2 = f2_from_bf16x2(wd[j]);
-                const uint64_t sq = f2_mul(x2, x2);
-                const uint64_t q1 = f2_sub(f2_add_rz(s1, sq), s1);
-                a1 = f2_add(a1, q1);
-                const uint64_t r1 = f2_sub(sq, q1);
-                const uint64_t q2 = f2_sub(f2_add_rz(s2, r1), s2);
-                a2 = f2_add(a2, q2);
-                a3 = f2_add(a3, f2_sub(r1, q2));
-            }
+            sumsq_word(vec[i].x, s1, s2, a1, a2, a3);
+            sumsq_word(vec[i].y, s1, s2, a1, a2, a3);
+            sumsq_word(vec[i].z, s1, s2, a1, a2, a3);
+            sumsq_word(vec[i].w, s1, s2, a1, a2, a3);
         }
-        n1 += __float2ll_rn(__fmul_rn(f2_lo(a1), sc.k1)) + __float2ll_rn(__fmul_rn(f2_hi(a1), sc.k1));
-        n2 += __float2ll_rn(__fmul_rn(f2_lo(a2), sc.k2)) + __float2ll_rn(__fmul_rn(f2_hi(a2), sc.k2));
+        sumsq_group_end(a1, a2, sc, n1, n2);
     }
-    n1 = warp_sum_ll(n1);
-    n2 = warp_sum_ll(n2);
-    float r = __fadd_rn(f2_lo(a3), f2_hi(a3));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) r = __fadd_rn(r, __shfl_xor_sync(0xffffffffu, r, off));
-    const long long T = (n1 << 16) + n2;          // units u2 = 2^(2ex - 30)
-    const double A = static_cast<double>(r) * static_cast<double>(sc.k2);
-    const double d = (8.0 * VPL + 8.0) * 0x1p-23;
-    // squares of values below 2^-63: at most 2^-149 each from exact, in units of u2
-    const double tiny = 8.0 * 32 * VPL * ldexp(1.0, -119 - 2 * ex);
-    const long long res = round24(T, A * (1.0 - d));
-    if (round24(T, A * (1.0 + d) + tiny) != res) return sumsq_row_exact(row, nvec);
-    return __fmul_rn(__ll2float_rn(res), pow2f(2 * ex - 30));
+    return sumsq_finish(n1, n2, a3, ex, VPL, sc, row, nvec);
 }
 
 // The same, reading the row (global or shared memory) twice instead of
 // holding it in registers.
 __device__ float warp_sumsq_rn_mem(const uint4 *row, int nvec) {
     const int lane = threadIdx.x & 31;
-    uint32_t amax = 0u, amin = 0x7F800000u;
-    for (int v = lane; v < nvec; v += 32) sumsq_extent(row[v], amax, amin);
+    uint32_t mx = 0u;
+    for (int v = lane; v < nvec; v += 32) mx = sumsq_vmax(mx, row[v]);
     int ex = 0;
     float early = 0.0f;
     bool slow;
-    if (!sumsq_plan(amax, amin, &ex, &early, &slow)) return slow ? sumsq_row_exact(row, nvec) : early;
+    if (!sumsq_plan(mx, &ex, &early, &slow)) return slow ? sumsq_row_exact(row, nvec) : early;
     const SumsqScales sc = sumsq_scales(ex);
+    const uint64_t s1 = f2_splat(sc.s1), s2 = f2_splat(sc.s2);
     long long n1 = 0, n2 = 0;
-    float a3 = 0.0f;
+    uint64_t a3 = 0;
     for (int v0 = lane; v0 < nvec; v0 += 32 * 16) {
-        float a1 = 0.0f, a2 = 0.0f;       // at most 128 squares: exact
+        uint64_t a1 = 0, a2 = 0;       // 64 squares per half at most: exact
 #pragma unroll 4
-        for (int v = v0; v < v0 + 32 * 16 && v < nvec; v += 32)
-            sumsq_split8(row[v], sc.s1, sc.s2, a1, a2, a3);
-        n1 += __float2ll_rn(__fmul_rn(a1, sc.k1));
-        n2 += __float2ll_rn(__fmul_rn(a2, sc.k2));
+        for (int v = v0; v < v0 + 32 * 16 && v < nvec; v += 32) {
+            const uint4 q = row[v];
+            sumsq_word(q.x, s1, s2, a1, a2, a3);
+            sumsq_word(q.y, s1, s2, a1, a2, a3);
+            sumsq_word(q.z, s1, s2, a1, a2, a3);
+            sumsq_word(q.w, s1, s2, a1, a2, a3);
+        }
+        sumsq_group_end(a1, a2, sc, n1, n2);
     }
-    return sumsq_finish(n1, n2, a3, ex, 8 * ((nvec + 31) / 32), sc, row, nvec);
+    return sumsq_finish(n1, n2, a3, ex, (nvec + 31) / 32, sc, row, nvec);
 }
 
 __global__ void __launch_bounds__(RT_THREADS)
