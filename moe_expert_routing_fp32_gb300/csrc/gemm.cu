@@ -513,51 +513,31 @@ __device__ __forceinline__ Tile decode_tile_pair(const Params &p, int tile, cons
 
 // One 32-row x 64-byte output box of an epilogue warp (lane i holds row
 // row0 + i as 16 words: 32 bf16 or 16 fp32 values starting at column col).
-// The rows are staged in one of the warp's two 2 KB shared-memory boxes in
+// The rows are staged in one of the warp's NBOX 2 KB shared-memory boxes in
 // the 64-byte swizzle of the output tensor map (16-byte chunk c of row r at
 // chunk c ^ ((r >> 1) & 3), conflict-free for the lanes' writes), then leave
-//   TMA:  as one TMA tensor store issued by lane 0 (two boxes per warp, so
-//         that the next box is written while the store reads the last);
-//   else: through the load/store units, the warp reading the box back
-//         row-contiguously (8 rows of 64 bytes per instruction) and writing
-//         coalesced 16-byte chunks (one box per warp suffices: the box is
-//         read back before it is written again).
-template <bool TMA>
-__device__ __forceinline__ void emit_out_box(const Params &p, uint8_t *ebox, int &eb, int lane,
+// as one TMA tensor store issued by lane 0.  With two boxes the next box is
+// written while the store reads the last; with one, the warp first waits for
+// the previous store to have read it.
+template <int NBOX>
+__device__ __forceinline__ void emit_out_box(uint8_t *ebox, int &eb, int lane,
                                              const uint32_t (&w)[16], const CUtensorMap *map,
                                              int col, int row0) {
+    static_assert(NBOX == 1 || NBOX == 2, "one or two staging boxes");
     uint8_t *box = ebox + eb * EPI_BYTES;
-    if (TMA && lane == 0) bulk_wait_read<1>();   // the store that last used this box has read it
+    if (lane == 0) bulk_wait_read<NBOX - 1>();   // the store that last used this box has read it
     __syncwarp();
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch)
         *reinterpret_cast<uint4 *>(box + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4)) =
             make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
-    if (TMA) {
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) {
-            tma_store_2d(map, box, col, row0);
-            bulk_commit();
-        }
-    } else {
-        __syncwarp();
-        const bool seg1 = map == &p.tmO1;
-        const bool f32 = (seg1 ? p.out1_f32 : p.out0_f32) != 0;
-        const int esz = f32 ? 4 : 2;
-        const int64_t ld = (seg1 ? p.ldo1 : p.ldo0) * esz;
-        uint8_t *g = static_cast<uint8_t *>(seg1 ? p.out1 : p.out0) +
-                     static_cast<int64_t>(row0) * ld + static_cast<int64_t>(col) * esz;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int id = i * 32 + lane;
-            const int r = id >> 2, ch = id & 3;
-            const uint4 v =
-                *reinterpret_cast<const uint4 *>(box + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
-            *reinterpret_cast<uint4 *>(g + r * ld + ch * 16) = v;
-        }
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(map, box, col, row0);
+        bulk_commit();
     }
-    if (TMA) eb ^= 1;
+    if (NBOX == 2) eb ^= 1;
 }
 
 template <int MODE>
@@ -851,7 +831,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         uint8_t *ebox = smem + Cfg2::EPI_OFF + (warp - 2) * 2 * EPI_BYTES;
         int eb = 0;
         auto emit_box = [&](const uint32_t(&w)[16], const CUtensorMap *map, int col, int row0) {
-            emit_out_box<true>(p, ebox, eb, lane, w, map, col, row0);
+            emit_out_box<2>(ebox, eb, lane, w, map, col, row0);
         };
         for (;;) {
             int tile = 0, got = 1;
@@ -1009,9 +989,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // soon as that is free and runs ahead on it over the staged k-slices (their
 // stages are released only once the half-1 MMAs of the slice are issued)
 // until half 1 is free too.  A four-deep ring of 48 KB stages gives that
-// run-ahead room; the output leaves through the load/store units from one
-// staging box per warp (the TMA engine stays with the operand loads; three
-// stages with TMA stores were 1.7% slower on the skewed load).
+// run-ahead room and leaves shared memory for one staging box per warp: the
+// output leaves as TMA tensor stores, each warp waiting for its previous
+// store to have read the box (measured against the same box read back and
+// written through the load/store units: the down matmul 1.8-3.6% faster).
 // A group's last block of at most 128 rows runs as M=128 pair MMAs (64 rows
 // per CTA): MMA h then occupies TMEM columns [256h, 256h + 128), the CTA's
 // 64 rows in lanes 0-63 for N columns 0-127 and again in lanes 64-127 for
@@ -1406,7 +1387,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? W_THREADS_G
         uint8_t *ebox = smem + CfgW::EPI_OFF + (warp - 2) * W_BOXES * EPI_BYTES;
         int eb = 0;
         auto emit_box = [&](const uint32_t(&w)[16], const CUtensorMap *map, int col, int row0) {
-            emit_out_box<false>(p, ebox, eb, lane, w, map, col, row0);
+            emit_out_box<W_BOXES>(ebox, eb, lane, w, map, col, row0);
         };
         for (;;) {
             int tile = 0, got = 1;
