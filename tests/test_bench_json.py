@@ -150,3 +150,20 @@ def test_y_f32_mode_counts_fp32_routed_rows():
     res = bench.finish_ours(_args(y_f32=True), wl, 1, 0, 10, 3, 80.0, _stages(1.0), CLK, None, {})
     assert res["config"]["routed_expert_outputs"].startswith("fp32")
     assert res["roofline"]["traffic"] is None
+
+
+def test_gathered_rows_count_no_permute_pass():
+    """With the rows gathered inside the w13 matmul (MOE_GATHER_A) the permute
+    stage has no bytes, the step one launch fewer, and the recorded w13
+    traffic (taken on the permute path's kernel) does not apply."""
+    wl = WORKLOADS["imagegen-16k"]
+    a = bench.stage_bytes_flops(wl, active=wl.E)
+    b = bench.stage_bytes_flops(wl, active=wl.E, gather=True)
+    assert a["permute"]["bytes"] > 0 and b["permute"]["bytes"] == 0
+    assert b["gemm_w13_swiglu"] == a["gemm_w13_swiglu"]
+    plain = bench.finish_ours(_args(), wl, 1, 0, 10, 3, 80.0, _stages(1.0), CLK, None, {})
+    gath = bench.finish_ours(_args(), wl, 1, 0, 10, 3, 80.0, _stages(1.0), CLK, None, {},
+                             gather=True)
+    assert gath["gpu_launches"] == plain["gpu_launches"] - 10
+    assert gath["roofline"]["traffic"] is None
+    assert "gathered" in gath["config"]["w13_rows"]
