@@ -46,6 +46,7 @@ the layer) on the host cores on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -157,7 +158,9 @@ def host_cores() -> int:
 
 # --------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling every 50 ms, started ahead of a timed region;
+    only the samples taken between begin() and end() are summarised."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
@@ -165,6 +168,7 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.proc = None
         self.path = None
+        self.t_begin = self.t_end = None
         try:
             import torch
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
@@ -181,22 +185,51 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
+    def begin(self):
+        """Wait (at most 3 s) until the sampler writes, then open the window."""
+        deadline = time.time() + 3.0
+        while self.proc is not None and time.time() < deadline:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
+        self.t_begin = time.time()
+
+    def end(self):
+        self.t_end = time.time()
+
     def stop(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.12)
+        time.sleep(0.06)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 8:
-                    rows.append(parts)
+            lines = f.readlines()
         os.unlink(self.path)
+        return self.summary(lines, self.t_begin, self.t_end)
+
+    @classmethod
+    def summary(cls, lines, t_begin=None, t_end=None) -> dict:
+        """Median SM clock, maximum clock, median power and the throttle
+        reasons seen, over the samples stamped inside [t_begin, t_end] (all
+        of them when none is)."""
+        rows = [[p.strip() for p in line.split(",")] for line in lines]
+        rows = [r for r in rows if len(r) >= 9]
+
+        def stamp(v):
+            try:
+                return datetime.datetime.strptime(v, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+        if t_begin is not None and t_end is not None:
+            inside = [r for r in rows if (stamp(r[0]) or 0.0) >= t_begin - 0.025 and
+                      (stamp(r[0]) or 0.0) <= t_end + 0.025]
+            if inside:
+                rows = inside
+        rows = [r[1:] for r in rows]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
 
@@ -210,16 +243,16 @@ class ClockSampler:
         pw = [num(r[2]) for r in rows if num(r[2]) is not None]
         reasons = set()
         for r in rows:
-            for name, v in zip(self.REASONS, r[4:8]):
+            for name, v in zip(cls.REASONS, r[4:8]):
                 if v.lower() == "active":
                     reasons.add(name)
+        window = round(t_end - t_begin, 3) if t_begin is not None and t_end is not None else None
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "power_w_median": statistics.median(pw) if pw else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "reasons": sorted(reasons), "samples": len(rows), "window_s": window}
 
 
-# --------------------------------------------------------------- traffic
 def kernel_fingerprint() -> str:
     h = hashlib.sha256()
     for rel in ("moe_expert_routing_fp32_gb300/csrc/gemm.cu",
@@ -427,6 +460,7 @@ def run_ours(args, rank, world, local):
             torch.distributed.barrier()
         torch.cuda.synchronize()
         clocks = ClockSampler(local)
+        clocks.begin()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record()
@@ -434,6 +468,7 @@ def run_ours(args, rank, world, local):
             step(d, i)
         end.record()
         torch.cuda.synchronize()
+        clocks.end()
         if dist:
             torch.distributed.barrier()
         clk = clocks.stop()
@@ -499,6 +534,7 @@ def run_ours(args, rank, world, local):
             torch.distributed.barrier()
         torch.cuda.synchronize()
         clocks = ClockSampler(local)
+        clocks.begin()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record()
@@ -506,6 +542,7 @@ def run_ours(args, rank, world, local):
             step(desc, i - (n_steady - K) if i >= n_steady - K else None)
         end.record()
         torch.cuda.synchronize()
+        clocks.end()
         sclk = clocks.stop()
         check("in the steady-state loop")
         sms = max_over_ranks(start.elapsed_time(end), world, dev)

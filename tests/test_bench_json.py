@@ -167,3 +167,26 @@ def test_gathered_rows_count_no_permute_pass():
     assert gath["gpu_launches"] == plain["gpu_launches"] - 10
     assert gath["roofline"]["traffic"] is None
     assert "gathered" in gath["config"]["w13_rows"]
+
+
+def test_clock_summary_keeps_the_timed_window():
+    """nvidia-smi samples before and after the timed region (idle clocks,
+    low power) are left out of the clock record."""
+    import datetime
+
+    def line(t, mhz, watts, cap="Not Active"):
+        ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return (f"{ts}, {mhz}, 2070, {watts}, 0x0, Not Active, Not Active, Not Active, "
+                f"{cap}\n")
+    t0 = 1_800_000_000.0
+    lines = [line(t0 - 0.5, 2070, 150), line(t0 - 0.2, 2070, 160)]
+    lines += [line(t0 + 0.05 * i, 1800 + i, 1300, "Active") for i in range(1, 8)]
+    lines += [line(t0 + 0.9, 2070, 200)]
+    s = bench.ClockSampler.summary(lines, t0, t0 + 0.4)
+    assert s["samples"] == 7
+    assert s["sm_mhz"] == 1804
+    assert s["power_w_median"] == 1300
+    assert s["reasons"] == ["sw_power_cap"]
+    assert s["window_s"] == pytest.approx(0.4)
+    everything = bench.ClockSampler.summary(lines)
+    assert everything["samples"] == 10
