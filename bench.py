@@ -254,11 +254,17 @@ class ClockSampler:
 
 
 def kernel_fingerprint() -> str:
+    """sha of the matmul sources with comments and whitespace taken out, so
+    that an edited comment does not void a recorded capture."""
+    import re
     h = hashlib.sha256()
     for rel in ("moe_expert_routing_fp32_gb300/csrc/gemm.cu",
                 "moe_expert_routing_fp32_gb300/csrc/common.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("".join(src.split()).encode())
     return h.hexdigest()[:12]
 
 

@@ -31,6 +31,15 @@
 // The two accumulators let the epilogue of tile i overlap the MMAs of i+1.
 // Every wait is bounded (MOE_DEV_TIMEOUT) and on abort each role lets its
 // in-flight copies / MMAs finish before the TMEM is freed.
+//
+// Two CTA-pair kernels (tcgen05 cta_group::2, clusters of two SMs, tiles
+// handed out in order through a per-launch counter) take the launches with
+// many rows per group: 256 x 256 tiles with a double-buffered accumulator,
+// and (the default there) 256 x 512 tiles whose accumulator fills TMEM,
+// with a quarter fewer operand bytes per flop.  The latter can also copy its
+// A rows itself by source token instead of reading permuted rows.  Each is
+// described above its code; the host picks per launch (MOE_GEMM_KERNEL=
+// single|pair|wide forces one).
 #include <cuda.h>
 
 #include <stdio.h>
