@@ -117,3 +117,27 @@ def test_no_device_is_an_error_not_a_fallback(L):
     P = ctypes.c_void_p
     fake = P(0x1000)
     assert L.moe_gate_topk(fake, 4, 8, 2, 0, fake, fake, None) == 5
+
+
+def _ws(L, desc):
+    n = ctypes.c_size_t(0)
+    assert L.moe_layer_workspace_size(ctypes.byref(desc), ctypes.byref(n)) == 0
+    return n.value
+
+
+def test_gathered_rows_change_the_workspace_only_where_they_apply(L):
+    """MOE_GATHER_A drops expanded_x from the layer workspace (its N x H
+    bf16 rows) and adds the source-token array (N int32), but only where the
+    w13 matmul runs on the wide pair kernel (>= 1024 rows per expert on
+    average, I a multiple of 256); elsewhere the flag is ignored."""
+    if os.environ.get("MOE_GEMM_KERNEL"):
+        pytest.skip("kernel choice forced in the environment")
+    T, H, E, k, I = 16384, 4096, 64, 8, 3072                 # 2048 rows per expert
+    N = T * k
+    plain = _ws(L, moe.make_desc(T, H, E, k, I, I, rmsnorm=True))
+    gath = _ws(L, moe.make_desc(T, H, E, k, I, I, rmsnorm=True, gather_a=True))
+    assert plain - gath >= N * H * 2 - N * 4 - 512            # alignment slack
+    T, H, I = 4096, 2048, 1024                                # 512 rows per expert
+    plain = _ws(L, moe.make_desc(T, H, E, k, I))
+    gath = _ws(L, moe.make_desc(T, H, E, k, I, gather_a=True))
+    assert plain == gath
