@@ -163,10 +163,16 @@ __device__ __forceinline__ float slot_weight(const float (&v)[NV], int k, bool r
 // (n + 8) 2^-23 for n squares per lane.  A nonzero |x| below 2^-63 has an
 // inexact fp32 square (at most 2^-149 off, or zero), which widens the
 // interval by H 2^-149: the exact sum is T + R with R in
-// [A (1 - d), A (1 + d) + H 2^-149 / u2].  Rounded to 24 bits, both ends of
-// that interval giving the same fp32 value decides the result; otherwise (the
+// [A (1 - d), A (1 + d) + H 2^-149 / u2].  The ends are taken in 64-bit
+// fixed point with 16 fractional bits (T below 2^46, else the slow path; A
+// below the row length H, at most 2^20 here, else the slow path): A rounded down
+// for the lower end and up for the upper one, d A rounded up with at least
+// 2^-23 of a unit to spare, more than the 2^-149 terms (below 2^-67 u2 for
+// ex >= -20).  Rounded to 24 bits, both
+// ends giving the same fp32 value decides the result; otherwise (the
 // interval holds a rounding tie, or the sum sits exactly on one with no
-// residual) the slow path decides.
+// residual) the slow path decides.  All of it is integer arithmetic: the
+// fp64 rate of the part is a small fraction of its fp32 rate.
 // Slow path: every square m^2 * 2^(2E-268) (m the 8-bit significand, E the
 // biased exponent, at least 1) is added exactly into a fixed-point number of
 // 20 32-bit limbs per lane (unit 2^-266), the lanes' numbers are added
@@ -251,21 +257,17 @@ __device__ __noinline__ float sumsq_row_exact(const uint4 *row, int nvec) {
     return __shfl_sync(0xffffffffu, res, 0);
 }
 
-// n + f (an integer n >= 2^30 and a real f >= 0, in units u2) rounded to 24
-// significant bits, nearest-even: the rounded value, an integer of at most 24
-// significant bits.  (n >= 2^30: the largest square alone is at least 2^30 u2.)
-__device__ __forceinline__ long long round24(long long n0, double f) {
-    const double fl = floor(f);
-    const long long n = n0 + static_cast<long long>(fl);
-    const double fr = f - fl;
-    const int top = 63 - __clzll(n);
-    const int L = top - 23;
-    const long long q = n >> L;
-    const long long rem = n & ((1ll << L) - 1);
-    const long long half = 1ll << (L - 1);
-    const double d = static_cast<double>(rem - half) + fr;
-    const bool up = d > 0.0 || (d == 0.0 && (q & 1));
-    return (q + (up ? 1 : 0)) << L;
+// v / 2^16 (v > 0 in fixed point with 16 fractional bits, its integer part
+// at least 2^30 in units u2) rounded to 24 significant bits, nearest-even:
+// the rounded value in units u2, an integer of at most 24 significant bits.
+// (At least 2^30: the largest square alone is at least 2^30 u2.)
+__device__ __forceinline__ long long round24_fx16(long long v) {
+    const int shift = (63 - __clzll(v)) - 23;       // >= 23: drops the fraction too
+    const long long q = v >> shift;
+    const long long rem = v & ((1ll << shift) - 1);
+    const long long half = 1ll << (shift - 1);
+    const bool up = rem > half || (rem == half && (q & 1));
+    return (q + (up ? 1 : 0)) << (shift - 16);
 }
 
 // Packed fp32 pairs (the two halves of a 64-bit register): one instruction
@@ -381,12 +383,19 @@ __device__ __forceinline__ float sumsq_finish(long long n1, long long n2, uint64
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) r = __fadd_rn(r, __shfl_xor_sync(0xffffffffu, r, off));
     const long long T = (n1 << 16) + n2;          // units u2 = 2^(2ex - 30)
-    const double A = static_cast<double>(r) * static_cast<double>(sc.k2);
-    const double d = (8.0 * vpl + 8.0) * 0x1p-23;
-    // squares of values below 2^-63: at most 2^-149 each from exact, in units of u2
-    const double tiny = 8.0 * 32 * vpl * ldexp(1.0, -119 - 2 * ex);
-    const long long res = round24(T, A * (1.0 - d));
-    if (round24(T, A * (1.0 + d) + tiny) != res) return sumsq_row_exact(row, nvec);
+    if (T >= (1ll << 46) || nvec > (1 << 17)) return sumsq_row_exact(row, nvec);
+    // A = r / u2 exactly in fp32 (a power-of-two scaling), below H; in fixed
+    // point with 16 fractional bits, rounded down and up
+    const float a16 = __fmul_rn(__fmul_rn(r, sc.k2), 65536.0f);
+    const long long a_lo = __float2ll_rd(a16), a_hi = __float2ll_ru(a16);
+    // d A with d = (8 vpl + 8) 2^-23: a multiple of 2^-23 units, rounded up
+    // past the next integer
+    const long long da = ((a_hi * (8ll * vpl + 8)) >> 23) + 1;
+    const long long base = T << 16;
+    const long long lo = max(base, base + a_lo - da);
+    const long long hi = base + a_hi + da;
+    const long long res = round24_fx16(lo);
+    if (round24_fx16(hi) != res) return sumsq_row_exact(row, nvec);
     // res has at most 24 significant bits: exact in fp32, and so is the
     // power-of-two scaling (the result is normal)
     return __fmul_rn(__ll2float_rn(res), pow2f(2 * ex - 30));
