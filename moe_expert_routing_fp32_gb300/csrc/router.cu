@@ -973,16 +973,25 @@ topk_kernel(const float *__restrict__ logits, int T, int E, int k, int renorm,
 // Used ahead of the tensor-core gate: one warp per row.  The row (at most
 // VPL 16-byte vectors per lane) is held in registers; its sum of squares is
 // the warp's exact one above; then xn = bf16((x * r) * gamma) leaves as
-// 16-byte stores.  No shared memory, no waits.
+// 16-byte stores.  gamma is staged in shared memory once per CTA (zeros past
+// the row), so the normalisation reads it without a global-load latency per
+// vector and without a bound check.  No waits.
 constexpr int RN_THREADS = 256;
 
 template <int VPL>
 __global__ void __launch_bounds__(RN_THREADS, 2)
 rmsnorm_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma, int T, int H,
                float eps, uint16_t *__restrict__ xn) {
+    __shared__ uint4 s_gamma[VPL * 32];
     const int lane = threadIdx.x & 31;
     const int nvec = H / 8;
     const int nwarps = gridDim.x * (RN_THREADS / 32);
+    if (gamma) {
+        for (int v = threadIdx.x; v < VPL * 32; v += RN_THREADS)
+            s_gamma[v] = v < nvec ? __ldg(reinterpret_cast<const uint4 *>(gamma) + v)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+        __syncthreads();
+    }
     for (int t = blockIdx.x * (RN_THREADS / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
         const uint4 *row = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
         uint4 q[VPL];
@@ -998,9 +1007,8 @@ rmsnorm_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamm
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
             const int v = lane + 32 * i;
-            if (v >= nvec) break;
             uint4 gq = make_uint4(0u, 0u, 0u, 0u);
-            if (gamma) gq = __ldg(reinterpret_cast<const uint4 *>(gamma) + v);
+            if (gamma) gq = s_gamma[v];
             const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
             const uint32_t wd[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
             uint32_t packed[4];
@@ -1012,7 +1020,7 @@ rmsnorm_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamm
                 const __nv_bfloat162 p2 = __floats2bfloat162_rn(f2_lo(y), f2_hi(y));
                 packed[j] = *reinterpret_cast<const uint32_t *>(&p2);
             }
-            out[v] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            if (v < nvec) out[v] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
     }
 }
