@@ -182,9 +182,7 @@ __device__ __forceinline__ float slot_weight(const float (&v)[NV], int k, bool r
 constexpr int SQ_LIMBS = 20;
 
 __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
-    return v;
+    return __reduce_max_sync(0xffffffffu, v);
 }
 __device__ __forceinline__ long long warp_sum_ll(long long v) {
 #pragma unroll
@@ -377,8 +375,17 @@ __device__ __forceinline__ void sumsq_group_end(uint64_t a1, uint64_t a2, const 
 __device__ __forceinline__ float sumsq_finish(long long n1, long long n2, uint64_t a3, int ex,
                                               int vpl, const SumsqScales &sc, const uint4 *row,
                                               int nvec) {
-    n1 = warp_sum_ll(n1);
-    n2 = warp_sum_ll(n2);
+    // A lane's n1 and n2 are each below ceil(vpl / 16) 2^23 (per group of 16
+    // vectors, two pair halves of 64 squares below 2^22 units each): up to
+    // 64 vectors per lane the warp's sums fit 32 bits and take one reduction
+    // instruction each.
+    if (vpl <= 64) {
+        n1 = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(n1));
+        n2 = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(n2));
+    } else {
+        n1 = warp_sum_ll(n1);
+        n2 = warp_sum_ll(n2);
+    }
     float r = __fadd_rn(f2_lo(a3), f2_hi(a3));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) r = __fadd_rn(r, __shfl_xor_sync(0xffffffffu, r, off));
