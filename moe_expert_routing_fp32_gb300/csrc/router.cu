@@ -149,30 +149,34 @@ __device__ __forceinline__ float slot_weight(const float (&v)[NV], int k, bool r
 //
 // Fast path (finite rows whose largest |x| lies in [2^-20, 2^40]), on packed
 // fp32 pairs (one instruction for two values).  With ex the exponent of the
-// largest |x|, every square is below 2^(2ex+2).  Each square v is split
-// exactly into
-//   q1 = v truncated to a multiple of u1 = 2^(2ex-14) (s1 + v rounded toward
-//        zero, minus s1, with s1 = 2^(2ex+9)),
-//   q2 = the rest truncated to a multiple of u2 = 2^(2ex-30) (s2 = 2^(2ex-7)),
-//   r2 = the rest, 0 <= r2 < u2.
-// The q1 of at most 64 squares (one half of the pairs of 16 vectors of a
-// lane) add up exactly in fp32 (multiples of u1 below 2^24 u1), likewise the
-// q2; those group sums become exact integers (units u1, u2) summed across
-// lanes in 64 bits, giving T = sum(q1 + q2) / u2 exactly.  The r2 are summed
-// in fp32 (A, in units of u2 after scaling) with a relative error below
-// (n + 8) 2^-23 for n squares per lane.  A nonzero |x| below 2^-63 has an
-// inexact fp32 square (at most 2^-149 off, or zero), which widens the
-// interval by H 2^-149: the exact sum is T + R with R in
-// [A (1 - d), A (1 + d) + H 2^-149 / u2].  The ends are taken in 64-bit
-// fixed point with 16 fractional bits (T below 2^46, else the slow path; A
-// below the row length H, at most 2^20 here, else the slow path): A rounded down
-// for the lower end and up for the upper one, d A rounded up with at least
-// 2^-23 of a unit to spare, more than the 2^-149 terms (below 2^-67 u2 for
-// ex >= -20).  Rounded to 24 bits, both
-// ends giving the same fp32 value decides the result; otherwise (the
-// interval holds a rounding tie, or the sum sits exactly on one with no
-// residual) the slow path decides.  All of it is integer arithmetic: the
-// fp64 rate of the part is a small fraction of its fp32 rate.
+// largest |x|, every square v is below 2^(2ex+2) and exact in fp32 (16
+// significant bits; see below for |x| < 2^-63).  Per group of at most 64
+// squares (one half of the pairs of 16 vectors of a lane) two accumulators
+// are kept inside one binade each, so that every addition into them is an
+// error-free transformation of round-to-nearest (the accumulator is the
+// larger operand):
+//   a1 starts at s1 = 2^(2ex+9) and stays below s1 + 2^(2ex+8), on the grid
+//      u1 = 2^(2ex-14):  t = a1 + v,  r1 = v - (t - a1) exactly,  a1 = t,
+//      so |r1| <= u1 / 2;
+//   a2 starts at s2 = 3 2^(2ex-8) and stays within s2 +- 2^(2ex-9), on the
+//      grid u2 = 2^(2ex-30):  t = a2 + r1,  e = r1 - (t - a2) exactly,
+//      a2 = t, so |e| <= u2 / 2.
+// a1 - s1 and a2 - s2 are then exact integers in units u1 and u2 (signed for
+// a2), summed across the lanes as integers, giving T = sum(v - e) / u2
+// exactly.  The e are summed in fp32 (A, in units of u2 after scaling); a
+// value passes through at most m = 4 vpl + 5 roundings (vpl vectors per
+// lane: 4 vpl per pair half, the halves, five butterfly steps), so the
+// error is at most m 2^-24 (1 + 2^-20) sum|e| <= (4 vpl + 5) vpl 2^-17 u2.
+// A nonzero |x| below 2^-63 has an inexact fp32 square (at most 2^-149 off,
+// or zero), which moves the sum by at most H 2^-149, below 2^-66 u2 for
+// ex >= -20.  The exact sum is thus within E of T + A.  The ends T + A -+ E
+// are taken in 64-bit fixed point with 16 fractional bits (T below 2^46,
+// else the slow path; A rounded down for the lower end and up for the upper
+// one; E rounded up with at least one unit to spare).  Rounded to 24 bits,
+// both ends giving the same fp32 value decides the result; otherwise (the
+// interval holds a rounding tie, or the sum sits exactly on one) the slow
+// path decides.  All of it is fp32 and integer arithmetic: the fp64 rate of
+// the part is a small fraction of its fp32 rate.
 // Slow path: every square m^2 * 2^(2E-268) (m the 8-bit significand, E the
 // biased exponent, at least 1) is added exactly into a fixed-point number of
 // 20 32-bit limbs per lane (unit 2^-266), the lanes' numbers are added
@@ -256,9 +260,10 @@ __device__ __noinline__ float sumsq_row_exact(const uint4 *row, int nvec) {
 }
 
 // v / 2^16 (v > 0 in fixed point with 16 fractional bits, its integer part
-// at least 2^30 in units u2) rounded to 24 significant bits, nearest-even:
+// at least 2^29 in units u2) rounded to 24 significant bits, nearest-even:
 // the rounded value in units u2, an integer of at most 24 significant bits.
-// (At least 2^30: the largest square alone is at least 2^30 u2.)
+// (At least 2^29: the largest square alone is at least 2^30 u2, the error
+// terms below 2^19 u2 for the row lengths taken here.)
 __device__ __forceinline__ long long round24_fx16(long long v) {
     const int shift = (63 - __clzll(v)) - 23;       // >= 23: drops the fraction too
     const long long q = v >> shift;
@@ -270,11 +275,6 @@ __device__ __forceinline__ long long round24_fx16(long long v) {
 
 // Packed fp32 pairs (the two halves of a 64-bit register): one instruction
 // works on both values.
-__device__ __forceinline__ uint64_t f2_add_rz(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -315,7 +315,8 @@ __device__ __forceinline__ float pow2f(int e) {   // 2^e, e in fp32's normal ran
     return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 __device__ __forceinline__ SumsqScales sumsq_scales(int ex) {
-    return SumsqScales{pow2f(2 * ex + 9), pow2f(2 * ex - 7), pow2f(14 - 2 * ex), pow2f(30 - 2 * ex)};
+    return SumsqScales{pow2f(2 * ex + 9), 3.0f * pow2f(2 * ex - 8), pow2f(14 - 2 * ex),
+                       pow2f(30 - 2 * ex)};
 }
 
 // Pass 1 over a vector: the packed maximum of its 16-bit magnitudes.
@@ -348,25 +349,27 @@ __device__ __forceinline__ bool sumsq_plan(uint32_t mx, int *ex, float *early, b
     return true;
 }
 
-// Pass 2 over one word (two bf16 values): the squares split into q1, q2 and
-// the rest, accumulated into a1, a2 and a3.
-__device__ __forceinline__ void sumsq_word(uint32_t w, uint64_t s1, uint64_t s2, uint64_t &a1,
-                                           uint64_t &a2, uint64_t &a3) {
+// Pass 2 over one word (two bf16 values): the squares added into a1, their
+// rounding errors into a2, and those rounding errors into a3.
+__device__ __forceinline__ void sumsq_word(uint32_t w, uint64_t &a1, uint64_t &a2, uint64_t &a3) {
     const uint64_t x2 = f2_from_bf16x2(w);
     const uint64_t sq = f2_mul(x2, x2);
-    const uint64_t q1 = f2_sub(f2_add_rz(s1, sq), s1);
-    a1 = f2_add(a1, q1);
-    const uint64_t r1 = f2_sub(sq, q1);
-    const uint64_t q2 = f2_sub(f2_add_rz(s2, r1), s2);
-    a2 = f2_add(a2, q2);
-    a3 = f2_add(a3, f2_sub(r1, q2));
+    const uint64_t t1 = f2_add(a1, sq);
+    const uint64_t r1 = f2_sub(sq, f2_sub(t1, a1));
+    a1 = t1;
+    const uint64_t t2 = f2_add(a2, r1);
+    a3 = f2_add(a3, f2_sub(r1, f2_sub(t2, a2)));
+    a2 = t2;
 }
 
-// A group's exact q1 and q2 sums (both halves) as integers in units u1, u2.
+// A group's exact accumulator offsets (both halves) as integers in units u1,
+// u2 (the subtractions are exact: each accumulator stays within a factor of
+// two of its start).
 __device__ __forceinline__ void sumsq_group_end(uint64_t a1, uint64_t a2, const SumsqScales &sc,
                                                 long long &n1, long long &n2) {
-    n1 += __float2ll_rn(__fmul_rn(f2_lo(a1), sc.k1)) + __float2ll_rn(__fmul_rn(f2_hi(a1), sc.k1));
-    n2 += __float2ll_rn(__fmul_rn(f2_lo(a2), sc.k2)) + __float2ll_rn(__fmul_rn(f2_hi(a2), sc.k2));
+    const uint64_t d1 = f2_sub(a1, f2_splat(sc.s1)), d2 = f2_sub(a2, f2_splat(sc.s2));
+    n1 += __float2ll_rn(__fmul_rn(f2_lo(d1), sc.k1)) + __float2ll_rn(__fmul_rn(f2_hi(d1), sc.k1));
+    n2 += __float2ll_rn(__fmul_rn(f2_lo(d2), sc.k2)) + __float2ll_rn(__fmul_rn(f2_hi(d2), sc.k2));
 }
 
 // The lanes' integer sums and residual sums -> the rounded result, or the
@@ -375,13 +378,13 @@ __device__ __forceinline__ void sumsq_group_end(uint64_t a1, uint64_t a2, const 
 __device__ __forceinline__ float sumsq_finish(long long n1, long long n2, uint64_t a3, int ex,
                                               int vpl, const SumsqScales &sc, const uint4 *row,
                                               int nvec) {
-    // A lane's n1 and n2 are each below ceil(vpl / 16) 2^23 (per group of 16
-    // vectors, two pair halves of 64 squares below 2^22 units each): up to
+    // A lane's |n1| and |n2| are each below ceil(vpl / 16) 2^23 (per group of
+    // 16 vectors, two pair halves of 64 terms below 2^22 units each): up to
     // 64 vectors per lane the warp's sums fit 32 bits and take one reduction
     // instruction each.
     if (vpl <= 64) {
-        n1 = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(n1));
-        n2 = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(n2));
+        n1 = __reduce_add_sync(0xffffffffu, static_cast<int>(n1));
+        n2 = __reduce_add_sync(0xffffffffu, static_cast<int>(n2));
     } else {
         n1 = warp_sum_ll(n1);
         n2 = warp_sum_ll(n2);
@@ -391,16 +394,16 @@ __device__ __forceinline__ float sumsq_finish(long long n1, long long n2, uint64
     for (int off = 16; off > 0; off >>= 1) r = __fadd_rn(r, __shfl_xor_sync(0xffffffffu, r, off));
     const long long T = (n1 << 16) + n2;          // units u2 = 2^(2ex - 30)
     if (T >= (1ll << 46) || nvec > (1 << 17)) return sumsq_row_exact(row, nvec);
-    // A = r / u2 exactly in fp32 (a power-of-two scaling), below H; in fixed
-    // point with 16 fractional bits, rounded down and up
+    // A = r / u2 exactly in fp32 (a power-of-two scaling), |A| <= H / 2; in
+    // fixed point with 16 fractional bits, rounded down and up
     const float a16 = __fmul_rn(__fmul_rn(r, sc.k2), 65536.0f);
     const long long a_lo = __float2ll_rd(a16), a_hi = __float2ll_ru(a16);
-    // d A with d = (8 vpl + 8) 2^-23: a multiple of 2^-23 units, rounded up
-    // past the next integer
-    const long long da = ((a_hi * (8ll * vpl + 8)) >> 23) + 1;
+    // E = (4 vpl + 5) vpl 2^-17 u2 = (4 vpl + 5) vpl / 2 units, rounded up
+    // with more than one unit to spare
+    const long long err = (4ll * vpl + 6) * vpl / 2 + 2;
     const long long base = T << 16;
-    const long long lo = max(base, base + a_lo - da);
-    const long long hi = base + a_hi + da;
+    const long long lo = base + a_lo - err;
+    const long long hi = base + a_hi + err;
     const long long res = round24_fx16(lo);
     if (round24_fx16(hi) != res) return sumsq_row_exact(row, nvec);
     // res has at most 24 significant bits: exact in fp32, and so is the
@@ -423,18 +426,18 @@ __device__ __forceinline__ float warp_sumsq_rn_packed(const uint4 (&vec)[VPL], c
     bool slow;
     if (!sumsq_plan(mx, &ex, &early, &slow)) return slow ? sumsq_row_exact(row, nvec) : early;
     const SumsqScales sc = sumsq_scales(ex);
-    const uint64_t s1 = f2_splat(sc.s1), s2 = f2_splat(sc.s2);
+    const uint64_t s1 = f2_splat(sc.s1), s2 = f2_splat(sc.s2);   // accumulator starts
     long long n1 = 0, n2 = 0;
     uint64_t a3 = 0;
 #pragma unroll
     for (int g = 0; g < VPL; g += 16) {
-        uint64_t a1 = 0, a2 = 0;       // 64 squares per half at most: exact
+        uint64_t a1 = s1, a2 = s2;     // 64 squares per half at most
 #pragma unroll
         for (int i = g; i < g + 16 && i < VPL; ++i) {
-            sumsq_word(vec[i].x, s1, s2, a1, a2, a3);
-            sumsq_word(vec[i].y, s1, s2, a1, a2, a3);
-            sumsq_word(vec[i].z, s1, s2, a1, a2, a3);
-            sumsq_word(vec[i].w, s1, s2, a1, a2, a3);
+            sumsq_word(vec[i].x, a1, a2, a3);
+            sumsq_word(vec[i].y, a1, a2, a3);
+            sumsq_word(vec[i].z, a1, a2, a3);
+            sumsq_word(vec[i].w, a1, a2, a3);
         }
         sumsq_group_end(a1, a2, sc, n1, n2);
     }
@@ -452,18 +455,18 @@ __device__ float warp_sumsq_rn_mem(const uint4 *row, int nvec) {
     bool slow;
     if (!sumsq_plan(mx, &ex, &early, &slow)) return slow ? sumsq_row_exact(row, nvec) : early;
     const SumsqScales sc = sumsq_scales(ex);
-    const uint64_t s1 = f2_splat(sc.s1), s2 = f2_splat(sc.s2);
+    const uint64_t s1 = f2_splat(sc.s1), s2 = f2_splat(sc.s2);   // accumulator starts
     long long n1 = 0, n2 = 0;
     uint64_t a3 = 0;
     for (int v0 = lane; v0 < nvec; v0 += 32 * 16) {
-        uint64_t a1 = 0, a2 = 0;       // 64 squares per half at most: exact
+        uint64_t a1 = s1, a2 = s2;     // 64 squares per half at most
 #pragma unroll 4
         for (int v = v0; v < v0 + 32 * 16 && v < nvec; v += 32) {
             const uint4 q = row[v];
-            sumsq_word(q.x, s1, s2, a1, a2, a3);
-            sumsq_word(q.y, s1, s2, a1, a2, a3);
-            sumsq_word(q.z, s1, s2, a1, a2, a3);
-            sumsq_word(q.w, s1, s2, a1, a2, a3);
+            sumsq_word(q.x, a1, a2, a3);
+            sumsq_word(q.y, a1, a2, a3);
+            sumsq_word(q.z, a1, a2, a3);
+            sumsq_word(q.w, a1, a2, a3);
         }
         sumsq_group_end(a1, a2, sc, n1, n2);
     }
