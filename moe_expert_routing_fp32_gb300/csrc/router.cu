@@ -985,7 +985,8 @@ topk_kernel(const float *__restrict__ logits, int T, int E, int k, int renorm,
 // the warp's exact one above; then xn = bf16((x * r) * gamma) leaves as
 // 16-byte stores.  gamma is staged in shared memory once per CTA (zeros past
 // the row), so the normalisation reads it without a global-load latency per
-// vector and without a bound check.  No waits.
+// vector and without a bound check.  While a row is summed, the warp's next
+// row is prefetched into L2.  No waits.
 constexpr int RN_THREADS = 256;
 
 template <int VPL>
@@ -1009,6 +1010,12 @@ rmsnorm_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamm
         for (int i = 0; i < VPL; ++i) {
             const int v = lane + 32 * i;
             q[i] = v < nvec ? __ldcs(row + v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        // the warp's next row into L2 meanwhile (one 128-byte line per lane and step)
+        if (t + nwarps < T) {
+            const char *nrow = reinterpret_cast<const char *>(x + static_cast<size_t>(t + nwarps) * H);
+            for (int off = lane * 128; off < H * 2; off += 32 * 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(nrow + off));
         }
         const float ss = warp_sumsq_rn_packed<VPL>(q, row, nvec);
         const float mean = __fdiv_rn(ss, static_cast<float>(H));
