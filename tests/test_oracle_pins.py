@@ -451,6 +451,13 @@ MUTANTS = {
     "layer_y_f32_no_shared": ("of[c] += ys[c];", "of[c] += 0.0;"),
     "finalize_f64_row_ignored": ("y_exp[(int64_t)row_idx[t * k + j] * H + c];",
                                  "y_exp[(int64_t)row_idx[t * k] * H + c];"),
+    "permute_reversed": ("xs + (int64_t)src_token[r] * H,", "xs + (int64_t)src_token[n - 1 - r] * H,"),
+    "expert_offsets_not_cumulative": ("offsets[e + 1] = offsets[e] + counts[e];",
+                                      "offsets[e + 1] = counts[e];"),
+    "grouped_weights_of_group_0": ("w13 + g * 2 * I * H, w2 + g * H * I, H, I,",
+                                   "w13, w2, H, I,"),
+    "grouped_down_of_other_group": ("w13 + g * 2 * I * H, w2 + g * H * I, H, I,",
+                                    "w13 + g * 2 * I * H, w2 + (G - 1 - g) * H * I, H, I,"),
     "ep_rank_off_by_one": ("for (int64_t rr = 0; rr < r; ++rr)",
                            "for (int64_t rr = 0; rr <= r; ++rr)"),
     "ep_finalize_wrong_side": ("memcpy(recv_y + (int64_t)local_src[d] * H, local_y + d * H,",
