@@ -61,6 +61,11 @@ def pin_rmsnorm():
     # to 1 in bf16 and xn = gamma exactly
     x = np.full((1, H), 0x4000, dtype=np.uint16)   # bf16 2.0
     assert np.array_equal(oracle.rmsnorm(x, gamma, 1e-6)[0], gamma)
+    # eps inside the root: constant row 1 with eps = 3 gives r = 1/sqrt(4) =
+    # 1/2 exactly, so xn = gamma / 2 (a power-of-two scaling of bf16, exact)
+    x = np.full((1, H), 0x3F80, dtype=np.uint16)   # bf16 1.0
+    half_gamma = f32_to_bf16_bits(bits_f64(gamma) * 0.5)
+    assert np.array_equal(oracle.rmsnorm(x, gamma, 3.0)[0], half_gamma)
     # with eps = 0, scaling x by a power of two leaves xn bit-identical
     x = f32_to_bf16_bits(rng.standard_normal((T, H)))
     x4 = f32_to_bf16_bits(bits_f64(x) * 4.0)
@@ -427,6 +432,7 @@ MUTANTS = {
     "sumsq_square_shift": ("const int sh = 2 * (e ? e : 1) - 2;",
                            "const int sh = 2 * (e ? e : 1) - 1;"),
     "rms_no_mean": ("ss / (float)H", "ss"),
+    "rms_no_eps": ("1.0f / sqrtf(mean + eps)", "1.0f / sqrtf(mean)"),
     "rms_no_gamma": ("v = v * bf16_to_float(gamma[h]);", "v = v;"),
     "gate_transposed": ("wg[e * H + h], acc)", "wg[h * E + e], acc)"),
     "gate_no_bias": ("acc = acc + bias[e];", "acc = acc;"),
@@ -434,6 +440,10 @@ MUTANTS = {
     "softmax_sign": ("exp((double)l[topk_idx[t * k + j]] - m) / den",
                      "exp(m - (double)l[topk_idx[t * k + j]]) / den"),
     "no_renorm": ("if (renorm) {", "if (0) {"),
+    "renorm_inverted": ("if (renorm) {", "if (!renorm) {"),
+    "topk_slots_reversed": ("topk_idx[t * k + j] = (int32_t)best;",
+                            "topk_idx[t * k + (k - 1 - j)] = (int32_t)best;"),
+    "finalize_unweighted": ("(double)topk_w[t * k + j] *", "1.0 *"),
     "route_src_mod": ("src_token[row] = (int32_t)(a / k);",
                       "src_token[row] = (int32_t)(a % k);"),
     "route_unstable": ("const int32_t row = offsets[e] + fill[e]++;",
