@@ -168,6 +168,17 @@ def pin_gate():
     ref = bits_f64(x) @ wg.T.astype(np.float64)
     bound = H * 2.0**-24 * (np.abs(bits_f64(x)) @ np.abs(wg.T.astype(np.float64)))
     assert np.all(np.abs(oracle.gate_logits(x, wg) - ref) <= bound)
+    # one fused multiply-add per term, ascending h (a worked case): x = [1, 1.5],
+    # w = [2, m 2^-47] with m = (2^25 + 1) / 3, so the second product is
+    # 2^-23 (1 + 2^-25) exactly.  An FMA chain rounds 2 + 2^-23 + 2^-48 up to
+    # 2 + 2^-22; rounding the product first (2^-23) leaves an exact tie that
+    # rounds to even (2), and so does the descending order (2^-23, then 2).
+    m = (2 ** 25 + 1) // 3
+    assert 3 * m == 2 ** 25 + 1 and m < 2 ** 24
+    xw = f32_to_bf16_bits(np.array([[1.0, 1.5]]))
+    ww = np.array([[2.0, m * 2.0 ** -47]], dtype=np.float32)
+    assert float(ww[0, 1]) == m * 2.0 ** -47
+    assert oracle.gate_logits(xw, ww)[0, 0] == np.float32(2.0 + 2.0 ** -22)
 
 
 def pin_topk():
@@ -436,6 +447,10 @@ MUTANTS = {
     "rms_no_gamma": ("v = v * bf16_to_float(gamma[h]);", "v = v;"),
     "gate_transposed": ("wg[e * H + h], acc)", "wg[h * E + e], acc)"),
     "gate_no_bias": ("acc = acc + bias[e];", "acc = acc;"),
+    "gate_mul_then_add": ("acc = fmaf(bf16_to_float(xs[t * H + h]), wg[e * H + h], acc);",
+                          "acc = acc + bf16_to_float(xs[t * H + h]) * wg[e * H + h];"),
+    "gate_descending_h": ("acc = fmaf(bf16_to_float(xs[t * H + h]), wg[e * H + h], acc);",
+                          "acc = fmaf(bf16_to_float(xs[t * H + (H - 1 - h)]), wg[e * H + (H - 1 - h)], acc);"),
     "topk_ties_high": ("l[e] > l[best]", "l[e] >= l[best]"),
     "softmax_sign": ("exp((double)l[topk_idx[t * k + j]] - m) / den",
                      "exp(m - (double)l[topk_idx[t * k + j]]) / den"),
