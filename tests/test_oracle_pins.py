@@ -66,6 +66,15 @@ def pin_rmsnorm():
     x = np.full((1, H), 0x3F80, dtype=np.uint16)   # bf16 1.0
     half_gamma = f32_to_bf16_bits(bits_f64(gamma) * 0.5)
     assert np.array_equal(oracle.rmsnorm(x, gamma, 3.0)[0], half_gamma)
+    # r = 1/sqrt(mean + eps) as two fp32 roundings (a worked case found by a
+    # search over fp32 values in [1, 2)): for a row of ones and eps = 32865
+    # 2^-23, sqrt(1 + eps) rounded to fp32 and its reciprocal rounded give
+    # exactly 1 - 2^-9, a bf16 tie that goes to even (1.0); the reciprocal
+    # square root of 1 + eps itself lies below 1 - 2^-9 and would give 1 - 2^-8
+    eps = 32865 * 2.0 ** -23
+    assert 1.0 / math.sqrt(1.0 + eps) < 1.0 - 2.0 ** -9 - 2.0 ** -30
+    ones = np.full(H, 0x3F80, dtype=np.uint16)
+    assert np.all(oracle.rmsnorm(x, ones, eps)[0] == 0x3F80)
     # with eps = 0, scaling x by a power of two leaves xn bit-identical
     x = f32_to_bf16_bits(rng.standard_normal((T, H)))
     x4 = f32_to_bf16_bits(bits_f64(x) * 4.0)
@@ -444,6 +453,8 @@ MUTANTS = {
                            "const int sh = 2 * (e ? e : 1) - 1;"),
     "rms_no_mean": ("ss / (float)H", "ss"),
     "rms_no_eps": ("1.0f / sqrtf(mean + eps)", "1.0f / sqrtf(mean)"),
+    "rms_r_in_double": ("1.0f / sqrtf(mean + eps)",
+                        "(float)(1.0 / sqrt((double)mean + (double)eps))"),
     "rms_no_gamma": ("v = v * bf16_to_float(gamma[h]);", "v = v;"),
     "gate_transposed": ("wg[e * H + h], acc)", "wg[h * E + e], acc)"),
     "gate_no_bias": ("acc = acc + bias[e];", "acc = acc;"),
