@@ -75,6 +75,28 @@ def pin_rmsnorm():
     assert 1.0 / math.sqrt(1.0 + eps) < 1.0 - 2.0 ** -9 - 2.0 ** -30
     ones = np.full(H, 0x3F80, dtype=np.uint16)
     assert np.all(oracle.rmsnorm(x, ones, eps)[0] == 0x3F80)
+    # xn = bf16((x r) gamma), each product rounded to fp32 (a worked case found
+    # by a search, its value derived here in exact arithmetic with explicit
+    # IEEE roundings): 255 ones and one x = 1.2890625 (gamma 0.7265625 there,
+    # ones elsewhere), eps = 33 / 4096.  x (r gamma), and a single rounding of
+    # x r gamma to bf16, both give the bf16 value one above.
+    from fractions import Fraction as Fr
+    assert _sqrt_rne(Fr(9, 4), 24) == Fr(3, 2)  # the exact helpers themselves
+    assert float(_sqrt_rne(Fr(2), 24)) == float(np.sqrt(np.float32(2.0)))
+    assert float(_rne(Fr(1, 3), 24)) == float(np.float32(1.0) / np.float32(3.0))
+    xv, gv, ev = Fr(1.2890625), Fr(0.7265625), Fr(33, 4096)
+    ss = 255 + xv * xv
+    assert _rne(ss, 24) == ss                   # exact in fp32
+    r = _rne(1 / _sqrt_rne(_rne(ss / 256 + ev, 24), 24), 24)
+    want = _rne(_rne(_rne(xv * r, 24) * gv, 24), 8)
+    assert _rne(_rne(xv * _rne(r * gv, 24), 24), 8) != want
+    assert _rne(xv * r * gv, 8) != want
+    row = np.full((1, 256), 0x3F80, dtype=np.uint16)
+    row[0, 77] = 0x3FA5                         # 1.2890625
+    gam = np.full(256, 0x3F80, dtype=np.uint16)
+    gam[77] = 0x3F3A                            # 0.7265625
+    got = oracle.rmsnorm(row, gam, float(ev))[0, 77]
+    assert bits_f64(np.array([got]))[0] == float(want)
     # with eps = 0, scaling x by a power of two leaves xn bit-identical
     x = f32_to_bf16_bits(rng.standard_normal((T, H)))
     x4 = f32_to_bf16_bits(bits_f64(x) * 4.0)
@@ -86,6 +108,39 @@ def pin_rmsnorm():
     got = bits_f64(oracle.rmsnorm(x, gamma, 1e-6))
     ulp = np.abs(ref) * 2.0**-7
     assert np.all(np.abs(got - ref) <= ulp + 1e-30)
+
+
+def _rne(S, p):
+    """A positive Fraction rounded to p significant bits, nearest-even
+    (normal range)."""
+    from fractions import Fraction
+    e = S.numerator.bit_length() - S.denominator.bit_length()
+    if Fraction(2) ** e > S:
+        e -= 1                               # 2^e <= S < 2^(e+1)
+    q = Fraction(2) ** (e - p + 1)
+    n = S / q
+    m = n.numerator // n.denominator
+    rem = n - m
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and m % 2 == 1):
+        m += 1
+    return m * q
+
+
+def _sqrt_rne(S, p):
+    """sqrt of a positive Fraction, correctly rounded to p significant bits
+    (nearest-even), by integer square roots."""
+    from fractions import Fraction
+    eS = S.numerator.bit_length() - S.denominator.bit_length()
+    if Fraction(2) ** eS > S:
+        eS -= 1
+    e = eS // 2                              # 2^e <= sqrt(S) < 2^(e+1)
+    q = Fraction(2) ** (e - p + 1)
+    A = S / (q * q)                          # sqrt(S) / q = sqrt(A)
+    n = math.isqrt(A.numerator // A.denominator)
+    half = (Fraction(2 * n + 1, 2)) ** 2
+    if A > half or (A == half and n % 2 == 1):
+        n += 1
+    return n * q
 
 
 def _f32_rne(S):
@@ -455,6 +510,10 @@ MUTANTS = {
     "rms_no_eps": ("1.0f / sqrtf(mean + eps)", "1.0f / sqrtf(mean)"),
     "rms_r_in_double": ("1.0f / sqrtf(mean + eps)",
                         "(float)(1.0 / sqrt((double)mean + (double)eps))"),
+    "rms_gamma_into_r": ("float v = bf16_to_float(xr[h]) * r;\n            if (gamma)\n                v = v * bf16_to_float(gamma[h]);",
+                         "float v = bf16_to_float(xr[h]) * (gamma ? r * bf16_to_float(gamma[h]) : r);"),
+    "rms_one_rounding": ("float v = bf16_to_float(xr[h]) * r;\n            if (gamma)\n                v = v * bf16_to_float(gamma[h]);\n            xn[t * H + h] = bf16_from_double((double)v);",
+                         "double v = (double)bf16_to_float(xr[h]) * r;\n            if (gamma)\n                v = v * bf16_to_float(gamma[h]);\n            xn[t * H + h] = bf16_from_double(v);"),
     "rms_no_gamma": ("v = v * bf16_to_float(gamma[h]);", "v = v;"),
     "gate_transposed": ("wg[e * H + h], acc)", "wg[h * E + e], acc)"),
     "gate_no_bias": ("acc = acc + bias[e];", "acc = acc;"),
