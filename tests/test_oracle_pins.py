@@ -97,6 +97,20 @@ def pin_rmsnorm():
     gam[77] = 0x3F3A                            # 0.7265625
     got = oracle.rmsnorm(row, gam, float(ev))[0, 77]
     assert bits_f64(np.array([got]))[0] == float(want)
+    # mean = ss / H as a rounded fp32 division (a worked case at H = 384,
+    # eps = 0, exact arithmetic): 382 ones, 3.5625 and 3.984375; the output at
+    # 3.5625 is 3.453125, where ss times the rounded 1/384 gives 3.4375
+    av, bv = Fr(3.5625), Fr(3.984375)
+    ss = 382 + av * av + bv * bv
+    assert _rne(ss, 24) == ss
+    r = _rne(1 / _sqrt_rne(_rne(ss / 384, 24), 24), 24)
+    want = _rne(_rne(av * r, 24), 8)
+    r_recip = _rne(1 / _sqrt_rne(_rne(ss * _rne(Fr(1, 384), 24), 24), 24), 24)
+    assert _rne(_rne(av * r_recip, 24), 8) != want
+    row = np.full((1, 384), 0x3F80, dtype=np.uint16)
+    row[0, 5], row[0, 300] = 0x4064, 0x407F     # 3.5625, 3.984375
+    got = oracle.rmsnorm(row, np.full(384, 0x3F80, dtype=np.uint16), 0.0)[0, 5]
+    assert bits_f64(np.array([got]))[0] == float(want) == 3.453125
     # with eps = 0, scaling x by a power of two leaves xn bit-identical
     x = f32_to_bf16_bits(rng.standard_normal((T, H)))
     x4 = f32_to_bf16_bits(bits_f64(x) * 4.0)
@@ -507,6 +521,7 @@ MUTANTS = {
     "sumsq_square_shift": ("const int sh = 2 * (e ? e : 1) - 2;",
                            "const int sh = 2 * (e ? e : 1) - 1;"),
     "rms_no_mean": ("ss / (float)H", "ss"),
+    "rms_mean_by_reciprocal": ("ss / (float)H", "ss * (1.0f / (float)H)"),
     "rms_no_eps": ("1.0f / sqrtf(mean + eps)", "1.0f / sqrtf(mean)"),
     "rms_r_in_double": ("1.0f / sqrtf(mean + eps)",
                         "(float)(1.0 / sqrt((double)mean + (double)eps))"),
